@@ -1,0 +1,495 @@
+// kvq_api.cu -- the C ABI (include/kvq.h): cache lifetime, append, certified decode,
+// exports for tests, per-kernel timing.
+//
+// Orchestration of one decode call ("Runtime-Certified Bounded-Error Quantized
+// Attention", gist.science technical summary, Method §1-§3): the INT8 scoring pass with
+// top-K* selection, the mixed-precision pass with certificate and ladder plan, a second
+// mixed pass for groups that asked for rungs 1-2, the dense rungs 3-4, and the
+// certificate write-out -- five stream-ordered launches with no host round trip; every
+// data-dependent decision is taken on the device.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kvq.h"
+#include "kvq_common.cuh"
+#include "kvq_launch.h"
+
+using namespace kvq;
+
+namespace {
+
+thread_local std::string g_err;
+
+kvq_status fail(kvq_status s, const std::string& msg) {
+  g_err = msg;
+  return s;
+}
+kvq_status cuda_fail(cudaError_t e, const char* where) {
+  g_err = std::string(where) + ": " + cudaGetErrorString(e);
+  return KVQ_ERR_CUDA;
+}
+
+#define KVQ_CUDA(call, where)                      \
+  do {                                             \
+    cudaError_t e_ = (call);                       \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+  } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__global__ void fill_u32(uint32_t* p, uint32_t v, size_t n) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = v;
+}
+
+enum KernelId { K_SCORE = 0, K_MIX0, K_MIX1, K_DENSE, K_FINAL, K_APPEND, K_COUNT };
+const char* kKernelNames[K_COUNT] = {"score_select", "mixed_round0", "mixed_round1",
+                                     "dense_fallback", "finalize", "quantize_append"};
+
+}  // namespace
+
+struct kvq_cache {
+  kvq_config cfg;
+  int device = 0, num_sms = 0;
+  int B = 0, Hq = 0, Hkv = 0, n_rep = 0, BG = 0, nbmax = 0, L = 0;
+  long long cap = 0;  // tier-2 tokens per (sequence, KV head)
+  std::vector<int> n_tokens;
+  std::vector<int> tail_parity;
+  // tier 1, all layers in one allocation
+  char* t1 = nullptr;
+  size_t off_kc = 0, off_ks = 0, off_vc = 0, off_vsv = 0, off_eta = 0, off_vmin = 0, off_vmax = 0,
+         off_ksm = 0, off_vsm = 0, off_tail = 0, t1_layer = 0;
+  // tier 2: pinned, mapped host memory, per layer
+  std::vector<__half*> t2k_host, t2v_host;
+  std::vector<__half*> t2k_dev, t2v_dev;
+  // scratch
+  char* scr = nullptr;
+  float *shat = nullptr, *lse8 = nullptr, *delta = nullptr, *lse16 = nullptr;
+  uint8_t *sel = nullptr, *kprom0 = nullptr, *kprom1 = nullptr, *vprom1 = nullptr;
+  HeadState* hst = nullptr;
+  GroupState* gst = nullptr;
+  float *part = nullptr, *dpart = nullptr;
+  unsigned int* counters = nullptr;
+  __half *q_stage = nullptr, *out_stage = nullptr;
+  kvq_certificate* cert_stage = nullptr;
+  int32_t* level_stage = nullptr;
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_in = nullptr, ev_mirror = nullptr;
+  int debug = 0;
+  int last_layer = -1, last_nb = 0;
+  // profiling
+  struct Rec { int id; cudaEvent_t a, b; };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> ev_pool;
+  double prof_ms[K_COUNT] = {0};
+  long long prof_n[K_COUNT] = {0};
+};
+
+namespace {
+
+int8_t* layer_kc(kvq_cache* c, int l) { return reinterpret_cast<int8_t*>(c->t1 + c->t1_layer * l + c->off_kc); }
+__half* layer_ks(kvq_cache* c, int l) { return reinterpret_cast<__half*>(c->t1 + c->t1_layer * l + c->off_ks); }
+uint8_t* layer_vc(kvq_cache* c, int l) { return reinterpret_cast<uint8_t*>(c->t1 + c->t1_layer * l + c->off_vc); }
+__half2* layer_vsv(kvq_cache* c, int l) { return reinterpret_cast<__half2*>(c->t1 + c->t1_layer * l + c->off_vsv); }
+float* layer_eta(kvq_cache* c, int l) { return reinterpret_cast<float*>(c->t1 + c->t1_layer * l + c->off_eta); }
+uint32_t* layer_vmin(kvq_cache* c, int l) { return reinterpret_cast<uint32_t*>(c->t1 + c->t1_layer * l + c->off_vmin); }
+uint32_t* layer_vmax(kvq_cache* c, int l) { return reinterpret_cast<uint32_t*>(c->t1 + c->t1_layer * l + c->off_vmax); }
+uint32_t* layer_ksm(kvq_cache* c, int l) { return reinterpret_cast<uint32_t*>(c->t1 + c->t1_layer * l + c->off_ksm); }
+uint32_t* layer_vsm(kvq_cache* c, int l) { return reinterpret_cast<uint32_t*>(c->t1 + c->t1_layer * l + c->off_vsm); }
+// partial-block buffers: [parity][K|V][BG][64][128]
+__half* layer_tail(kvq_cache* c, int l, int parity, int kv) {
+  __half* base = reinterpret_cast<__half*>(c->t1 + c->t1_layer * l + c->off_tail);
+  return base + ((size_t)(parity * 2 + kv) * c->BG) * BLK * D;
+}
+
+LayerAppend append_view(kvq_cache* c, int l) {
+  LayerAppend a;
+  a.BG = c->BG;
+  a.nbmax = c->nbmax;
+  a.kc = layer_kc(c, l); a.ks = layer_ks(c, l); a.vc = layer_vc(c, l); a.vsv = layer_vsv(c, l);
+  a.eta = layer_eta(c, l); a.vmin = layer_vmin(c, l); a.vmax = layer_vmax(c, l);
+  a.kscale_max = layer_ksm(c, l); a.vscale_max = layer_vsm(c, l);
+  const int p = c->tail_parity[l];
+  a.tail_k_in = layer_tail(c, l, p, 0); a.tail_v_in = layer_tail(c, l, p, 1);
+  a.tail_k_out = layer_tail(c, l, 1 - p, 0); a.tail_v_out = layer_tail(c, l, 1 - p, 1);
+  return a;
+}
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+cudaEvent_t pooled_event(kvq_cache* c) {
+  if (!c->ev_pool.empty()) {
+    cudaEvent_t e = c->ev_pool.back();
+    c->ev_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e;
+  cudaEventCreate(&e);
+  return e;
+}
+
+struct KernelScope {
+  kvq_cache* c;
+  int id;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr;
+  KernelScope(kvq_cache* c_, int id_, cudaStream_t st_) : c(c_), id(id_), st(st_) {
+    if (c->debug & KVQ_DEBUG_PROFILE) {
+      a = pooled_event(c);
+      cudaEventRecord(a, st);
+    }
+  }
+  cudaError_t done(cudaError_t e) {
+    if (e != cudaSuccess) return e;
+    if (c->debug & KVQ_DEBUG_PROFILE) {
+      cudaEvent_t b = pooled_event(c);
+      cudaEventRecord(b, st);
+      c->recs.push_back({id, a, b});
+    }
+    if (c->debug & KVQ_DEBUG_SYNC) {
+      e = cudaStreamSynchronize(st);
+      if (e == cudaSuccess) e = cudaGetLastError();
+    }
+    return e;
+  }
+};
+
+void free_all(kvq_cache* c) {
+  if (!c) return;
+  cudaDeviceSynchronize();
+  for (auto& r : c->recs) { c->ev_pool.push_back(r.a); c->ev_pool.push_back(r.b); }
+  for (auto e : c->ev_pool) cudaEventDestroy(e);
+  if (c->t1) cudaFree(c->t1);
+  if (c->scr) cudaFree(c->scr);
+  for (auto p : c->t2k_host) if (p) cudaFreeHost(p);
+  for (auto p : c->t2v_host) if (p) cudaFreeHost(p);
+  if (c->side) cudaStreamDestroy(c->side);
+  if (c->ev_in) cudaEventDestroy(c->ev_in);
+  if (c->ev_mirror) cudaEventDestroy(c->ev_mirror);
+  delete c;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_last_error(void) { return g_err.c_str(); }
+
+kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
+  if (!cfg || !out) return fail(KVQ_ERR_INVALID, "kvq_cache_create: NULL argument");
+  *out = nullptr;
+  const kvq_config& k = *cfg;
+  if (k.head_dim != D) return fail(KVQ_ERR_INVALID, "head_dim must be 128");
+  if (k.block_tokens != BLK) return fail(KVQ_ERR_INVALID, "block_tokens must be 64");
+  if (k.value_group != VG) return fail(KVQ_ERR_INVALID, "value_group must be 32");
+  if (k.n_layers < 1 || k.batch < 1 || k.n_kv_heads < 1 || k.n_q_heads < 1 || k.max_ctx < 1)
+    return fail(KVQ_ERR_INVALID, "n_layers, batch, heads and max_ctx must be >= 1");
+  if (k.n_q_heads % k.n_kv_heads != 0 || k.n_q_heads / k.n_kv_heads > MAXREP)
+    return fail(KVQ_ERR_INVALID, "n_q_heads / n_kv_heads must be an integer in 1..4");
+  if (k.rank_positions < 1) return fail(KVQ_ERR_INVALID, "rank_positions must be >= 1");
+  if (!(k.l4_head_fraction > 0.f && k.l4_head_fraction <= 1.f))
+    return fail(KVQ_ERR_INVALID, "l4_head_fraction must be in (0, 1]");
+
+  kvq_cache* c = new kvq_cache();
+  c->cfg = k;
+  cudaGetDevice(&c->device);
+  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  c->B = k.batch; c->Hq = k.n_q_heads; c->Hkv = k.n_kv_heads; c->n_rep = k.n_q_heads / k.n_kv_heads;
+  c->BG = c->B * c->Hkv; c->L = k.n_layers;
+  c->nbmax = k.max_ctx / BLK;
+  c->cap = (long long)((k.max_ctx + BLK - 1) / BLK) * BLK;
+  c->n_tokens.assign(c->L, 0);
+  c->tail_parity.assign(c->L, 0);
+
+  // ---- tier 1 ----
+  const size_t BG = c->BG, nbm = std::max(1, c->nbmax);
+  size_t o = 0;
+  c->off_kc = o;   o = align_up(o + BG * nbm * KC_BYTES, 256);
+  c->off_ks = o;   o = align_up(o + BG * nbm * D * 2, 256);
+  c->off_vc = o;   o = align_up(o + BG * nbm * VC_BYTES, 256);
+  c->off_vsv = o;  o = align_up(o + BG * nbm * VSV_WORDS * 4, 256);
+  c->off_eta = o;  o = align_up(o + BG * nbm * 4, 256);
+  c->off_vmin = o; o = align_up(o + BG * D * 4, 256);
+  c->off_vmax = o; o = align_up(o + BG * D * 4, 256);
+  c->off_ksm = o;  o = align_up(o + BG * 4, 256);
+  c->off_vsm = o;  o = align_up(o + BG * 4, 256);
+  c->off_tail = o; o = align_up(o + 4 * BG * BLK * D * 2, 256);
+  c->t1_layer = o;
+  if (cudaMalloc(&c->t1, c->t1_layer * c->L) != cudaSuccess) {
+    cudaGetLastError();
+    free_all(c);
+    return fail(KVQ_ERR_OOM, "tier-1 device allocation failed");
+  }
+  cudaMemset(c->t1, 0, c->t1_layer * c->L);
+  for (int l = 0; l < c->L; ++l) {
+    fill_u32<<<64, 256>>>(layer_vmin(c, l), 0xFF800000u, BG * D);  // encoding of +inf
+    fill_u32<<<64, 256>>>(layer_vmax(c, l), 0x007FFFFFu, BG * D);  // encoding of -inf
+  }
+
+  // ---- tier 2: pinned, mapped host memory ----
+  const size_t t2bytes = (size_t)BG * c->cap * D * sizeof(__half);
+  c->t2k_host.assign(c->L, nullptr); c->t2v_host.assign(c->L, nullptr);
+  c->t2k_dev.assign(c->L, nullptr); c->t2v_dev.assign(c->L, nullptr);
+  for (int l = 0; l < c->L; ++l) {
+    for (int kv = 0; kv < 2; ++kv) {
+      void* h = nullptr;
+      if (cudaHostAlloc(&h, t2bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+        cudaGetLastError();
+        free_all(c);
+        return fail(KVQ_ERR_HOST_OOM, "tier-2 pinned host allocation failed");
+      }
+      void* d = nullptr;
+      if (cudaHostGetDevicePointer(&d, h, 0) != cudaSuccess) {
+        cudaGetLastError();
+        (kv ? c->t2v_host : c->t2k_host)[l] = static_cast<__half*>(h);
+        free_all(c);
+        return fail(KVQ_ERR_HOST_OOM, "tier-2 memory is not mapped into the device");
+      }
+      (kv ? c->t2v_host : c->t2k_host)[l] = static_cast<__half*>(h);
+      (kv ? c->t2v_dev : c->t2k_dev)[l] = static_cast<__half*>(d);
+    }
+  }
+
+  // ---- scratch ----
+  const size_t HQ = (size_t)c->B * c->Hq;
+  const size_t NCH = nbm / CHUNK + 1;
+  o = 0;
+  const size_t s_shat = o;  o = align_up(o + HQ * nbm * BLK * 4, 256);
+  const size_t s_lse8 = o;  o = align_up(o + HQ * nbm * 4, 256);
+  const size_t s_delta = o; o = align_up(o + HQ * nbm * 4, 256);
+  const size_t s_lse16 = o; o = align_up(o + HQ * nbm * 4, 256);
+  const size_t s_sel = o;   o = align_up(o + HQ * nbm, 256);
+  const size_t s_kp0 = o;   o = align_up(o + BG * nbm, 256);
+  const size_t s_kp1 = o;   o = align_up(o + BG * nbm, 256);
+  const size_t s_vp1 = o;   o = align_up(o + BG * nbm, 256);
+  const size_t s_hst = o;   o = align_up(o + HQ * sizeof(HeadState), 256);
+  const size_t s_gst = o;   o = align_up(o + BG * sizeof(GroupState), 256);
+  const size_t s_part = o;  o = align_up(o + BG * NCH * MAXREP * (D + 4) * 4, 256);
+  const size_t s_dpart = o; o = align_up(o + BG * NCH * MAXREP * (D + 4) * 4, 256);
+  const size_t s_cnt = o;   o = align_up(o + (CNT_GROUP_BASE + 4 * BG) * 4, 256);
+  const size_t s_q = o;     o = align_up(o + HQ * D * 2, 256);
+  const size_t s_out = o;   o = align_up(o + HQ * D * 2, 256);
+  const size_t s_cert = o;  o = align_up(o + HQ * sizeof(kvq_certificate), 256);
+  const size_t s_lvl = o;   o = align_up(o + c->B * 4, 256);
+  if (cudaMalloc(&c->scr, o) != cudaSuccess) {
+    cudaGetLastError();
+    free_all(c);
+    return fail(KVQ_ERR_OOM, "scratch device allocation failed");
+  }
+  cudaMemset(c->scr, 0, o);
+  c->shat = reinterpret_cast<float*>(c->scr + s_shat);
+  c->lse8 = reinterpret_cast<float*>(c->scr + s_lse8);
+  c->delta = reinterpret_cast<float*>(c->scr + s_delta);
+  c->lse16 = reinterpret_cast<float*>(c->scr + s_lse16);
+  c->sel = reinterpret_cast<uint8_t*>(c->scr + s_sel);
+  c->kprom0 = reinterpret_cast<uint8_t*>(c->scr + s_kp0);
+  c->kprom1 = reinterpret_cast<uint8_t*>(c->scr + s_kp1);
+  c->vprom1 = reinterpret_cast<uint8_t*>(c->scr + s_vp1);
+  c->hst = reinterpret_cast<HeadState*>(c->scr + s_hst);
+  c->gst = reinterpret_cast<GroupState*>(c->scr + s_gst);
+  c->part = reinterpret_cast<float*>(c->scr + s_part);
+  c->dpart = reinterpret_cast<float*>(c->scr + s_dpart);
+  c->counters = reinterpret_cast<unsigned int*>(c->scr + s_cnt);
+  c->q_stage = reinterpret_cast<__half*>(c->scr + s_q);
+  c->out_stage = reinterpret_cast<__half*>(c->scr + s_out);
+  c->cert_stage = reinterpret_cast<kvq_certificate*>(c->scr + s_cert);
+  c->level_stage = reinterpret_cast<int32_t*>(c->scr + s_lvl);
+
+  if (cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_in, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&c->ev_mirror, cudaEventDisableTiming) != cudaSuccess) {
+    cudaError_t e = cudaGetLastError();
+    free_all(c);
+    return cuda_fail(e, "kvq_cache_create: stream/event");
+  }
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    free_all(c);
+    return cuda_fail(e, "kvq_cache_create");
+  }
+  *out = c;
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_destroy(kvq_cache* cache) {
+  free_all(cache);
+  return KVQ_OK;
+}
+
+kvq_status kvq_set_debug(kvq_cache* c, int flags) {
+  if (!c) return fail(KVQ_ERR_INVALID, "kvq_set_debug: NULL cache");
+  c->debug = flags;
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_length(const kvq_cache* c, int layer, int* n) {
+  if (!c || !n) return fail(KVQ_ERR_INVALID, "kvq_cache_length: NULL argument");
+  if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, "layer out of range");
+  *n = c->n_tokens[layer];
+  return KVQ_OK;
+}
+
+kvq_status kvq_append(kvq_cache* c, int layer, const void* k, const void* v, int n, void* stream) {
+  if (!c) return fail(KVQ_ERR_INVALID, "kvq_append: NULL cache");
+  if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, "kvq_append: layer out of range");
+  if (n < 0) return fail(KVQ_ERR_INVALID, "kvq_append: n_tokens < 0");
+  if (n == 0) return KVQ_OK;
+  if (!k || !v) return fail(KVQ_ERR_INVALID, "kvq_append: NULL k or v");
+  if (!is_device_ptr(k) || !is_device_ptr(v))
+    return fail(KVQ_ERR_INVALID, "kvq_append: k and v must be device memory");
+  const int pos = c->n_tokens[layer];
+  if ((long long)pos + n > c->cfg.max_ctx)
+    return fail(KVQ_ERR_CAPACITY, "kvq_append: cache capacity (max_ctx) exceeded");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // tier-2 mirror on the side stream, overlapped with quantisation
+  KVQ_CUDA(cudaEventRecord(c->ev_in, st), "kvq_append: event");
+  KVQ_CUDA(cudaStreamWaitEvent(c->side, c->ev_in, 0), "kvq_append: wait");
+  const size_t dpitch = (size_t)c->cap * D * sizeof(__half);
+  const size_t width = (size_t)n * D * sizeof(__half);
+  KVQ_CUDA(cudaMemcpy2DAsync(c->t2k_host[layer] + (size_t)pos * D, dpitch, k, width, width, c->BG,
+                             cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror K");
+  KVQ_CUDA(cudaMemcpy2DAsync(c->t2v_host[layer] + (size_t)pos * D, dpitch, v, width, width, c->BG,
+                             cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror V");
+  KVQ_CUDA(cudaEventRecord(c->ev_mirror, c->side), "kvq_append: event");
+  {
+    KernelScope ks(c, K_APPEND, st);
+    KVQ_CUDA(ks.done(launch_append(append_view(c, layer), k, v, n, pos, st)), "quantize_append");
+  }
+  KVQ_CUDA(cudaStreamWaitEvent(st, c->ev_mirror, 0), "kvq_append: join");
+  c->n_tokens[layer] = pos + n;
+  c->tail_parity[layer] ^= 1;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q, float tau, float eps,
+                                void* out, kvq_certificate* cert, int32_t* ladder_level,
+                                void* stream) {
+  if (!c) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: NULL cache");
+  if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: layer out of range");
+  if (!q || !out) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: NULL q or out");
+  if (!(tau > 0.f && tau <= 1.f)) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: tau_cov must be in (0, 1]");
+  if (!(eps >= 0.f)) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: eps must be >= 0");
+  const int N = c->n_tokens[layer];
+  if (N == 0) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: layer holds no tokens");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t HQ = (size_t)c->B * c->Hq;
+  const bool q_dev = is_device_ptr(q), out_dev = is_device_ptr(out);
+  const bool cert_dev = cert && is_device_ptr(cert);
+  const bool lvl_dev = ladder_level && is_device_ptr(ladder_level);
+  bool host_any = !q_dev || !out_dev || (cert && !cert_dev) || (ladder_level && !lvl_dev);
+  const __half* qd = static_cast<const __half*>(q);
+  if (!q_dev) {
+    KVQ_CUDA(cudaMemcpyAsync(c->q_stage, q, HQ * D * 2, cudaMemcpyHostToDevice, st), "stage q");
+    qd = c->q_stage;
+  }
+  __half* od = out_dev ? static_cast<__half*>(out) : c->out_stage;
+  kvq_certificate* cd = cert_dev ? cert : c->cert_stage;
+  int32_t* ld = lvl_dev ? ladder_level : c->level_stage;
+
+  LayerView V;
+  V.B = c->B; V.Hq = c->Hq; V.Hkv = c->Hkv; V.n_rep = c->n_rep; V.BG = c->BG;
+  V.nb = N / BLK; V.n_tail = N % BLK; V.nbmax = std::max(1, c->nbmax); V.cap = c->cap;
+  V.kc = layer_kc(c, layer); V.ks = layer_ks(c, layer); V.vc = layer_vc(c, layer);
+  V.vsv = layer_vsv(c, layer); V.eta = layer_eta(c, layer);
+  V.vmin = layer_vmin(c, layer); V.vmax = layer_vmax(c, layer);
+  V.kscale_max = layer_ksm(c, layer); V.vscale_max = layer_vsm(c, layer);
+  const int p = c->tail_parity[layer];
+  V.tail_k = layer_tail(c, layer, p, 0); V.tail_v = layer_tail(c, layer, p, 1);
+  V.t2k = c->t2k_dev[layer]; V.t2v = c->t2v_dev[layer];
+  V.q = qd; V.out = od; V.tau = tau; V.eps = eps;
+  V.l4_frac = c->cfg.l4_head_fraction; V.rank_positions = c->cfg.rank_positions; V.debug = c->debug;
+  V.shat = c->shat; V.lse8 = c->lse8; V.delta = c->delta; V.lse16 = c->lse16; V.sel = c->sel;
+  V.kprom0 = c->kprom0; V.kprom1 = c->kprom1; V.vprom1 = c->vprom1;
+  V.hst = c->hst; V.gst = c->gst; V.part = c->part; V.dpart = c->dpart; V.counters = c->counters;
+
+  const bool all_dense = (tau >= 1.f) || (c->debug & KVQ_DEBUG_FORCE_DENSE);
+  if (!all_dense) {
+    { KernelScope s(c, K_SCORE, st); KVQ_CUDA(s.done(launch_score_select(V, score_grid(c->num_sms), st)), "score_select"); }
+    { KernelScope s(c, K_MIX0, st); KVQ_CUDA(s.done(launch_mixed(V, 0, mixed_grid(c->num_sms), st)), "mixed_round0"); }
+    { KernelScope s(c, K_MIX1, st); KVQ_CUDA(s.done(launch_mixed(V, 1, mixed_grid(c->num_sms), st)), "mixed_round1"); }
+  }
+  { KernelScope s(c, K_DENSE, st); KVQ_CUDA(s.done(launch_dense(V, all_dense ? 1 : 0, dense_grid(c->num_sms), st)), "dense_fallback"); }
+  { KernelScope s(c, K_FINAL, st); KVQ_CUDA(s.done(launch_finalize(V, cd, ld, st)), "finalize"); }
+
+  if (!out_dev) KVQ_CUDA(cudaMemcpyAsync(out, od, HQ * D * 2, cudaMemcpyDeviceToHost, st), "copy out");
+  if (cert && !cert_dev) KVQ_CUDA(cudaMemcpyAsync(cert, cd, HQ * sizeof(kvq_certificate), cudaMemcpyDeviceToHost, st), "copy cert");
+  if (ladder_level && !lvl_dev) KVQ_CUDA(cudaMemcpyAsync(ladder_level, ld, c->B * 4, cudaMemcpyDeviceToHost, st), "copy level");
+  if (host_any) KVQ_CUDA(cudaStreamSynchronize(st), "kvq_decode_attention: sync");
+  c->last_layer = layer;
+  c->last_nb = all_dense ? -1 : V.nb;
+  return KVQ_OK;
+}
+
+kvq_status kvq_export_tier1(kvq_cache* c, int layer, void* kc, void* ks, void* vc, void* vs,
+                            void* vo, float* eta, float* vmin, float* vmax, void* stream) {
+  if (!c) return fail(KVQ_ERR_INVALID, "kvq_export_tier1: NULL cache");
+  if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, "kvq_export_tier1: layer out of range");
+  const int nb = c->n_tokens[layer] / BLK;
+  KVQ_CUDA(launch_export_tier1(append_view(c, layer), nb, kc, ks, vc, vs, vo, eta, vmin, vmax,
+                               static_cast<cudaStream_t>(stream)), "export_tier1");
+  return KVQ_OK;
+}
+
+kvq_status kvq_export_decode_state(kvq_cache* c, uint8_t* sel, uint8_t* kprom0, uint8_t* kprom1,
+                                   uint8_t* vprom1, float* lse8, float* delta, void* stream) {
+  if (!c) return fail(KVQ_ERR_INVALID, "kvq_export_decode_state: NULL cache");
+  if (c->last_layer < 0 || c->last_nb < 0)
+    return fail(KVQ_ERR_INVALID, "kvq_export_decode_state: no certified decode call yet");
+  const int nb = c->last_nb;
+  if (nb == 0) return KVQ_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t HQ = (size_t)c->B * c->Hq, nbm = std::max(1, c->nbmax);
+  auto cp = [&](void* dst, const void* src, size_t elem, size_t rows) -> cudaError_t {
+    if (!dst) return cudaSuccess;
+    return cudaMemcpy2DAsync(dst, nb * elem, src, nbm * elem, nb * elem, rows, cudaMemcpyDeviceToDevice, st);
+  };
+  KVQ_CUDA(cp(sel, c->sel, 1, HQ), "export sel");
+  KVQ_CUDA(cp(kprom0, c->kprom0, 1, c->BG), "export kprom0");
+  KVQ_CUDA(cp(kprom1, c->kprom1, 1, c->BG), "export kprom1");
+  KVQ_CUDA(cp(vprom1, c->vprom1, 1, c->BG), "export vprom1");
+  KVQ_CUDA(cp(lse8, c->lse8, 4, HQ), "export lse8");
+  KVQ_CUDA(cp(delta, c->delta, 4, HQ), "export delta");
+  return KVQ_OK;
+}
+
+kvq_status kvq_profile_read(kvq_cache* c, kvq_kernel_stat* stats, int max, int* n, int reset) {
+  if (!c || !n || (max > 0 && !stats)) return fail(KVQ_ERR_INVALID, "kvq_profile_read: NULL argument");
+  for (auto& r : c->recs) {
+    KVQ_CUDA(cudaEventSynchronize(r.b), "kvq_profile_read: sync");
+    float ms = 0.f;
+    KVQ_CUDA(cudaEventElapsedTime(&ms, r.a, r.b), "kvq_profile_read: elapsed");
+    c->prof_ms[r.id] += ms;
+    c->prof_n[r.id] += 1;
+    c->ev_pool.push_back(r.a);
+    c->ev_pool.push_back(r.b);
+  }
+  c->recs.clear();
+  int w = 0;
+  for (int i = 0; i < K_COUNT && w < max; ++i) {
+    if (c->prof_n[i] == 0) continue;
+    std::memset(&stats[w], 0, sizeof(kvq_kernel_stat));
+    std::strncpy(stats[w].name, kKernelNames[i], sizeof(stats[w].name) - 1);
+    stats[w].launches = c->prof_n[i];
+    stats[w].total_ms = c->prof_ms[i];
+    ++w;
+  }
+  *n = w;
+  if (reset) {
+    for (int i = 0; i < K_COUNT; ++i) { c->prof_ms[i] = 0; c->prof_n[i] = 0; }
+  }
+  return KVQ_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,285 @@
+// kvq_dense.cu -- rungs 3 and 4 of the fallback ladder: exact dense FP16 attention over
+// tier 2, and the final certificate write-out.
+//
+// "Runtime-Certified Bounded-Error Quantized Attention" (gist.science technical summary),
+// Method §1 (fallback pages FP16 data in from tier 2 and runs exact dense attention for
+// the affected head or layer), Method §3 (rung 3: per-head dense when the ranking check
+// fails; rung 4: the whole layer dense) and Contributions ("deterministic recovery":
+// O_dense is returned when the certified bound cannot be met).
+// Readings: a head that failed its ranking check, or whose bound still exceeds eps after
+// rungs 1-2, is recomputed densely (rung 3); when at least l4_head_fraction of a
+// sequence's query heads are at rung 3, or tau_cov = 1, every head of that sequence is
+// (rung 4).  Dense heads report E_key = E_val = 0.
+//
+// The kernel reads FP16 keys and values straight from pinned host memory over the host
+// link (split-K over 16-block chunks, online softmax per chunk), which is the bound of
+// this path; the CUDA cores keep up with the link, so no tensor-core tiling is used.
+#include "kvq_common.cuh"
+#include "kvq_launch.h"
+#include "kvq.h"
+
+namespace kvq {
+
+namespace {
+
+struct __align__(16) DenseSmem {
+  __half kbuf[BLK][D + 8];
+  __half vbuf[BLK][D];
+  float qf[MAXREP][D];
+  float s[MAXREP][BLK];
+  float red[MAXREP][4];
+  int item;
+  int mask;
+  int is_last;
+};
+
+__device__ __forceinline__ size_t head_row(const LayerView& V, int b, int g, int r) {
+  return (size_t)b * V.Hq + (size_t)g * V.n_rep + r;
+}
+
+// Heads of group hs that need dense attention (bit r = head slot r).
+__device__ int dense_mask(const LayerView& V, int hs, int all_dense) {
+  const int b = hs / V.Hkv, g = hs % V.Hkv;
+  const int full = (1 << V.n_rep) - 1;
+  if (all_dense) return full;
+  int n3 = 0;
+  for (int h = 0; h < V.Hq; ++h) n3 += (V.hst[(size_t)b * V.Hq + h].level1 == 3);
+  if ((float)n3 >= V.l4_frac * (float)V.Hq) return full;
+  int m = 0;
+  for (int r = 0; r < V.n_rep; ++r)
+    if (V.hst[head_row(V, b, g, r)].level1 == 3) m |= 1 << r;
+  return m;
+}
+
+__device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dense, DenseSmem& sm) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = hs / V.Hkv, g = hs % V.Hkv;
+  const int nch = max(1, (V.nb + CHUNK - 1) / CHUNK);
+  const int NCH = V.nbmax / CHUNK + 1;
+  // partial block exact scores (warp = head slot)
+  if (warp < V.n_rep) {
+    const __half* q = V.q + head_row(V, b, g, warp) * D;
+    for (int t = lane; t < BLK; t += 32) {
+      float s = -INFINITY;
+      if (t < V.n_tail) {
+        const __half* k = V.tail_k + ((size_t)hs * BLK + t) * D;
+        s = 0.f;
+        for (int c = 0; c < D; c += 2) {
+          const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(k + c));
+          const float2 qq = __half22float2(*reinterpret_cast<const __half2*>(q + c));
+          s = fmaf(qq.x, kk.x, s);
+          s = fmaf(qq.y, kk.y, s);
+        }
+        s *= INV_SQRT_D;
+      }
+      sm.s[warp][t] = s;
+    }
+  }
+  __syncthreads();
+  for (int r = 0; r < V.n_rep; ++r) {
+    if (!(mask >> r & 1)) continue;
+    // global max over chunk maxima and the partial block
+    float M = -INFINITY;
+    for (int c = 0; c < nch && V.nb > 0; ++c)
+      M = fmaxf(M, V.dpart[(((size_t)hs * NCH + c) * MAXREP + r) * (D + 4) + D]);
+    for (int t = 0; t < V.n_tail; ++t) M = fmaxf(M, sm.s[r][t]);
+    float L = 0.f, a = 0.f;
+    for (int c = 0; c < nch && V.nb > 0; ++c) {
+      const float* pp = V.dpart + (((size_t)hs * NCH + c) * MAXREP + r) * (D + 4);
+      const float w = expf(pp[D] - M);
+      L += pp[D + 1] * w;
+      a += pp[tid] * w;
+    }
+    for (int t = 0; t < V.n_tail; ++t) {
+      const float p = expf(sm.s[r][t] - M);
+      L += p;
+      a += p * __half2float(V.tail_v[((size_t)hs * BLK + t) * D + tid]);
+    }
+    V.out[head_row(V, b, g, r) * D + tid] = __float2half_rn(a / L);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int n3 = 0;
+    if (!all_dense)
+      for (int h = 0; h < V.Hq; ++h) n3 += (V.hst[(size_t)b * V.Hq + h].level1 == 3);
+    const bool l4 = all_dense || ((float)n3 >= V.l4_frac * (float)V.Hq);
+    for (int r = 0; r < V.n_rep; ++r) {
+      HeadState& h = V.hst[head_row(V, b, g, r)];
+      if (all_dense) {
+        h.M = 0.f; h.lse_int8 = 0.f; h.tail_lse = 0.f;
+        h.k_star = V.nb; h.rank_ok = 1; h.planned = 0; h.level1 = 0; h.n_vprom = 0;
+      }
+      if (mask >> r & 1) {
+        h.level = l4 ? 4 : 3;
+        h.e_key = 0.f;
+        h.e_val = 0.f;
+      }
+    }
+    GroupState& gs = V.gst[hs];
+    if (all_dense) {
+      gs.need_round1 = 0; gs.n_kprom0 = 0; gs.n_kprom1 = 0; gs.n_vprom1 = 0; gs.bytes = 0;
+    }
+    gs.need_dense = 1;
+    gs.bytes += 2LL * V.nb * F16_BLOCK_BYTES;
+  }
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) {
+  __shared__ DenseSmem sm;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nch = max(1, (V.nb + CHUNK - 1) / CHUNK);
+  const int NCH = V.nbmax / CHUNK + 1;
+  const int total = V.BG * nch;
+  unsigned int* cnt_group = V.counters + CNT_GROUP_BASE + 3 * V.BG;
+  int cur_hs = -1;
+
+  for (;;) {
+    if (tid == 0) {
+      const int it = (int)atomicAdd(&V.counters[CNT_DENSE_Q], 1u);
+      sm.item = it;
+      sm.mask = (it < total) ? dense_mask(V, it / nch, all_dense) : 0;
+    }
+    __syncthreads();
+    const int item = sm.item;
+    const int mask = sm.mask;
+    if (item >= total) break;
+    if (mask == 0) { __syncthreads(); continue; }
+    const int hs = item / nch, ch = item % nch;
+    const int b = hs / V.Hkv, g = hs % V.Hkv;
+    if (hs != cur_hs) {
+      cur_hs = hs;
+      for (int i = tid; i < MAXREP * D; i += blockDim.x) {
+        const int r = i / D, c = i % D;
+        sm.qf[r][c] = (r < V.n_rep) ? __half2float(V.q[head_row(V, b, g, r) * D + c]) : 0.f;
+      }
+      __syncthreads();
+    }
+    // online softmax over the chunk; thread = channel, all four head slots
+    float m[MAXREP], l[MAXREP], a[MAXREP];
+    for (int r = 0; r < MAXREP; ++r) { m[r] = -INFINITY; l[r] = 0.f; a[r] = 0.f; }
+    const int blk_end = min(V.nb, (ch + 1) * CHUNK);
+    for (int blk = ch * CHUNK; blk < blk_end; ++blk) {
+      const size_t src = ((size_t)hs * V.cap + (size_t)blk * BLK) * D;
+      {
+        const uint4* ks = reinterpret_cast<const uint4*>(V.t2k + src);
+        const uint4* vs = reinterpret_cast<const uint4*>(V.t2v + src);
+        for (int i = tid; i < BLK * D / 8; i += blockDim.x) {
+          const int row = i >> 4, col = (i & 15) * 8;
+          *reinterpret_cast<uint4*>(&sm.kbuf[row][col]) = ks[i];
+          *reinterpret_cast<uint4*>(&sm.vbuf[row][col]) = vs[i];
+        }
+      }
+      __syncthreads();
+      {
+        const int t = tid & 63, rp = (tid >> 6) * 2;
+        float s0 = 0.f, s1 = 0.f;
+        for (int c = 0; c < D; c += 8) {
+          const uint4 kv = *reinterpret_cast<const uint4*>(&sm.kbuf[t][c]);
+          const __half2* k2 = reinterpret_cast<const __half2*>(&kv);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float2 kf = __half22float2(k2[j]);
+            s0 = fmaf(sm.qf[rp][c + 2 * j], kf.x, s0);
+            s0 = fmaf(sm.qf[rp][c + 2 * j + 1], kf.y, s0);
+            s1 = fmaf(sm.qf[rp + 1][c + 2 * j], kf.x, s1);
+            s1 = fmaf(sm.qf[rp + 1][c + 2 * j + 1], kf.y, s1);
+          }
+        }
+        sm.s[rp][t] = s0 * INV_SQRT_D;
+        sm.s[rp + 1][t] = s1 * INV_SQRT_D;
+      }
+      __syncthreads();
+      {  // block max per head, then p_t = exp(s_t - m_new) in place (warp = head slot)
+        const int r = warp;
+        const float x0 = sm.s[r][lane], x1 = sm.s[r][lane + 32];
+        const float mn = fmaxf(m[r], warp_max(fmaxf(x0, x1)));
+        const float p0 = expf(x0 - mn), p1 = expf(x1 - mn);
+        sm.s[r][lane] = p0;
+        sm.s[r][lane + 32] = p1;
+        const float ls = warp_sum(p0 + p1);
+        if (lane == 0) { sm.red[r][0] = mn; sm.red[r][1] = ls; }
+      }
+      __syncthreads();
+      for (int r = 0; r < V.n_rep; ++r) {
+        const float mn = sm.red[r][0];
+        const float sc = (m[r] == -INFINITY) ? 0.f : expf(m[r] - mn);
+        float as = 0.f;
+        for (int t = 0; t < BLK; ++t) as = fmaf(sm.s[r][t], __half2float(sm.vbuf[t][tid]), as);
+        l[r] = l[r] * sc + sm.red[r][1];
+        a[r] = a[r] * sc + as;
+        m[r] = mn;
+      }
+      __syncthreads();
+    }
+    float* pp = V.dpart + (((size_t)hs * NCH + ch) * MAXREP) * (D + 4);
+    for (int r = 0; r < V.n_rep; ++r) {
+      pp[r * (D + 4) + tid] = a[r];
+      if (tid == 0) {
+        pp[r * (D + 4) + D] = m[r];
+        pp[r * (D + 4) + D + 1] = l[r];
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      const unsigned int old = atomicAdd(&cnt_group[hs], 1u);
+      sm.is_last = (old == (unsigned int)(nch - 1));
+    }
+    __syncthreads();
+    if (sm.is_last) {
+      __threadfence();
+      combine_dense(V, hs, mask, all_dense, sm);
+      if (tid == 0) cnt_group[hs] = 0u;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const unsigned int old = atomicAdd(&V.counters[CNT_DENSE_EXIT], 1u);
+    if (old == gridDim.x - 1) {
+      V.counters[CNT_DENSE_Q] = 0u;
+      V.counters[CNT_DENSE_EXIT] = 0u;
+    }
+  }
+}
+
+// Final certificates and per-sequence ladder level; one CTA per sequence.
+__global__ void finalize_kernel(LayerView V, kvq_certificate* cert, int32_t* level) {
+  const int b = blockIdx.x;
+  __shared__ int mx;
+  if (threadIdx.x == 0) mx = 0;
+  __syncthreads();
+  for (int h = threadIdx.x; h < V.Hq; h += blockDim.x) {
+    HeadState& s = V.hst[(size_t)b * V.Hq + h];
+    if (s.level < 0) s.level = s.level1;
+    const int g = h / V.n_rep;
+    kvq_certificate c;
+    c.e_key = s.e_key;
+    c.e_val = s.e_val;
+    c.rank_ok = s.rank_ok;
+    c.level = s.level;
+    c.k_star = s.k_star;
+    c.n_val_promoted = s.n_vprom;
+    c.promoted_bytes = V.gst[(size_t)b * V.Hkv + g].bytes;
+    if (cert) cert[(size_t)b * V.Hq + h] = c;
+    atomicMax(&mx, s.level);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && level) level[b] = mx;
+}
+
+int dense_grid(int num_sms) { return num_sms * 3; }
+
+cudaError_t launch_dense(const LayerView& V, int all_dense, int grid, cudaStream_t st) {
+  dense_kernel<<<grid, 128, 0, st>>>(V, all_dense);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const LayerView& V, kvq_certificate* cert, int32_t* level,
+                            cudaStream_t st) {
+  finalize_kernel<<<V.B, 128, 0, st>>>(V, cert, level);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

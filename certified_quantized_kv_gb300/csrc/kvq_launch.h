@@ -1,0 +1,38 @@
+// kvq_launch.h -- host-side launchers of the kernels (internal to the library).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvq.h"
+#include "kvq_common.cuh"
+
+namespace kvq {
+
+// Pointers of one layer's tier 1 and partial-block buffers, for the append path.
+struct LayerAppend {
+  int BG, nbmax;
+  int8_t* kc; __half* ks; uint8_t* vc; __half2* vsv; float* eta;
+  uint32_t* vmin; uint32_t* vmax; uint32_t* kscale_max; uint32_t* vscale_max;
+  const __half* tail_k_in; const __half* tail_v_in;
+  __half* tail_k_out; __half* tail_v_out;
+};
+
+cudaError_t launch_append(const LayerAppend& L, const void* k, const void* v, int n, int pos,
+                          cudaStream_t st);
+cudaError_t launch_export_tier1(const LayerAppend& L, int nb, void* kc, void* ks, void* vc,
+                                void* vs, void* vo, float* eta, float* vmin, float* vmax,
+                                cudaStream_t st);
+
+// Decode pipeline (kvq_score.cu, kvq_mixed.cu, kvq_dense.cu).
+int score_grid(int num_sms);
+int mixed_grid(int num_sms);
+int dense_grid(int num_sms);
+cudaError_t launch_score_select(const LayerView& V, int grid, cudaStream_t st);
+cudaError_t launch_mixed(const LayerView& V, int round, int grid, cudaStream_t st);
+cudaError_t launch_dense(const LayerView& V, int all_dense, int grid, cudaStream_t st);
+cudaError_t launch_finalize(const LayerView& V, kvq_certificate* cert, int32_t* level,
+                            cudaStream_t st);
+
+}  // namespace kvq

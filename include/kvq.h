@@ -1,0 +1,184 @@
+/*
+ * kvq.h -- C ABI of the certified quantized-KV decode-attention library (GB300, sm_103a).
+ *
+ * The method is "Runtime-Certified Bounded-Error Quantized Attention" (gist.science
+ * technical summary).  Section names used below:
+ *   Method §1  tiered storage: tier 1 in VRAM holds per-channel INT8 keys, per-group INT4
+ *              values, their scale/offset metadata and a per-block error annotation;
+ *              tier 2 keeps the unquantised FP16 keys and values in pinned system RAM as
+ *              the ground truth for fallback.
+ *   Method §2  two-term error decomposition: E_key bounds the total-variation distortion
+ *              of the softmax caused by key quantisation through the per-token score
+ *              perturbation Delta; E_val bounds the INT4 value reconstruction error as the
+ *              attention-mass-weighted sum of the per-block errors eta_b.  Both come from
+ *              quantities already tracked (scales, query norms, value ranges).
+ *   Method §3  a light INT8 scoring pass estimates per-block attention mass; the top-K*
+ *              blocks covering tau_cov of it get FP16 keys from tier 2; a ranking check
+ *              compares INT8 and FP16 block orderings; a four-rung fallback ladder (more
+ *              coverage, FP16 values, per-head dense, per-layer dense) follows.
+ *   Contributions, "deterministic recovery": when the certified bound cannot be met the
+ *              returned output is the dense FP16 attention O_dense.
+ *
+ * Conventions for every call
+ *   - Shapes: B = batch, Hq = query heads, Hkv = KV heads, D = head_dim = 128, blocks of
+ *     64 tokens, value groups of 32 channels.  Query head h uses KV head h / (Hq / Hkv).
+ *   - FP16 data is IEEE binary16, passed as void*.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is enqueued on
+ *     it in stream order; a call returns once its work is enqueued, unless it says
+ *     otherwise.  One cache must not be used from two streams at once: every call
+ *     reuses the cache's scratch memory.
+ *   - Errors: every call returns a kvq_status; kvq_last_error() gives the text of the
+ *     calling thread's last failure.  A failed call leaves the cache as it was, except
+ *     after KVQ_ERR_CUDA, which reports an error of the CUDA runtime (the context may be
+ *     unusable).
+ *   - Inputs must be finite.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvq_status {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID = 1,   /* bad argument, NULL pointer, unsupported shape, empty cache */
+  KVQ_ERR_OOM = 2,       /* device memory allocation failed */
+  KVQ_ERR_HOST_OOM = 3,  /* pinned host (tier-2) allocation failed */
+  KVQ_ERR_CAPACITY = 4,  /* append beyond max_ctx tokens */
+  KVQ_ERR_CUDA = 5,      /* a CUDA runtime call failed */
+  KVQ_ERR_TIMEOUT = 6    /* reserved for bounded device waits */
+} kvq_status;
+
+/* Cache shape and the method's open parameters.  head_dim must be 128, block_tokens 64
+ * and value_group 32; n_q_heads / n_kv_heads must be 1, 2, 3 or 4. */
+typedef struct kvq_config {
+  int n_layers;
+  int batch;
+  int n_q_heads;
+  int n_kv_heads;
+  int head_dim;
+  int block_tokens;
+  int value_group;
+  int max_ctx;             /* tokens per sequence and layer */
+  int rank_positions;      /* ranking check compares the top-R blocks (R >= 1; default 1) */
+  float l4_head_fraction;  /* rung 4 when >= this fraction of a sequence's heads are at
+                              rung 3 (in (0, 1]; default 0.5) */
+} kvq_config;
+
+/* Per-head certificate of one decode call (Method §2, §3). */
+typedef struct kvq_certificate {
+  float e_key;             /* bound on the key-quantisation error of the output (max-abs) */
+  float e_val;             /* bound on the value-reconstruction error (max-abs) */
+  int32_t rank_ok;         /* 1 if the INT8 and FP16 rankings of the selected blocks agree */
+  int32_t level;           /* ladder rung reached: 0 certified as is, 1 coverage expanded,
+                              2 values promoted, 3 per-head dense, 4 per-layer dense */
+  int32_t k_star;          /* blocks selected for this head by the top-K* pass */
+  int32_t n_val_promoted;  /* value blocks paged in for the head's certified result */
+  int64_t promoted_bytes;  /* tier-2 bytes read over the host link for this head's KV
+                              group during the call (same for all heads of the group) */
+} kvq_certificate;
+
+typedef struct kvq_cache kvq_cache;
+
+/* Debug flags for kvq_set_debug. */
+#define KVQ_DEBUG_FORCE_RANK_FAIL 0x1  /* every ranking check reports inconsistency */
+#define KVQ_DEBUG_FORCE_DENSE     0x2  /* every head takes rung 4 */
+#define KVQ_DEBUG_SYNC            0x4  /* synchronise and check after every kernel */
+#define KVQ_DEBUG_PROFILE         0x8  /* time every kernel with CUDA events */
+
+/* kvq_cache_create -- allocate tier 1 (device), tier 2 (pinned, mapped host memory) and
+ * scratch for `n_layers` layers of `batch` sequences of up to `max_ctx` tokens (Method §1).
+ * The library owns all of it until kvq_cache_destroy.  Uses the current CUDA device.
+ * Errors: KVQ_ERR_INVALID (cfg NULL or unsupported), KVQ_ERR_OOM, KVQ_ERR_HOST_OOM. */
+kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out);
+
+/* kvq_cache_destroy -- synchronise the device and free everything.  NULL is a no-op. */
+kvq_status kvq_cache_destroy(kvq_cache* cache);
+
+/* kvq_append -- quantise-and-append `n_tokens` new tokens to every sequence of `layer`
+ * (Method §1).  k and v are caller-owned device buffers [B, Hkv, n_tokens, D] of FP16.
+ * Full 64-token blocks are quantised into tier 1 (INT8 keys with one fp16 scale per
+ * block and channel; INT4 values with fp16 scale and offset per token and 32-channel
+ * group; eta_b = max |v - v_hat| over the block); the partial last block stays FP16 in
+ * VRAM until it fills.  Every token is also mirrored to tier 2 by a copy on an internal
+ * side stream that `stream` waits for before any later work, so k and v may be reused
+ * by later work on `stream`.  n_tokens = 0 is a no-op.
+ * Errors: KVQ_ERR_INVALID (layer out of range, NULL buffers, n_tokens < 0),
+ * KVQ_ERR_CAPACITY (length would exceed max_ctx), KVQ_ERR_CUDA. */
+kvq_status kvq_append(kvq_cache* cache, int layer, const void* k, const void* v,
+                      int n_tokens, void* stream);
+
+/* kvq_decode_attention -- certified decode attention of one query token per sequence
+ * against the cached `layer` (Method §2, §3; deterministic recovery).
+ *   q            [B, Hq, D] FP16, device or host memory
+ *   tau_cov      coverage target in (0, 1]; tau_cov == 1 takes rung 4 for every head
+ *   eps          certificate budget on E_key + E_val (max-abs over the head's output),
+ *                eps >= 0; +inf accepts every head whose ranking check passes
+ *   out          [B, Hq, D] FP16, device or host memory
+ *   cert         [B * Hq] certificates (may be NULL), device or host memory
+ *   ladder_level [B] highest rung reached per sequence (may be NULL), device or host
+ * If any of q, out, cert or ladder_level is host memory, the call stages it through
+ * device buffers and synchronises `stream` before returning.  Tier-2 blocks are read
+ * directly by the kernels through the host link (NVLink-C2C); no host round trip
+ * happens inside the call.
+ * Errors: KVQ_ERR_INVALID (layer out of range, empty layer, tau_cov outside (0, 1],
+ * eps < 0 or NaN, NULL q/out), KVQ_ERR_CUDA. */
+kvq_status kvq_decode_attention(kvq_cache* cache, int layer, const void* q, float tau_cov,
+                                float eps, void* out, kvq_certificate* cert,
+                                int32_t* ladder_level, void* stream);
+
+/* kvq_last_error -- text of the calling thread's last error ("" if none).  The pointer
+ * stays valid until the thread's next failing call. */
+const char* kvq_last_error(void);
+
+/* kvq_set_debug -- set KVQ_DEBUG_* flags on the cache (0 clears them). */
+kvq_status kvq_set_debug(kvq_cache* cache, int flags);
+
+/* kvq_cache_length -- tokens currently cached for `layer`. */
+kvq_status kvq_cache_length(const kvq_cache* cache, int layer, int* n_tokens);
+
+/* kvq_export_tier1 -- copy the tier-1 contents of `layer` into caller device buffers in
+ * canonical layout (nb = full blocks of the layer); any pointer may be NULL to skip it:
+ *   kc int8 [B, Hkv, nb, 64, D]        ks fp16 [B, Hkv, nb, D]
+ *   vc uint8 [B, Hkv, nb, 64, D] (one code 0..15 per byte)
+ *   vs fp16 [B, Hkv, nb, 64, D/32]     vo fp16 [B, Hkv, nb, 64, D/32]
+ *   eta float [B, Hkv, nb]             vmin, vmax float [B, Hkv, D]
+ * Stream-ordered.  Errors: KVQ_ERR_INVALID, KVQ_ERR_CUDA. */
+kvq_status kvq_export_tier1(kvq_cache* cache, int layer, void* kc, void* ks, void* vc,
+                            void* vs, void* vo, float* eta, float* vmin, float* vmax,
+                            void* stream);
+
+/* kvq_export_decode_state -- copy the selection state of the last decode call into caller
+ * device buffers (any may be NULL).  nb = full blocks of that call's layer.
+ *   sel    uint8 [B, Hq, nb]   1 if the block is in the head's top-K* set S_h
+ *   kprom0 uint8 [B, Hkv, nb]  FP16-key blocks of the first pass (union of S_h)
+ *   kprom1 uint8 [B, Hkv, nb]  FP16-key blocks after rung 1 (== kprom0 if not run)
+ *   vprom1 uint8 [B, Hkv, nb]  FP16-value blocks after rung 2
+ *   lse8   float [B, Hq, nb]   INT8 block log-mass;  delta float [B, Hq, nb]  Delta_b
+ * Stream-ordered.  Errors: KVQ_ERR_INVALID (no decode yet), KVQ_ERR_CUDA. */
+kvq_status kvq_export_decode_state(kvq_cache* cache, uint8_t* sel, uint8_t* kprom0,
+                                   uint8_t* kprom1, uint8_t* vprom1, float* lse8,
+                                   float* delta, void* stream);
+
+/* Per-kernel timing collected while KVQ_DEBUG_PROFILE is set. */
+typedef struct kvq_kernel_stat {
+  char name[32];
+  int64_t launches;
+  double total_ms;
+} kvq_kernel_stat;
+
+/* kvq_profile_read -- synchronise the cache's streams and return up to `max` kernel
+ * statistics accumulated since the last reset (n = entries written).  reset != 0 clears
+ * them afterwards.  Errors: KVQ_ERR_INVALID, KVQ_ERR_CUDA. */
+kvq_status kvq_profile_read(kvq_cache* cache, kvq_kernel_stat* stats, int max, int* n,
+                            int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

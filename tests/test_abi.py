@@ -1,0 +1,48 @@
+"""The C-ABI library loads and exports every function include/kvq.h declares (CPU only:
+no compute call is made)."""
+
+import ctypes
+import os
+
+import certified_quantized_kv_gb300 as kvq
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _lib():
+    if not os.path.exists(kvq.LIB_PATH):
+        from certified_quantized_kv_gb300 import build
+        build.build()
+    return kvq.load_library()
+
+
+def test_header_symbols_exported():
+    names = kvq.header_functions(os.path.join(ROOT, "include", "kvq.h"))
+    assert len(names) >= 10, names
+    lib = ctypes.CDLL(kvq.LIB_PATH) if _lib() else None
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_null_and_invalid_arguments_without_gpu():
+    lib = _lib()
+    # argument checks run before any CUDA call
+    assert lib.kvq_cache_create(None, None) == kvq.KVQ_ERR_INVALID
+    assert b"NULL" in lib.kvq_last_error()
+    cfg = kvq.kvq_config(1, 1, 32, 8, 64, 64, 32, 1024, 1, 0.5)       # head_dim 64
+    h = ctypes.c_void_p()
+    assert lib.kvq_cache_create(ctypes.byref(cfg), ctypes.byref(h)) == kvq.KVQ_ERR_INVALID
+    assert b"head_dim" in lib.kvq_last_error()
+    cfg = kvq.kvq_config(1, 1, 48, 8, 128, 64, 32, 1024, 1, 0.5)      # n_rep = 6
+    assert lib.kvq_cache_create(ctypes.byref(cfg), ctypes.byref(h)) == kvq.KVQ_ERR_INVALID
+    assert lib.kvq_cache_destroy(None) == kvq.KVQ_OK
+    assert lib.kvq_append(None, 0, None, None, 1, None) == kvq.KVQ_ERR_INVALID
+    assert lib.kvq_decode_attention(None, 0, None, 0.9, 0.25, None, None, None, None) == kvq.KVQ_ERR_INVALID
+
+
+def test_certificate_layout_matches_header():
+    text = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    body = text[text.index("typedef struct kvq_certificate"):]
+    body = body[: body.index("} kvq_certificate;")]
+    fields = [ln.split(";")[0].split()[-1] for ln in body.splitlines()[1:] if ";" in ln]
+    assert fields == list(kvq.CERT_DTYPE.names)

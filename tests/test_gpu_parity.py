@@ -1,0 +1,185 @@
+"""CUDA path (through the C ABI) against the oracle, element by element.
+
+Sizes span several 64-token blocks, 16-block work chunks and a ragged partial block.
+Tolerances are defined in tests/_parity.py.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import certified_quantized_kv_gb300 as kvq  # noqa: E402
+import oracle as O  # noqa: E402
+import workloads as W  # noqa: E402
+from _parity import (compare_decode, compare_tier1, gpu_run, oracle_run)  # noqa: E402
+
+
+def _check(q, K, V, tau, eps, chunks=None, **kw):
+    g = gpu_run(q, K, V, tau, eps, chunks=chunks, **kw)
+    t1, r = oracle_run(q, K, V, tau, eps, rank_positions=kw.get("rank_positions", 1),
+                       l4=kw.get("l4", 0.5))
+    compare_tier1(g["t1"], t1)
+    st = compare_decode(g, t1, r, tau, eps, q.shape[1] // K.shape[1])
+    return g, r, st
+
+
+# ---------------------------------------------------------------------------------
+# Method §1: quantise-and-append, bit-exact, any append pattern
+# ---------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("chunks", [None, [1, 63, 64, 100, 1, 500], [64] * 12 + [17], [7] * 115])
+def test_tier1_bit_exact(chunks):
+    q, K, V = W.tiny(seed=3, ctx=805, Hq=8, Hkv=2, batch=2, kscale=3.0)
+    g = gpu_run(q, K, V, 0.9, 0.25, chunks=chunks)
+    t1, _ = oracle_run(q, K, V, 0.9, 0.25)
+    compare_tier1(g["t1"], t1)
+
+
+def test_tier1_edge_values():
+    """Zero channels, constant groups, huge and tiny magnitudes, exact ties."""
+    q, K, V = W.tiny(seed=4, ctx=64 * 4, Hq=4, Hkv=1)
+    K = K.float(); V = V.float()
+    K[:, :, :64, 3] = 0.0
+    K[:, :, 64:128, :] *= 3000.0
+    K[:, :, 128:192, :] *= 1e-4
+    V[:, :, :64, :32] = 1.5
+    V[:, :, 64:128, 32:64] *= 2000.0
+    V[:, :, 192:, :] = torch.round(V[:, :, 192:, :] * 4) / 4
+    g = gpu_run(q, K.half(), V.half(), 0.9, 0.25)
+    t1, _ = oracle_run(q, K.half(), V.half(), 0.9, 0.25)
+    compare_tier1(g["t1"], t1)
+
+
+# ---------------------------------------------------------------------------------
+# Method §2-§3: decode parity
+# ---------------------------------------------------------------------------------
+
+def test_decode_c1_shape():
+    q, K, V = W.c1()                       # 4096 tokens, 32 q heads / 8 KV heads
+    g, r, st = _check(q, K, V, 0.995, 0.25)
+    assert st["strict"] >= 24, st
+
+
+@pytest.mark.parametrize("ctx", [64 * 16, 64 * 16 + 1, 64 * 33 + 63, 37, 64])
+def test_decode_ragged(ctx):
+    q, K, V = W.tiny(seed=5, ctx=ctx, Hq=8, Hkv=2, batch=2, kscale=3.0)
+    _check(q, K, V, 0.95, 0.25, chunks=[ctx // 3, ctx - ctx // 3])
+
+
+@pytest.mark.parametrize("n_rep", [1, 2, 3])
+def test_decode_gqa_widths(n_rep):
+    q, K, V = W.tiny(seed=6, ctx=64 * 20 + 9, Hq=2 * n_rep, Hkv=2, kscale=3.0)
+    _check(q, K, V, 0.95, 0.25)
+
+
+def test_ladder_rungs_parity():
+    """Value groups with an 8x range push heads to rung 2; a tight eps adds rung 1."""
+    q, K, V = W.tiny(seed=7, ctx=64 * 40 + 11, Hq=8, Hkv=2, kscale=6.0)
+    V = V.float()
+    V[:, :, :, :32] *= 8
+    V = V.half()
+    for tau, eps in [(0.995, 0.25), (0.8, 0.25), (0.5, 0.3), (0.9, 0.05)]:
+        g, r, st = _check(q, K, V, tau, eps)
+        assert st["strict"] > 0
+
+
+def test_rung_levels_seen():
+    q, K, V = W.c3_layer(0, ctx=8192, Hq=8, Hkv=2)
+    g, r, st = _check(q, K, V, 0.995, 0.25)
+    assert (r.planned >= 1).any(), "workload did not reach rungs 1-2"
+
+
+def test_tau_one_is_dense():
+    q, K, V = W.tiny(seed=8, ctx=64 * 10 + 3, Hq=8, Hkv=2, kscale=3.0)
+    g = gpu_run(q, K, V, 1.0, 0.25)
+    assert np.all(g["cert"]["level"] == 4) and np.all(g["cert"]["e_key"] == 0)
+    for h in range(8):
+        dense = O.dense_attention(q[0, h].numpy(), K[0, h // 4].numpy(), V[0, h // 4].numpy())
+        assert np.allclose(g["out"][0, h].float().numpy(), dense, atol=2e-3, rtol=1e-2)
+
+
+def test_forced_rank_failure_goes_dense():
+    q, K, V = W.tiny(seed=9, ctx=64 * 10 + 3, Hq=8, Hkv=2, kscale=3.0)
+    g = gpu_run(q, K, V, 0.95, 0.25, debug=kvq.DEBUG_FORCE_RANK_FAIL)
+    assert np.all(g["cert"]["rank_ok"] == 0)
+    assert np.all(g["cert"]["level"] == 4) and np.all(g["level"] == 4)
+    for h in range(8):
+        dense = O.dense_attention(q[0, h].numpy(), K[0, h // 4].numpy(), V[0, h // 4].numpy())
+        assert np.allclose(g["out"][0, h].float().numpy(), dense, atol=2e-3, rtol=1e-2)
+
+
+def test_planted_block_fires_rank_check():
+    q, K, V, info = W.c4(batch=2, ctx=8192, Hq=8, Hkv=2)
+    g, r, st = _check(q, K, V, 0.995, 0.25)
+    assert np.all(g["cert"]["rank_ok"] == 0)
+    assert np.all(g["level"] == 4)
+
+
+def test_eps_special_cases():
+    q, K, V = W.tiny(seed=10, ctx=64 * 12 + 5, Hq=8, Hkv=2, kscale=3.0)
+    g, r, st = _check(q, K, V, 0.9, math.inf)
+    c = g["cert"]
+    assert np.all((c["level"] == 0) | (c["rank_ok"] == 0))
+    g0, r0, st0 = _check(q, K, V, 0.9, 0.0)
+    c0 = g0["cert"]
+    assert np.all((c0["level"] >= 3) | ((c0["e_key"] == 0) & (c0["e_val"] == 0)))
+
+
+def test_host_buffers_match_device_buffers():
+    q, K, V = W.tiny(seed=11, ctx=64 * 9 + 1, Hq=8, Hkv=2, kscale=3.0)
+    gd = gpu_run(q, K, V, 0.95, 0.25)
+    gh = gpu_run(q, K, V, 0.95, 0.25, host_io=True)
+    assert torch.equal(gd["out"], gh["out"])
+    assert np.array_equal(gd["cert"], gh["cert"]) and np.array_equal(gd["level"], gh["level"])
+
+
+def test_deterministic_repeat():
+    q, K, V = W.c1(ctx=64 * 50 + 7, Hq=8, Hkv=2)
+    g = gpu_run(q, K, V, 0.995, 0.25, repeat=3)
+    o0, c0, l0 = g["runs"][0]
+    for o, c, l in g["runs"][1:]:
+        assert torch.equal(o, o0) and np.array_equal(c, c0) and np.array_equal(l, l0)
+
+
+def test_rank_positions_two():
+    q, K, V = W.tiny(seed=12, ctx=64 * 30 + 2, Hq=8, Hkv=2, kscale=4.0)
+    _check(q, K, V, 0.9, 0.25, rank_positions=2)
+
+
+# ---------------------------------------------------------------------------------
+# C-ABI error behaviour
+# ---------------------------------------------------------------------------------
+
+def test_errors():
+    cache = kvq.Cache(1, 1, 4, 1, max_ctx=128)
+    try:
+        q = torch.zeros(1, 4, 128, dtype=torch.float16, device="cuda")
+        out = torch.empty_like(q)
+        with pytest.raises(kvq.KvqError) as e:
+            cache.decode(0, q, 0.9, 0.25, out)       # empty layer
+        assert e.value.status == kvq.KVQ_ERR_INVALID
+        k = torch.zeros(1, 1, 100, 128, dtype=torch.float16, device="cuda")
+        cache.append(0, k, k)
+        with pytest.raises(kvq.KvqError) as e:
+            cache.append(0, k, k)                    # 200 > max_ctx
+        assert e.value.status == kvq.KVQ_ERR_CAPACITY
+        assert cache.length(0) == 100
+        for tau, eps in [(0.0, 0.25), (1.5, 0.25), (0.9, -1.0), (0.9, float("nan"))]:
+            with pytest.raises(kvq.KvqError) as e:
+                cache.decode(0, q, tau, eps, out)
+            assert e.value.status == kvq.KVQ_ERR_INVALID
+        with pytest.raises(kvq.KvqError):
+            cache.decode(1, q, 0.9, 0.25, out)       # layer out of range
+        cache.decode(0, q, 0.9, 0.25, out)           # still usable
+    finally:
+        cache.close()
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.Cache(1, 1, 6, 1, max_ctx=128)           # n_rep = 6 unsupported
+    assert e.value.status == kvq.KVQ_ERR_INVALID
