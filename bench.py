@@ -1,0 +1,382 @@
+"""Benchmark: certified decode-attention tokens/s/layer at 128K context on one GB300.
+
+One step = one certified decode step of every layer of the workload (each layer:
+INT8 scoring + top-K* selection, mixed-precision pass with certificate and ladder plan,
+second pass for rungs 1-2, dense rungs 3-4, certificate write-out), with the caches
+already resident (tier 1 in HBM, tier 2 in pinned host memory).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Under torchrun (N > 1) every rank runs an independent replica
+(the path has no data exchange between sequences or heads) and rank 0 reports the
+aggregate.  `--impl reference` times the CPU oracle on a bounded sample of the same
+workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+WORKLOAD = dict(name="c3_llama8b_ctx128k_32l", batch=1, ctx=131072, layers=32, q_heads=32,
+                kv_heads=8, head_dim=128, tau_cov=0.995, eps=0.25, seed=2)
+METRIC = "certified decode-attn tokens/s/layer at 128K ctx; HBM GB/s vs peak"
+UNIT = "tokens/s/layer"
+TIER1_BYTES_PER_TOKEN_HEAD = 212        # 128 K codes + 4 K scales + 64 V codes + 16 V scale/offset
+SCORE_BYTES_PER_TOKEN_HEAD = 132        # K codes + K scales (scoring pass)
+MIX_BYTES_PER_TOKEN_HEAD = 80           # V codes + V scale/offset (mixed pass, tail blocks)
+F16_BLOCK = 16384
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1])); mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                      "sw_power_cap"), f[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        finally:
+            os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------
+# reference arm / CPU baseline: the oracle on a bounded sample
+# ---------------------------------------------------------------------------------
+
+def oracle_sample(wl: dict, groups: int = 1) -> dict:
+    """Time the oracle on `groups` (sequence, KV head) groups of one layer of the workload.
+
+    Runs single-threaded (BLAS threads pinned to 1 by the caller's environment).
+    Returns the per-layer time scaled from the sample.
+    """
+    import oracle as O
+    import workloads as W
+    q, K, V = W.c3_layer(0, device="cpu", seed=wl["seed"], batch=wl["batch"], ctx=wl["ctx"],
+                         Hq=wl["q_heads"], Hkv=wl["kv_heads"])
+    n_rep = wl["q_heads"] // wl["kv_heads"]
+    total = 0.0
+    for g in range(groups):
+        qs = q[:, g * n_rep:(g + 1) * n_rep].numpy()
+        Ks, Vs = K[:, g:g + 1].numpy(), V[:, g:g + 1].numpy()
+        t0 = time.perf_counter()
+        t1 = O.quantize_layer(Ks, Vs)          # the oracle derives tier 1 itself; not timed below
+        total_q = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        O.decode_layer(qs, Ks, Vs, t1, wl["tau_cov"], wl["eps"], O.OracleConfig(n_rep=n_rep))
+        total += time.perf_counter() - t0
+        del total_q
+    per_group = total / groups
+    t_layer = per_group * wl["batch"] * wl["kv_heads"]
+    return {"t_layer_s": t_layer, "sample_s": total, "groups": groups}
+
+
+def run_oracle_subprocess(wl: dict, groups: int = 1) -> dict:
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "print(json.dumps(bench.oracle_sample(json.loads(sys.argv[1]), %d)))" % (ROOT, groups))
+    r = subprocess.run([sys.executable, "-c", code, json.dumps(wl)], capture_output=True, text=True,
+                       env=env, timeout=1200)
+    if r.returncode != 0:
+        raise RuntimeError(r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def reference_arm(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    times = []
+    for i in range(args.warmup + args.steps):
+        s = run_oracle_subprocess(wl, 1)
+        if i >= args.warmup:
+            times.append(s["t_layer_s"])
+    t_layer = float(np.mean(times))
+    value = wl["batch"] / t_layer
+    sample = (f"oracle decode of 1 of {wl['batch'] * wl['kv_heads']} (sequence, KV head) groups "
+              f"(4 query heads) of one {wl['ctx']}-token layer per step, scaled to the layer")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_layer * wl["layers"] * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": _config(wl),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def _config(wl):
+    return {"workload": wl["name"], "batch": wl["batch"], "ctx": wl["ctx"], "layers": wl["layers"],
+            "q_heads": wl["q_heads"], "kv_heads": wl["kv_heads"], "head_dim": wl["head_dim"],
+            "tau_cov": wl["tau_cov"], "eps": wl["eps"],
+            "l2": "inputs larger than L2: tier 1 and tier 2 of all layers are streamed every step"}
+
+
+# ---------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------
+
+def measure_h2d(torch):
+    n = 256 << 20
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device="cuda")
+    best = 1e9
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); d.copy_(h, non_blocking=True); e1.record(); e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return n / best / 1e6   # GB/s
+
+
+def our_arm(args, wl):
+    import torch
+    import torch.distributed as dist
+    import certified_quantized_kv_gb300 as kvq
+    import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    B, L, N = wl["batch"], wl["layers"], wl["ctx"]
+    Hq, Hkv, D = wl["q_heads"], wl["kv_heads"], wl["head_dim"]
+    tau, eps = wl["tau_cov"], wl["eps"]
+
+    cache = kvq.Cache(L, B, Hq, Hkv, max_ctx=N)
+    qs, qs_host = [], []
+    t_fill = time.time()
+    for layer in range(L):
+        q, K, V = W.c3_layer(layer, device="cuda", seed=wl["seed"] + 1000 * rank, batch=B, ctx=N, Hq=Hq, Hkv=Hkv)
+        cache.append(layer, K.contiguous(), V.contiguous())
+        qs.append(q.contiguous())
+        qs_host.append(q.cpu().pin_memory())
+        del K, V
+    torch.cuda.synchronize()
+    t_fill = time.time() - t_fill
+    outs = [torch.empty(B, Hq, D, dtype=torch.float16, device="cuda") for _ in range(L)]
+    certs = [torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda") for _ in range(L)]
+    lvls = [torch.empty(B, dtype=torch.int32, device="cuda") for _ in range(L)]
+
+    def step():
+        for layer in range(L):
+            cache.decode(layer, qs[layer], tau, eps, outs[layer], certs[layer], lvls[layer])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(args.steps):
+            step()
+        e1.record(st)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+        dist.barrier()
+    ms_per_step = ms / args.steps
+    value = world * B * L / (ms_per_step / 1e3)
+
+    # certificates of the last step: ladder histogram, promoted bytes
+    hist = [0] * 5
+    prom = 0
+    n_rep = Hq // Hkv
+    for layer in range(L):
+        c = kvq.certificates(certs[layer]).reshape(B, Hq)
+        for lv in c["level"].ravel():
+            hist[int(lv)] += 1
+        prom += int(c["promoted_bytes"][:, ::n_rep].sum())
+
+    # per-kernel durations: a second pass with CUDA events around every kernel
+    cache.set_debug(kvq.DEBUG_PROFILE)
+    cache.profile_read(reset=True)
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize()
+    prof = cache.profile_read(reset=True)
+    cache.set_debug(0)
+
+    # end to end through the C ABI with host buffers (q in, out + certificate back)
+    outs_h = [torch.empty(B, Hq, D, dtype=torch.float16).pin_memory() for _ in range(L)]
+    certs_h = [torch.empty(B * Hq * 32, dtype=torch.uint8).pin_memory() for _ in range(L)]
+    lvls_h = [torch.empty(B, dtype=torch.int32).pin_memory() for _ in range(L)]
+
+    def step_host():
+        for layer in range(L):
+            cache.decode(layer, qs_host[layer], tau, eps, outs_h[layer], certs_h[layer], lvls_h[layer])
+
+    step_host()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step_host()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    e2e_value = world * B * L / e2e_s
+    h2d = L * B * Hq * D * 2
+    d2h = L * (B * Hq * D * 2 + B * Hq * 32 + B * 4)
+
+    h2d_gbs = measure_h2d(torch)
+    if rank != 0:
+        cache.close()
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    hbm_peak, peak_kind = _peaks()
+    kern = {}
+    for name, (n, tot) in prof.items():
+        kern[name] = {"launches": n, "avg_us": 1e3 * tot / max(1, n), "total_ms": tot}
+    tot_all = sum(v["total_ms"] for v in kern.values()) or 1.0
+    for v in kern.values():
+        v["share"] = v["total_ms"] / tot_all
+    units = B * Hkv * N      # token x KV-head units per layer
+    algo = {"score_select": SCORE_BYTES_PER_TOKEN_HEAD * units,
+            "mixed_round0": MIX_BYTES_PER_TOKEN_HEAD * units}
+    dom = max(kern.items(), key=lambda kv: kv[1]["total_ms"])[0] if kern else None
+    roofline = None
+    if dom in algo:
+        achieved = algo[dom] / (kern[dom]["avg_us"] * 1e-6) / 1e9
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
+                    "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
+                    "traffic": None,
+                    "algorithmic_bytes_per_launch": algo[dom]}
+    # whole tier-1 pass (scoring + mixed) against the HBM roofline
+    t1_us = sum(kern[k]["avg_us"] for k in ("score_select", "mixed_round0") if k in kern)
+    tier1 = None
+    if t1_us > 0:
+        tier1_bytes = TIER1_BYTES_PER_TOKEN_HEAD * units
+        tier1 = {"bytes_per_layer": tier1_bytes, "us_per_layer": t1_us,
+                 "achieved_gbs": tier1_bytes / (t1_us * 1e-6) / 1e9,
+                 "frac_of_hbm": tier1_bytes / (t1_us * 1e-6) / 1e9 / hbm_peak}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32 accumulate (int8/int4/f16 MMA operands)",
+        "data": "synthetic (seeded Gaussian caches shaped like Llama-3.1-8B attention)",
+        "config": _config(wl),
+        "clocks": clk.summary(),
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(sum(v["launches"] for v in kern.values())) // max(1, args.steps) * args.steps,
+        "roofline": roofline,
+        "tier1_pass": tier1,
+        "kernels": kern,
+        "ladder_histogram": hist,
+        "promoted_bytes_per_step": prom,
+        "host_link": {"h2d_gbs_measured": h2d_gbs,
+                      "promoted_us_at_h2d": prom / L / (h2d_gbs * 1e3) if h2d_gbs else None},
+        "fill_s": t_fill,
+    }
+    if args.cpu_baseline:
+        try:
+            s = run_oracle_subprocess(wl, 1)
+            line["cpu_baseline"] = {
+                "value": wl["batch"] / s["t_layer_s"], "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": (f"oracle decode of 1 of {B * Hkv} (sequence, KV head) groups of one "
+                           f"{N}-token layer ({s['sample_s']:.1f} s of CPU), scaled to the layer")}
+        except Exception as e:  # pragma: no cover
+            line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                    "sample": f"failed: {e}"[:200]}
+    print(json.dumps(line), flush=True)
+    cache.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--layers", type=int, default=None, help="override the layer count (not the headline)")
+    ap.add_argument("--ctx", type=int, default=None, help="override the context (not the headline)")
+    ap.add_argument("--batch", type=int, default=None, help="override the batch (not the headline)")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    wl = dict(WORKLOAD)
+    for k in ("layers", "ctx", "batch"):
+        v = getattr(args, k)
+        if v is not None:
+            wl[k] = v
+            wl["name"] = f"c3_shape_custom_b{wl['batch']}_ctx{wl['ctx']}_{wl['layers']}l"
+    if args.impl == "reference":
+        reference_arm(args, wl)
+    else:
+        our_arm(args, wl)
+
+
+if __name__ == "__main__":
+    main()
