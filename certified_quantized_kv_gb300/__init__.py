@@ -79,6 +79,7 @@ def load_library() -> ctypes.CDLL:
         "kvq_export_tier1": [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp],
         "kvq_export_decode_state": [vp, vp, vp, vp, vp, vp, vp, vp],
         "kvq_profile_read": [vp, ctypes.POINTER(kvq_kernel_stat), i32, ctypes.POINTER(i32), i32],
+        "kvq_dense_decode_noalloc": [vp, vp, vp, i32, i32, i32, i32, vp, vp],
     }
     for name, argt in sigs.items():
         fn = getattr(lib, name)
@@ -206,6 +207,20 @@ class Cache:
         n = ctypes.c_int()
         _check(self.lib.kvq_profile_read(self.handle, arr, 16, ctypes.byref(n), int(reset)))
         return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(n.value)}
+
+
+def dense_decode_noalloc(q, k, v, out, stream=None):
+    """Exact dense FP16 decode attention with no allocation (kvq_dense_decode_noalloc).
+
+    For callers that cannot allocate device memory at call time; q, out: device fp16
+    [B, Hq, 128]; k, v: device fp16 [B, Hkv, n_tokens, 128].  Its scratch is a fixed
+    8 MiB device array shared by every call, so overlapping calls must be serialised.
+    """
+    assert q.is_contiguous() and k.is_contiguous() and v.is_contiguous() and out.is_contiguous()
+    B, Hq, _ = q.shape
+    Hkv, N = k.shape[1], k.shape[2]
+    _check(load_library().kvq_dense_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N,
+                                                   _ptr(out), _stream(stream)))
 
 
 def header_functions(header_path: str | None = None) -> list[str]:

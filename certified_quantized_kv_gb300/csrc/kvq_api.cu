@@ -53,6 +53,11 @@ const char* kKernelNames[K_COUNT] = {"score_select", "mixed_round0", "mixed_roun
 
 }  // namespace
 
+namespace kvq {
+// Lets other translation units of the library report through kvq_last_error().
+void set_last_error(const std::string& msg) { g_err = msg; }
+}  // namespace kvq
+
 struct kvq_cache {
   kvq_config cfg;
   int device = 0, num_sms = 0;

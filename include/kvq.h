@@ -177,6 +177,29 @@ typedef struct kvq_kernel_stat {
 kvq_status kvq_profile_read(kvq_cache* cache, kvq_kernel_stat* stats, int max, int* n,
                             int reset);
 
+/* kvq_dense_decode_noalloc -- exact dense FP16 decode attention that allocates no memory.
+ * The paper has no counterpart to this call.  It is for callers that cannot allocate
+ * device memory when they call: a process whose device memory is fully held by another
+ * framework's pool, an embedding that owns only fixed buffers, or a step that must not
+ * fail on allocation.  It computes softmax(q K^T / sqrt(D)) V -- the same dense attention
+ * as the ladder's rungs 3-4 -- over caller-owned FP16 keys and values, keeping its
+ * split-K partials and counters in one static 8 MiB device array instead of calling
+ * cudaMalloc, cudaFree or any allocating routine.
+ *   q   [B, Hq, D] FP16, device;  k, v [B, Hkv, n_tokens, D] FP16, device
+ *   out [B, Hq, D] FP16, device (caller-owned);  Hq / Hkv in 1..4, n_tokens >= 1
+ * Size limit: B * Hkv * ceil(n_tokens / 1024) * 2112 bytes of partials (plus a few
+ * counters) must fit in the 8 MiB array, e.g. B * Hkv = 8 with up to 507904 tokens.
+ * The array exists once per device that loads the library and is held until the
+ * process exits.  The first call on a device, with that device current, looks up the
+ * array's device address; make that first call before any stream capture.  Every call
+ * shares the array and clears the counters it needs itself; calls whose work overlaps
+ * on the GPU (other streams, other host threads) race on it and must be serialised.
+ * Stream-ordered.  Errors: KVQ_ERR_INVALID (NULL or host pointers, bad shape),
+ * KVQ_ERR_CAPACITY (beyond the size limit), KVQ_ERR_CUDA. */
+kvq_status kvq_dense_decode_noalloc(const void* q, const void* k, const void* v, int batch,
+                                    int n_q_heads, int n_kv_heads, int n_tokens, void* out,
+                                    void* stream);
+
 #ifdef __cplusplus
 }
 #endif
