@@ -384,7 +384,10 @@ class DecodeResult:
     level: np.ndarray          # int [B, Hq]
     k_star: np.ndarray         # int [B, Hq]
     n_val_promoted: np.ndarray  # int [B, Hq]
-    promoted_bytes: np.ndarray  # int64 [B, Hq] (tier-2 bytes of the head's KV group)
+    promoted_bytes: np.ndarray  # int64 [B, Hq]: tier-2 bytes paged in for the head's KV group
+                                # (FP16 key blocks of the union U, plus rung-1 key blocks,
+                                # rung-2 value blocks, and K and V of every full block
+                                # when a head of the group goes dense)
     ladder_level: np.ndarray   # int [B]
     # diagnostics for parity tests
     sel: list = field(default_factory=list)      # [B][Hq] selected blocks in order
@@ -497,7 +500,9 @@ def decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Tier1,
                 if asking:
                     U1[adds_k] = True
                     V1[adds_v] = True
-                    group_bytes[b, g] += (int(U1.sum()) + int(V1.sum())) * blk_bytes
+                    # each FP16 block is paged in once per call: rung 1 adds only the
+                    # new key blocks, rung 2 the value blocks
+                    group_bytes[b, g] += (int(U1.sum()) - int(U.sum()) + int(V1.sum())) * blk_bytes
                     for h in asking:
                         P = per[h]
                         r1 = mixed_attention(P["s_ex"], P["s_hat"], Vg, v_hat, P["delta"], eta, R, U1, V1)
