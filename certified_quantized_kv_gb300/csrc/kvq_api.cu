@@ -47,9 +47,11 @@ __global__ void fill_u32(uint32_t* p, uint32_t v, size_t n) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = v;
 }
 
-enum KernelId { K_SCORE = 0, K_MIX0, K_MIX1, K_DENSE, K_FINAL, K_APPEND, K_COUNT };
-const char* kKernelNames[K_COUNT] = {"score_select", "mixed_round0", "mixed_round1",
-                                     "dense_fallback", "finalize", "quantize_append"};
+enum KernelId { K_SCORE = 0, K_SELECT, K_MIX0, K_COMB0, K_MIX1, K_COMB1, K_DENSE, K_FINAL,
+                K_APPEND, K_COUNT };
+const char* kKernelNames[K_COUNT] = {"score", "select", "mixed_round0", "combine_round0",
+                                     "mixed_round1", "combine_round1", "dense_fallback",
+                                     "finalize", "quantize_append"};
 
 }  // namespace
 
@@ -61,7 +63,7 @@ void set_last_error(const std::string& msg) { g_err = msg; }
 struct kvq_cache {
   kvq_config cfg;
   int device = 0, num_sms = 0;
-  int B = 0, Hq = 0, Hkv = 0, n_rep = 0, BG = 0, nbmax = 0, L = 0;
+  int B = 0, Hq = 0, Hkv = 0, n_rep = 0, BG = 0, nbmax = 0, nbmax_used = 0, L = 0;
   long long cap = 0;  // tier-2 tokens per (sequence, KV head)
   std::vector<int> n_tokens;
   std::vector<int> tail_parity;
@@ -76,9 +78,10 @@ struct kvq_cache {
   char* scr = nullptr;
   float *shat = nullptr, *lse8 = nullptr, *delta = nullptr, *lse16 = nullptr;
   uint8_t *sel = nullptr, *kprom0 = nullptr, *kprom1 = nullptr, *vprom1 = nullptr;
+  uint32_t* mkey = nullptr;
   HeadState* hst = nullptr;
   GroupState* gst = nullptr;
-  float *part = nullptr, *dpart = nullptr;
+  float *part = nullptr, *part1 = nullptr, *dpart = nullptr;
   unsigned int* counters = nullptr;
   __half *q_stage = nullptr, *out_stage = nullptr;
   kvq_certificate* cert_stage = nullptr;
@@ -204,6 +207,8 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   if (k.n_q_heads % k.n_kv_heads != 0 || k.n_q_heads / k.n_kv_heads > MAXREP)
     return fail(KVQ_ERR_INVALID, "n_q_heads / n_kv_heads must be an integer in 1..4");
   if (k.rank_positions < 1) return fail(KVQ_ERR_INVALID, "rank_positions must be >= 1");
+  if (k.max_ctx > (1 << 21))   // selection keeps one key per block in shared memory
+    return fail(KVQ_ERR_INVALID, "max_ctx must be <= 2097152 tokens");
   if (!(k.l4_head_fraction > 0.f && k.l4_head_fraction <= 1.f))
     return fail(KVQ_ERR_INVALID, "l4_head_fraction must be in (0, 1]");
 
@@ -213,13 +218,14 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
   c->B = k.batch; c->Hq = k.n_q_heads; c->Hkv = k.n_kv_heads; c->n_rep = k.n_q_heads / k.n_kv_heads;
   c->BG = c->B * c->Hkv; c->L = k.n_layers;
-  c->nbmax = k.max_ctx / BLK;
+  c->nbmax_used = k.max_ctx / BLK;
+  c->nbmax = (std::max(1, c->nbmax_used) + 15) / 16 * 16;   // row stride of per-block arrays
   c->cap = (long long)((k.max_ctx + BLK - 1) / BLK) * BLK;
   c->n_tokens.assign(c->L, 0);
   c->tail_parity.assign(c->L, 0);
 
   // ---- tier 1 ----
-  const size_t BG = c->BG, nbm = std::max(1, c->nbmax);
+  const size_t BG = c->BG, nbm = c->nbmax;
   size_t o = 0;
   c->off_kc = o;   o = align_up(o + BG * nbm * KC_BYTES, 256);
   c->off_ks = o;   o = align_up(o + BG * nbm * D * 2, 256);
@@ -276,12 +282,14 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   const size_t s_delta = o; o = align_up(o + HQ * nbm * 4, 256);
   const size_t s_lse16 = o; o = align_up(o + HQ * nbm * 4, 256);
   const size_t s_sel = o;   o = align_up(o + HQ * nbm, 256);
+  const size_t s_mkey = o;  o = align_up(o + HQ * nbm * 4, 256);
   const size_t s_kp0 = o;   o = align_up(o + BG * nbm, 256);
   const size_t s_kp1 = o;   o = align_up(o + BG * nbm, 256);
   const size_t s_vp1 = o;   o = align_up(o + BG * nbm, 256);
   const size_t s_hst = o;   o = align_up(o + HQ * sizeof(HeadState), 256);
   const size_t s_gst = o;   o = align_up(o + BG * sizeof(GroupState), 256);
   const size_t s_part = o;  o = align_up(o + BG * NCH * MAXREP * (D + 4) * 4, 256);
+  const size_t s_part1 = o; o = align_up(o + BG * NCH * MAXREP * (D + 4) * 4, 256);
   const size_t s_dpart = o; o = align_up(o + BG * NCH * MAXREP * (D + 4) * 4, 256);
   const size_t s_cnt = o;   o = align_up(o + (CNT_GROUP_BASE + 4 * BG) * 4, 256);
   const size_t s_q = o;     o = align_up(o + HQ * D * 2, 256);
@@ -299,12 +307,14 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   c->delta = reinterpret_cast<float*>(c->scr + s_delta);
   c->lse16 = reinterpret_cast<float*>(c->scr + s_lse16);
   c->sel = reinterpret_cast<uint8_t*>(c->scr + s_sel);
+  c->mkey = reinterpret_cast<uint32_t*>(c->scr + s_mkey);
   c->kprom0 = reinterpret_cast<uint8_t*>(c->scr + s_kp0);
   c->kprom1 = reinterpret_cast<uint8_t*>(c->scr + s_kp1);
   c->vprom1 = reinterpret_cast<uint8_t*>(c->scr + s_vp1);
   c->hst = reinterpret_cast<HeadState*>(c->scr + s_hst);
   c->gst = reinterpret_cast<GroupState*>(c->scr + s_gst);
   c->part = reinterpret_cast<float*>(c->scr + s_part);
+  c->part1 = reinterpret_cast<float*>(c->scr + s_part1);
   c->dpart = reinterpret_cast<float*>(c->scr + s_dpart);
   c->counters = reinterpret_cast<unsigned int*>(c->scr + s_cnt);
   c->q_stage = reinterpret_cast<__half*>(c->scr + s_q);
@@ -405,7 +415,7 @@ kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q, float ta
 
   LayerView V;
   V.B = c->B; V.Hq = c->Hq; V.Hkv = c->Hkv; V.n_rep = c->n_rep; V.BG = c->BG;
-  V.nb = N / BLK; V.n_tail = N % BLK; V.nbmax = std::max(1, c->nbmax); V.cap = c->cap;
+  V.nb = N / BLK; V.n_tail = N % BLK; V.nbmax = c->nbmax; V.cap = c->cap;
   V.kc = layer_kc(c, layer); V.ks = layer_ks(c, layer); V.vc = layer_vc(c, layer);
   V.vsv = layer_vsv(c, layer); V.eta = layer_eta(c, layer);
   V.vmin = layer_vmin(c, layer); V.vmax = layer_vmax(c, layer);
@@ -418,12 +428,16 @@ kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q, float ta
   V.shat = c->shat; V.lse8 = c->lse8; V.delta = c->delta; V.lse16 = c->lse16; V.sel = c->sel;
   V.kprom0 = c->kprom0; V.kprom1 = c->kprom1; V.vprom1 = c->vprom1;
   V.hst = c->hst; V.gst = c->gst; V.part = c->part; V.dpart = c->dpart; V.counters = c->counters;
+  V.mkey = c->mkey; V.part1 = c->part1;
 
   const bool all_dense = (tau >= 1.f) || (c->debug & KVQ_DEBUG_FORCE_DENSE);
   if (!all_dense) {
-    { KernelScope s(c, K_SCORE, st); KVQ_CUDA(s.done(launch_score_select(V, score_grid(c->num_sms), st)), "score_select"); }
+    { KernelScope s(c, K_SCORE, st); KVQ_CUDA(s.done(launch_score(V, score_grid(c->num_sms), st)), "score"); }
+    { KernelScope s(c, K_SELECT, st); KVQ_CUDA(s.done(launch_select(V, st)), "select"); }
     { KernelScope s(c, K_MIX0, st); KVQ_CUDA(s.done(launch_mixed(V, 0, mixed_grid(c->num_sms), st)), "mixed_round0"); }
+    { KernelScope s(c, K_COMB0, st); KVQ_CUDA(s.done(launch_combine(V, 0, st)), "combine_round0"); }
     { KernelScope s(c, K_MIX1, st); KVQ_CUDA(s.done(launch_mixed(V, 1, mixed_grid(c->num_sms), st)), "mixed_round1"); }
+    { KernelScope s(c, K_COMB1, st); KVQ_CUDA(s.done(launch_combine(V, 1, st)), "combine_round1"); }
   }
   { KernelScope s(c, K_DENSE, st); KVQ_CUDA(s.done(launch_dense(V, all_dense ? 1 : 0, dense_grid(c->num_sms), st)), "dense_fallback"); }
   { KernelScope s(c, K_FINAL, st); KVQ_CUDA(s.done(launch_finalize(V, cd, ld, st)), "finalize"); }
@@ -455,7 +469,7 @@ kvq_status kvq_export_decode_state(kvq_cache* c, uint8_t* sel, uint8_t* kprom0, 
   const int nb = c->last_nb;
   if (nb == 0) return KVQ_OK;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t HQ = (size_t)c->B * c->Hq, nbm = std::max(1, c->nbmax);
+  const size_t HQ = (size_t)c->B * c->Hq, nbm = c->nbmax;
   auto cp = [&](void* dst, const void* src, size_t elem, size_t rows) -> cudaError_t {
     if (!dst) return cudaSuccess;
     return cudaMemcpy2DAsync(dst, nb * elem, src, nbm * elem, nb * elem, rows, cudaMemcpyDeviceToDevice, st);

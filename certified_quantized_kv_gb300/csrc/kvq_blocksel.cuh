@@ -1,0 +1,241 @@
+// kvq_blocksel.cuh -- block-wide (256-thread) reductions and the "top blocks covering a
+// target" selection used by the top-K* pass and by rungs 1-2 of the ladder.
+//
+// Selection rule ("Runtime-Certified Bounded-Error Quantized Attention", gist.science
+// technical summary, Method §3): take blocks in descending value, ties to the lower
+// block index, until the taken weight reaches the target.  Values v_i in [0, 1] are
+// passed as keys (fp32 bits, order-preserving for v >= 0; 0 = not a candidate) and
+// weighted in fixed point, w_i = floor(v_i 2^62), so every sum is an exact integer and
+// the choice does not depend on summation order.
+//
+// Method: the threshold key is found 10 bits per level (keys of values <= 1 are below
+// 2^30): each warp accumulates its keys' weights into a private 1024-bucket histogram,
+// the warps' histograms are summed, a block scan finds the bucket where the running
+// weight from the top reaches the target, and once that bucket holds at most SEL_CAND
+// keys they are ranked exactly.
+#pragma once
+
+#include "kvq_common.cuh"
+
+namespace kvq {
+
+constexpr int BS_THREADS = 256;
+constexpr int BS_WARPS = BS_THREADS / 32;
+
+struct BlockRed {
+  float f[BS_WARPS];
+  unsigned long long u[BS_WARPS];
+  int i[BS_WARPS];
+};
+
+__device__ __forceinline__ float block_sum(float v, BlockRed& r) {
+  v = warp_sum(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r.f[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < BS_WARPS; ++w) t += r.f[w];
+  return t;
+}
+
+__device__ __forceinline__ float block_max(float v, BlockRed& r) {
+  v = warp_max(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r.f[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < BS_WARPS; ++w) t = fmaxf(t, r.f[w]);
+  return t;
+}
+
+__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, BlockRed& r) {
+  v = warp_sum_u64(v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r.u[threadIdx.x >> 5] = v;
+  __syncthreads();
+  unsigned long long t = 0;
+#pragma unroll
+  for (int w = 0; w < BS_WARPS; ++w) t += r.u[w];
+  return t;
+}
+
+__device__ __forceinline__ int block_sum_int(int v, BlockRed& r) {
+  v = (int)__reduce_add_sync(0xffffffffu, (unsigned)v);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) r.i[threadIdx.x >> 5] = v;
+  __syncthreads();
+  int t = 0;
+#pragma unroll
+  for (int w = 0; w < BS_WARPS; ++w) t += r.i[w];
+  return t;
+}
+
+// Exclusive prefix sum over the block in thread order; *total = the block total.
+__device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v, BlockRed& r,
+                                                                  unsigned long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned long long incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  __syncthreads();
+  if (lane == 31) r.u[warp] = incl;
+  __syncthreads();
+  unsigned long long before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < BS_WARPS; ++w) {
+    if (w < warp) before += r.u[w];
+    tot += r.u[w];
+  }
+  *total = tot;
+  return before + incl - v;
+}
+
+// Shared-memory workspace of block_select_top (dynamic shared memory).
+struct BlockSelSmem {
+  unsigned long long hist[BS_WARPS][1024];   // per-warp private histograms
+  int cidx[SEL_CAND];
+  uint32_t ckey[SEL_CAND];
+  int order[SEL_CAND];
+  unsigned long long above;
+  uint32_t prefix;
+  int ncand;
+  int last;
+  unsigned long long take_w;
+  BlockRed red;
+};
+
+// keys: n keys in shared memory (thread t owns the contiguous range [t*kpt, t*kpt+kpt)).
+// Calls mark(i) for every taken block; returns their count; *taken = weight taken.
+template <typename MarkFn>
+__device__ int block_select_top(int n, const uint32_t* keys, unsigned long long target, MarkFn mark,
+                                BlockSelSmem& ws, unsigned long long* taken) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int kpt = (n + BS_THREADS - 1) / BS_THREADS;
+  const int i0 = tid * kpt, i1 = min(n, i0 + kpt);
+  unsigned long long mytot = 0;
+  for (int i = i0; i < i1; ++i) mytot += key_weight(keys[i]);
+  const unsigned long long tot = block_sum_u64(mytot, ws.red);
+  *taken = 0ull;
+  if (target == 0ull) return 0;
+  if (tot < target) {  // out of reach: take every candidate
+    int cnt = 0;
+    for (int i = i0; i < i1; ++i)
+      if (keys[i] != 0u) { mark(i); ++cnt; }
+    *taken = tot;
+    return block_sum_int(cnt, ws.red);
+  }
+  uint32_t prefix = 0;
+  unsigned long long above = 0;
+  int level = 0, ncand = 0;
+  for (; level < 3; ++level) {
+    const int sh = 20 - 10 * level;
+    for (int d = lane; d < 1024; d += 32) ws.hist[warp][d] = 0ull;
+    __syncwarp();
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t k = keys[i];
+      if (k != 0u && (level == 0 || (k >> (sh + 10)) == prefix))
+        atomicAdd(&ws.hist[warp][(k >> sh) & 1023u], key_weight(k));
+    }
+    __syncthreads();
+    // thread t owns buckets 1023-4t .. 1020-4t (descending)
+    unsigned long long bw[4], run = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int bk = 1023 - 4 * tid - j;
+      unsigned long long s = 0;
+#pragma unroll
+      for (int w = 0; w < BS_WARPS; ++w) s += ws.hist[w][bk];
+      bw[j] = s;
+      run += s;
+    }
+    unsigned long long total;
+    unsigned long long c = above + block_excl_scan_u64(run, ws.red, &total);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (c < target && c + bw[j] >= target) {
+        ws.prefix = (prefix << 10) | (uint32_t)(1023 - 4 * tid - j);
+        ws.above = c;
+      }
+      c += bw[j];
+    }
+    __syncthreads();
+    prefix = ws.prefix;
+    above = ws.above;
+    int cnt = 0;
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t k = keys[i];
+      cnt += (k != 0u && (k >> sh) == prefix);
+    }
+    ncand = block_sum_int(cnt, ws.red);
+    if (ncand <= SEL_CAND || level == 2) break;
+  }
+  const int sh = 20 - 10 * level;
+  const unsigned long long rem = target - above;
+  int cnt = 0;
+  unsigned long long take_w = 0;
+  if (ncand > SEL_CAND) {
+    // level 2 reached with one key value left: ties, lowest indices first
+    const unsigned long long wt = key_weight(prefix);
+    const unsigned long long need = wt ? (rem + wt - 1) / wt : 0ull;
+    int mine = 0;
+    for (int i = i0; i < i1; ++i) mine += (keys[i] != 0u && keys[i] == prefix);
+    unsigned long long ties;
+    unsigned long long rank = block_excl_scan_u64((unsigned long long)mine, ws.red, &ties);
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t k = keys[i];
+      if (k == 0u) continue;
+      if (k > prefix) { mark(i); ++cnt; }
+      else if (k == prefix) {
+        if (rank < need) { mark(i); ++cnt; }
+        ++rank;
+      }
+    }
+    take_w = (need < ties ? need : ties) * wt;
+  } else {
+    if (tid == 0) ws.ncand = 0;
+    __syncthreads();
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t k = keys[i];
+      if (k == 0u) continue;
+      if ((k >> sh) > prefix) { mark(i); ++cnt; }
+      else if ((k >> sh) == prefix) {
+        const int slot = atomicAdd(&ws.ncand, 1);
+        ws.cidx[slot] = i;
+        ws.ckey[slot] = k;
+      }
+    }
+    __syncthreads();
+    const int nc = ws.ncand;
+    for (int a = tid; a < nc; a += BS_THREADS) {
+      const uint32_t ka = ws.ckey[a];
+      const int ia = ws.cidx[a];
+      int rank = 0;
+      for (int b2 = 0; b2 < nc; ++b2) {
+        const uint32_t kb = ws.ckey[b2];
+        rank += (kb > ka) || (kb == ka && ws.cidx[b2] < ia);
+      }
+      ws.order[rank] = a;
+    }
+    if (tid == 0) { ws.last = nc - 1; ws.take_w = 0ull; }
+    __syncthreads();
+    // running weight in rank order; thread r handles rank r (nc <= SEL_CAND <= 256)
+    const unsigned long long w = (tid < nc) ? key_weight(ws.ckey[ws.order[tid]]) : 0ull;
+    unsigned long long tot_c;
+    const unsigned long long excl = block_excl_scan_u64(w, ws.red, &tot_c);
+    if (tid < nc && excl < rem && excl + w >= rem) { ws.last = tid; ws.take_w = excl + w; }
+    __syncthreads();
+    const int last = ws.last;
+    take_w = (ws.take_w != 0ull || last < 0) ? ws.take_w : tot_c;
+    if (tid <= last && tid < nc) { mark(ws.cidx[ws.order[tid]]); ++cnt; }
+    __syncthreads();
+  }
+  *taken = above + take_w;
+  return block_sum_int(cnt, ws.red);
+}
+
+}  // namespace kvq

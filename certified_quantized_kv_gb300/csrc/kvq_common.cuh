@@ -35,7 +35,8 @@ constexpr int KC_BYTES = BLK * D;          // 8192
 constexpr int VC_BYTES = BLK * D / 2;      // 4096
 constexpr int VSV_WORDS = BLK * NG;        // 256 half2
 constexpr int F16_BLOCK_BYTES = BLK * D * 2;  // 16384 bytes of FP16 per block (K or V)
-constexpr int CHUNK = 16;        // blocks per work item of the streaming kernels
+constexpr int CHUNK = 16;        // blocks per work item of the mixed and dense passes
+constexpr int SCORE_CHUNK = 8;   // blocks per work item of the scoring pass
 constexpr float KAPPA = 0.5f + 1.0f / 256.0f;
 constexpr float INV_SQRT_D = 0.088388347648318440550f;  // 1/sqrt(128), rounded to fp32
 
@@ -69,7 +70,7 @@ struct LayerView {
   int B, Hq, Hkv, n_rep, BG;
   int nb;          // full blocks of the layer
   int n_tail;      // tokens in the partial block (0..63)
-  int nbmax;       // block capacity per (sequence, KV head)
+  int nbmax;       // block capacity per (sequence, KV head), a multiple of 16
   long long cap;   // token capacity of tier 2 per (sequence, KV head)
   // tier 1 of this layer
   const int8_t* kc;      // [BG][nbmax][8192]
@@ -105,7 +106,9 @@ struct LayerView {
   HeadState* hst;        // [B*Hq]
   GroupState* gst;       // [BG]
   float* part;           // [BG][nbmax/CHUNK+1][MAXREP][D+4] partials of the mixed pass
+  float* part1;          // same shape: deltas of the second mixed pass
   float* dpart;          // [BG][nbmax/CHUNK+1][MAXREP][D+4] partials of the dense pass
+  uint32_t* mkey;        // [B][Hq][nbmax] selection keys (normalised values, fp32 bits)
   unsigned int* counters;  // work queues and completion counters (self-resetting)
 };
 
@@ -197,120 +200,26 @@ __device__ __forceinline__ float prescale_for(float xmax) {
 }
 
 // ---------------------------------------------------------------------------------
-// Warp-cooperative "top blocks covering a target" selection (radix select).
-//
-// Among n values v_i >= 0 with fixed-point weights F_i (uint64, F_i = v_i/scale * 2^62),
-// take blocks in descending v (ties: lower index first) until their F sum reaches
-// target.  Keys are the fp32 bit patterns of v (order-preserving for v >= 0).  Zero
-// values are never taken.  mark(i) is called for every taken block; the call returns
-// their count and stores the sum of their weights in *taken (same value in every lane).
-// Fixed-point integer sums make the choice independent of
-// summation order.  hist: 256 uint64 of shared memory owned by this warp.
+// Fixed-point weights of selection keys (see kvq_blocksel.cuh)
 // ---------------------------------------------------------------------------------
-template <typename KeyFn, typename WeightFn, typename MarkFn>
-__device__ int warp_select_top(int n, unsigned long long target, KeyFn key_of, WeightFn w_of,
-                               MarkFn mark, unsigned long long* hist,
-                               unsigned long long* taken) {
-  const int lane = threadIdx.x & 31;
-  *taken = 0ull;
-  if (target == 0ull) return 0;
-  // total weight of strictly positive keys
-  unsigned long long tot = 0;
-  for (int i = lane; i < n; i += 32) {
-    if (key_of(i) != 0u) tot += w_of(i);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  if (tot < target) {  // the target is out of reach: take every positive block
-    *taken = tot;
-    int cnt = 0;
-    for (int base = 0; base < n; base += 32) {   // uniform trip count for the ballot
-      const int i = base + lane;
-      const bool t = (i < n) && key_of(i) != 0u;
-      if (t) mark(i);
-      cnt += __popc(__ballot_sync(0xffffffffu, t));
-    }
-    return cnt;
-  }
-  uint32_t prefix = 0;             // decided high bits of the threshold key
-  unsigned long long above = 0;    // weight of keys strictly above the current prefix range
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    for (int d = lane; d < 256; d += 32) hist[d] = 0ull;
-    __syncwarp();
-    for (int i = lane; i < n; i += 32) {
-      const uint32_t k = key_of(i);
-      if (k == 0u) continue;
-      const bool match = (pass == 0) || ((k >> (shift + 8)) == prefix);
-      if (match) atomicAdd(&hist[(k >> shift) & 255u], w_of(i));
-    }
-    __syncwarp();
-    // lane L owns digits 255-8L .. 248-8L (descending); suffix scan from the top
-    unsigned long long loc[8];
-    unsigned long long run = 0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      loc[j] = hist[255 - 8 * lane - j];
-      run += loc[j];
-    }
-    unsigned long long incl = run;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    const unsigned long long excl = incl - run;
-    // find first digit (from the top) where above + cumulative >= target
-    int found = -1;
-    unsigned long long before = 0;
-    {
-      unsigned long long c = above + excl;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (found < 0 && c + loc[j] >= target) {
-          found = 255 - 8 * lane - j;
-          before = c;
-        }
-        c += loc[j];
-      }
-    }
-    const unsigned int has = __ballot_sync(0xffffffffu, found >= 0);
-    const int src = __ffs(has) - 1;  // lowest lane = highest digits
-    const int dsel = __shfl_sync(0xffffffffu, found, src);
-    above = __shfl_sync(0xffffffffu, before, src);
-    prefix = (prefix << 8) | (uint32_t)dsel;
-    __syncwarp();
-  }
-  // prefix is now the full threshold key; `above` = weight of keys > prefix.
-  // ties: take the lowest-index blocks with key == prefix until the target is met.
-  unsigned long long wt = 0;
-  for (int i = lane; i < n; i += 32)
-    if (key_of(i) == prefix) { wt = w_of(i); }
-  // all ties share one key, hence one weight (weights are a function of the key)
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const unsigned long long t = __shfl_xor_sync(0xffffffffu, wt, o);
-    wt = wt > t ? wt : t;
-  }
-  const unsigned long long rem = target - above;
-  const unsigned long long need = wt ? (rem + wt - 1) / wt : 0ull;
-  int cnt = 0;
-  unsigned long long ties_seen = 0;
-  for (int base = 0; base < n; base += 32) {
-    const int i = base + lane;
-    const uint32_t k = (i < n) ? key_of(i) : 0u;
-    const bool gt = (i < n) && k != 0u && k > prefix;
-    const bool eq = (i < n) && k != 0u && k == prefix;
-    const unsigned int eqm = __ballot_sync(0xffffffffu, eq);
-    const unsigned long long rank = ties_seen + __popc(eqm & ((1u << lane) - 1u));
-    const bool take = gt || (eq && rank < need);
-    if (take) mark(i);
-    cnt += __popc(__ballot_sync(0xffffffffu, take));
-    ties_seen += __popc(eqm);
-  }
-  const unsigned long long nt = need < ties_seen ? need : ties_seen;
-  *taken = above + nt * wt;
-  return cnt;
+__device__ __forceinline__ unsigned long long key_weight(uint32_t key) {
+  // floor(v * 2^62) for v = bits `key` in [0, 1], with integer shifts only (no FP64):
+  // v = m * 2^(e - 150) with the 24-bit significand m, so v * 2^62 = m * 2^(e - 88).
+  const int e = (int)(key >> 23);
+  if (e == 0) return 0ull;                     // zero or below 2^-126: weight 0
+  const unsigned long long m = (unsigned long long)((key & 0x7fffffu) | 0x800000u);
+  const int sh = e - 88;
+  if (sh >= 0) return m << sh;                 // e <= 127 keeps this below 2^63
+  if (sh <= -24) return 0ull;
+  return m >> (-sh);
 }
+
+__device__ __forceinline__ unsigned long long warp_sum_u64(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+constexpr int SEL_CAND = 256;   // candidates ranked exactly by block_select_top
 
 }  // namespace kvq

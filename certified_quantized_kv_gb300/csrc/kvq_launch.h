@@ -29,8 +29,10 @@ cudaError_t launch_export_tier1(const LayerAppend& L, int nb, void* kc, void* ks
 int score_grid(int num_sms);
 int mixed_grid(int num_sms);
 int dense_grid(int num_sms);
-cudaError_t launch_score_select(const LayerView& V, int grid, cudaStream_t st);
+cudaError_t launch_score(const LayerView& V, int grid, cudaStream_t st);
+cudaError_t launch_select(const LayerView& V, cudaStream_t st);
 cudaError_t launch_mixed(const LayerView& V, int round, int grid, cudaStream_t st);
+cudaError_t launch_combine(const LayerView& V, int round, cudaStream_t st);
 cudaError_t launch_dense(const LayerView& V, int all_dense, int grid, cudaStream_t st);
 cudaError_t launch_finalize(const LayerView& V, kvq_certificate* cert, int32_t* level,
                             cudaStream_t st);

@@ -24,9 +24,11 @@
 // then each warp (one 32-channel value group) multiplies them into V: INT4 codes on the
 // tensor cores (channels as MMA rows, tokens as k, the eight MMA columns = four heads x
 // hi/lo halves of p * scale), FP16 values of promoted blocks on the CUDA cores.  M >= every
-// score, so no online rescaling is needed.  The CTA that completes a group combines the
+// score, so no online rescaling is needed.  A second kernel combines the
 // chunk partials in a fixed order and writes the output, certificate and ladder plan.
+// (That combine runs as its own kernel, one CTA per sequence and query head.)
 #include "kvq_common.cuh"
+#include "kvq_blocksel.cuh"
 #include "kvq_launch.h"
 
 namespace kvq {
@@ -36,27 +38,18 @@ namespace {
 constexpr int KROW = D + 8;   // padded FP16 row (272 bytes): conflict-free 16-byte reads
 
 struct __align__(16) MixSmem {
-  float p[2][MAXREP][BLK];
+  float p[2][MAXREP][BLK];    // INT4-path weights
+  float pn[2][MAXREP][BLK];   // FP16-value weights / FP16 scores
   float qf[MAXREP][D];
   float M[MAXREP];
-  union __align__(16) {
-    struct {
-      __half kbuf[BLK][KROW];
-      __half vbuf[BLK][D];
-    } st;
-    struct {
-      unsigned long long hist[4][256];
-      float tail_s[MAXREP][BLK];
-      float l[MAXREP];
-      float lse[MAXREP];
-      float red[4];
-      int cnt[4];
-    } cb;
-  } u;
+  struct {
+    __half kbuf[BLK][KROW];
+    __half vbuf[BLK][D];
+  } st;
   int item;
-  int is_last;
   int skip;
 };
+
 
 __device__ __forceinline__ size_t head_row(const LayerView& V, int b, int g, int r) {
   return (size_t)b * V.Hq + (size_t)g * V.n_rep + r;
@@ -85,248 +78,15 @@ __device__ __forceinline__ void load_f16_block_dense(__half (*dst)[D], const __h
   }
 }
 
-// Combine the chunk partials of one group, add the partial block, write outputs and the
-// certificate; in the first pass also run the ranking check and plan rungs 1 and 2.
-__device__ void combine_group(const LayerView& V, int hs, int round, MixSmem& sm) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = hs / V.Hkv, g = hs % V.Hkv;
-  const int nb = V.nb;
-  const int nch = max(1, (nb + CHUNK - 1) / CHUNK);
-  const int NCH = V.nbmax / CHUNK + 1;
-  const uint8_t* kfl = (round == 0 ? V.kprom0 : V.kprom1) + (size_t)hs * V.nbmax;
-  const uint8_t* vfl = V.vprom1 + (size_t)hs * V.nbmax;
-
-  // which heads take this pass's result
-  bool take[MAXREP];
-  for (int r = 0; r < MAXREP; ++r) {
-    take[r] = false;
-    if (r < V.n_rep) {
-      const HeadState& h = V.hst[head_row(V, b, g, r)];
-      take[r] = (round == 0) || (h.planned == 1 || h.planned == 2);
-    }
-  }
-
-  // (1) chunk partials in fixed order: thread = channel
-  float acc[MAXREP];
-  for (int r = 0; r < MAXREP; ++r) acc[r] = 0.f;
-  for (int c = 0; c < nch; ++c) {
-    const float* pp = V.part + (((size_t)hs * NCH + c) * MAXREP) * (D + 4);
-    for (int r = 0; r < V.n_rep; ++r) acc[r] += pp[r * (D + 4) + tid];
-  }
-  if (warp < V.n_rep) {
-    float l = 0.f;
-    for (int c = lane; c < nch; c += 32)
-      l += V.part[(((size_t)hs * NCH + c) * MAXREP + warp) * (D + 4) + D];
-    l = warp_sum(l);
-    // (2) partial FP16 block: exact scores
-    const size_t hb = head_row(V, b, g, warp);
-    const float M = V.hst[hb].M;
-    const __half* q = V.q + hb * D;
-    float lt = 0.f;
-    for (int t = lane; t < V.n_tail; t += 32) {
-      const __half* k = V.tail_k + ((size_t)hs * BLK + t) * D;
-      float s = 0.f;
-      for (int c = 0; c < D; c += 2) {
-        const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(k + c));
-        const float2 qq = __half22float2(*reinterpret_cast<const __half2*>(q + c));
-        s = fmaf(qq.x, kk.x, s);
-        s = fmaf(qq.y, kk.y, s);
-      }
-      const float p = expf(s * INV_SQRT_D - M);
-      sm.u.cb.tail_s[warp][t] = p;
-      lt += p;
-    }
-    lt = warp_sum(lt);
-    if (lane == 0) {
-      sm.u.cb.l[warp] = l + lt;
-      sm.u.cb.lse[warp] = lt;  // tail mass numerator, normalised below
-    }
-  }
-  __syncthreads();
-  for (int r = 0; r < V.n_rep; ++r) {
-    float a = acc[r];
-    for (int t = 0; t < V.n_tail; ++t)
-      a += sm.u.cb.tail_s[r][t] * __half2float(V.tail_v[((size_t)hs * BLK + t) * D + tid]);
-    if (take[r]) {
-      const size_t hb = head_row(V, b, g, r);
-      V.out[hb * D + tid] = __float2half_rn(a / sm.u.cb.l[r]);
-    }
-  }
-  // value range R = max_c (vmax_c - vmin_c)
-  float rng = ord2f(V.vmax[hs * D + tid]) - ord2f(V.vmin[hs * D + tid]);
-  rng = warp_max(rng);
-  if (lane == 0) sm.u.cb.red[warp] = rng;
-  __syncthreads();
-  const float R = fmaxf(fmaxf(sm.u.cb.red[0], sm.u.cb.red[1]), fmaxf(sm.u.cb.red[2], sm.u.cb.red[3]));
-
-  // (3) certificate per head: warp = head slot
-  if (warp < V.n_rep && take[warp]) {
-    const int r = warp;
-    const size_t hb = head_row(V, b, g, r);
-    HeadState hsd = V.hst[hb];
-    const float L = sm.u.cb.l[r];
-    const float LSEp = hsd.M + logf(L);
-    const float tail_mass = sm.u.cb.lse[r] / L;
-    const float* lse8 = V.lse8 + hb * V.nbmax;
-    const float* lse16 = V.lse16 + hb * V.nbmax;
-    const float* dl = V.delta + hb * V.nbmax;
-    const float* eta = V.eta + (size_t)hs * V.nbmax;
-    float S = 0.f, A = 0.f, Ev = 0.f;
-    for (int i = lane; i < nb; i += 32) {
-      const bool kp = kfl[i] != 0;
-      const float pm = expf((kp ? lse16[i] : lse8[i]) - LSEp);
-      if (kp) {
-        A += pm;
-      } else {
-        S += pm * expm1f(dl[i]);
-        A += pm * expf(-dl[i]);
-      }
-      if (!vfl[i]) Ev += pm * eta[i];
-    }
-    S = warp_sum(S);
-    A = warp_sum(A) + tail_mass;
-    Ev = warp_sum(Ev);
-    const float e_key = S / A * R;
-    const float e_val = Ev;
-    hsd.e_key = e_key;
-    hsd.e_val = e_val;
-
-    if (round == 0) {
-      // ranking-consistency check over S_h: top-R positions by INT8 and by FP16 log-mass
-      const uint8_t* sel = V.sel + hb * V.nbmax;
-      bool ok = true;
-      if (hsd.k_star > 1) {
-        float last8 = INFINITY, last16 = INFINITY;
-        int idx8 = -1, idx16 = -1;
-        const int R_rank = min(V.rank_positions, hsd.k_star);
-        for (int pos = 0; pos < R_rank && ok; ++pos) {
-          // next entry after (last, idx) in descending order, ties to lower index
-          float b8 = -INFINITY, b16 = -INFINITY;
-          int i8 = 0x7fffffff, i16 = 0x7fffffff;
-          for (int i = lane; i < nb; i += 32) {
-            if (!sel[i]) continue;
-            const float x8 = lse8[i], x16 = lse16[i];
-            const bool after8 = (x8 < last8) || (x8 == last8 && i > idx8);
-            const bool after16 = (x16 < last16) || (x16 == last16 && i > idx16);
-            if (after8 && (x8 > b8 || (x8 == b8 && i < i8))) { b8 = x8; i8 = i; }
-            if (after16 && (x16 > b16 || (x16 == b16 && i < i16))) { b16 = x16; i16 = i; }
-          }
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) {
-            const float ob8 = __shfl_xor_sync(0xffffffffu, b8, o);
-            const int oi8 = __shfl_xor_sync(0xffffffffu, i8, o);
-            if (ob8 > b8 || (ob8 == b8 && oi8 < i8)) { b8 = ob8; i8 = oi8; }
-            const float ob16 = __shfl_xor_sync(0xffffffffu, b16, o);
-            const int oi16 = __shfl_xor_sync(0xffffffffu, i16, o);
-            if (ob16 > b16 || (ob16 == b16 && oi16 < i16)) { b16 = ob16; i16 = oi16; }
-          }
-          ok = (i8 == i16);
-          last8 = b8; idx8 = i8; last16 = b16; idx16 = i16;
-        }
-      }
-      if (V.debug & 0x1) ok = false;
-      hsd.rank_ok = ok ? 1 : 0;
-      int planned = 0;
-      if (!ok) {
-        planned = 3;
-      } else if (!(e_key + e_val <= V.eps)) {
-        const float eps = V.eps;
-        float S_proj = S;
-        uint8_t* k1 = V.kprom1 + (size_t)hs * V.nbmax;
-        uint8_t* v1 = V.vprom1 + (size_t)hs * V.nbmax;
-        if (e_key > eps * 0.5f) {
-          planned = 1;
-          // rung 1: take INT8 blocks by descending mass_b (e^Delta_b - 1) until the
-          // removed share reaches S - eps A / (2R)
-          const double need = 1.0 - (double)eps * (double)A / (2.0 * (double)R * (double)S);
-          auto key_of = [&](int i) -> uint32_t {
-            if (kfl[i]) return 0u;
-            const float pm = expf(lse8[i] - LSEp);
-            return __float_as_uint(pm * expm1f(dl[i]));
-          };
-          auto w_of = [&](int i) -> unsigned long long {
-            return fixed62((double)__uint_as_float(key_of(i)) / (double)S);
-          };
-          auto mark = [&](int i) { k1[i] = 1; };
-          unsigned long long taken = 0;
-          warp_select_top(nb, fixed62(need), key_of, w_of, mark, sm.u.cb.hist[warp], &taken);
-          S_proj = (float)((double)S * (1.0 - (double)taken / 4611686018427387904.0));
-          if (S_proj < 0.f) S_proj = 0.f;
-        }
-        const float ekey_proj = S_proj / A * R;
-        if (!(ekey_proj + e_val <= eps)) {
-          planned = 2;
-          if (e_val > 0.f) {
-            const double need = 1.0 - ((double)eps - (double)ekey_proj) / (double)e_val;
-            auto key_of = [&](int i) -> uint32_t {
-              if (vfl[i]) return 0u;
-              const float pm = expf((kfl[i] ? lse16[i] : lse8[i]) - LSEp);
-              return __float_as_uint(pm * eta[i]);
-            };
-            auto w_of = [&](int i) -> unsigned long long {
-              return fixed62((double)__uint_as_float(key_of(i)) / (double)e_val);
-            };
-            auto mark = [&](int i) { v1[i] = 1; };
-            unsigned long long taken = 0;
-            warp_select_top(nb, fixed62(need), key_of, w_of, mark, sm.u.cb.hist[warp], &taken);
-          }
-        }
-      }
-      hsd.planned = planned;
-      hsd.level1 = planned;  // rungs 1/2 are confirmed (or raised to 3) by the second pass
-    } else {
-      hsd.level1 = (e_key + e_val <= V.eps) ? hsd.planned : 3;
-    }
-    if (lane == 0) V.hst[hb] = hsd;
-  }
-  __syncthreads();
-  // group bookkeeping
-  if (round == 0) {
-    if (tid == 0) {
-      int need = 0;
-      for (int r = 0; r < V.n_rep; ++r) {
-        const int p = V.hst[head_row(V, b, g, r)].planned;
-        need |= (p == 1 || p == 2);
-      }
-      V.gst[hs].need_round1 = need;
-    }
-  } else {
-    int nk = 0, nv = 0;
-    for (int i = tid; i < nb; i += blockDim.x) {
-      nk += V.kprom1[(size_t)hs * V.nbmax + i];
-      nv += V.vprom1[(size_t)hs * V.nbmax + i];
-    }
-    nk = (int)warp_sum((float)nk);
-    nv = (int)warp_sum((float)nv);
-    if (lane == 0) sm.u.cb.cnt[warp] = nk | (nv << 16);
-    __syncthreads();
-    if (tid == 0) {
-      int tk = 0, tv = 0;
-      for (int w = 0; w < 4; ++w) { tk += sm.u.cb.cnt[w] & 0xffff; tv += sm.u.cb.cnt[w] >> 16; }
-      GroupState gs = V.gst[hs];
-      gs.n_kprom1 = tk;
-      gs.n_vprom1 = tv;
-      gs.bytes += (long long)(tk + tv) * F16_BLOCK_BYTES;
-      V.gst[hs] = gs;
-      for (int r = 0; r < V.n_rep; ++r) {
-        HeadState& h = V.hst[head_row(V, b, g, r)];
-        if (h.planned == 1 || h.planned == 2) h.n_vprom = tv;
-      }
-    }
-  }
-}
-
 }  // namespace
 
-__global__ void __launch_bounds__(128) mixed_kernel(LayerView V, int round) {
+__global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
   __shared__ MixSmem sm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int nch = max(1, (V.nb + CHUNK - 1) / CHUNK);
   const int NCH = V.nbmax / CHUNK + 1;
   const int total = V.BG * nch;
-  unsigned int* cnt_group = V.counters + CNT_GROUP_BASE + (1 + round) * V.BG;
-  const uint8_t* kflags = round == 0 ? V.kprom0 : V.kprom1;
   int par = 0;
   int cur_hs = -1;
   float pre_v = 1.f;
@@ -367,32 +127,40 @@ __global__ void __launch_bounds__(128) mixed_kernel(LayerView V, int round) {
     float lsum = 0.f;    // sum p for head = warp
 
     const int blk_end = min(V.nb, (ch + 1) * CHUNK);
-    for (int blk = ch * CHUNK; blk < blk_end; ++blk, par ^= 1) {
+    for (int blk = ch * CHUNK; blk < blk_end; ++blk) {
       const size_t bi = (size_t)hs * V.nbmax + blk;
-      const bool kp = kflags[bi] != 0;
-      const bool vp = (round == 1) && V.vprom1[bi] != 0;
-      // ---- stage 1: p_t = exp(s'_t - M) for the group's query heads ----
-      if (!kp) {
-        const int r = warp;
-        float p0 = 0.f, p1 = 0.f;
-        if (r < V.n_rep) {
-          const float2 s2 = __ldcs(reinterpret_cast<const float2*>(
-              V.shat + head_row(V, b, g, r) * ((size_t)V.nbmax * BLK) + (size_t)blk * BLK + 2 * lane));
-          p0 = __expf(s2.x - sm.M[r]);
-          p1 = __expf(s2.y - sm.M[r]);
-        }
-        sm.p[par][r][2 * lane] = p0;
-        sm.p[par][r][2 * lane + 1] = p1;
-        lsum += p0 + p1;
-      } else {
-        load_f16_block(sm.u.st.kbuf, V.t2k + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
+      const bool kp0 = V.kprom0[bi] != 0;
+      bool newk = false, vp = false;
+      if (round == 1) {
+        newk = !kp0 && V.kprom1[bi] != 0;
+        vp = V.vprom1[bi] != 0;
+        if (!newk && !vp) continue;   // precision unchanged: contribution unchanged
+      }
+      par ^= 1;
+      const int r = warp;
+      const bool act = r < V.n_rep;
+      float* shat_r = V.shat + head_row(V, b, g, act ? r : 0) * ((size_t)V.nbmax * BLK) + (size_t)blk * BLK;
+      const bool need_k16 = (round == 0) ? kp0 : newk;
+      // ---- stage 1: probabilities of the block's 64 tokens for the group's heads ----
+      // Round 0: p = exp(s' - M), s' = FP16 score on promoted blocks (computed from tier 2
+      // and kept in the score scratch for the second pass), INT8 score elsewhere.
+      // Round 1: INT4 weights = p_new - p_old (or -p_old where the values are promoted);
+      // FP16-value weights = p_new.
+      float so0 = 0.f, so1 = 0.f;
+      if (act && (round == 1 || !kp0)) {
+        so0 = __ldcs(shat_r + lane);
+        so1 = __ldcs(shat_r + lane + 32);
+      }
+      float sn0 = so0, sn1 = so1;
+      if (need_k16) {
+        load_f16_block(sm.st.kbuf, V.t2k + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
         __syncthreads();
         {
           const int t = tid & 63, rp = (tid >> 6) * 2;  // heads rp, rp+1
           float s0 = 0.f, s1 = 0.f;
 #pragma unroll 4
           for (int c = 0; c < D; c += 8) {
-            const uint4 kv = *reinterpret_cast<const uint4*>(&sm.u.st.kbuf[t][c]);
+            const uint4 kv = *reinterpret_cast<const uint4*>(&sm.st.kbuf[t][c]);
             const __half2* k2 = reinterpret_cast<const __half2*>(&kv);
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -403,34 +171,51 @@ __global__ void __launch_bounds__(128) mixed_kernel(LayerView V, int round) {
               s1 = fmaf(sm.qf[rp + 1][c + 2 * j + 1], kf.y, s1);
             }
           }
-          sm.p[par][rp][t] = s0 * INV_SQRT_D;
-          sm.p[par][rp + 1][t] = s1 * INV_SQRT_D;
+          sm.pn[par][rp][t] = s0 * INV_SQRT_D;
+          sm.pn[par][rp + 1][t] = s1 * INV_SQRT_D;
         }
         __syncthreads();
-        {
-          const int r = warp;
-          const float x0 = sm.p[par][r][lane], x1 = sm.p[par][r][lane + 32];
-          float p0 = 0.f, p1 = 0.f;
-          if (r < V.n_rep) {
-            const float m = warp_max(fmaxf(x0, x1));
-            const float l = warp_sum(expf(x0 - m) + expf(x1 - m));
-            if (lane == 0) V.lse16[head_row(V, b, g, r) * V.nbmax + blk] = m + logf(l);
-            p0 = expf(x0 - sm.M[r]);
-            p1 = expf(x1 - sm.M[r]);
-          }
-          sm.p[par][r][lane] = p0;
-          sm.p[par][r][lane + 32] = p1;
-          lsum += p0 + p1;
+        sn0 = sm.pn[par][r][lane];
+        sn1 = sm.pn[par][r][lane + 32];
+        if (act) {
+          const float m = warp_max(fmaxf(sn0, sn1));
+          const float l = warp_sum(expf(sn0 - m) + expf(sn1 - m));
+          if (lane == 0) V.lse16[head_row(V, b, g, r) * V.nbmax + blk] = m + logf(l);
+          shat_r[lane] = sn0;
+          shat_r[lane + 32] = sn1;
         }
       }
+      float pn0 = 0.f, pn1 = 0.f, pi0 = 0.f, pi1 = 0.f;
+      if (act) {
+        const float M = sm.M[r];
+        if (round == 0) {
+          pn0 = kp0 ? expf(sn0 - M) : __expf(sn0 - M);
+          pn1 = kp0 ? expf(sn1 - M) : __expf(sn1 - M);
+          pi0 = pn0;
+          pi1 = pn1;
+          lsum += pn0 + pn1;
+        } else {
+          const float po0 = kp0 ? expf(so0 - M) : __expf(so0 - M);   // as the first pass
+          const float po1 = kp0 ? expf(so1 - M) : __expf(so1 - M);
+          pn0 = newk ? expf(sn0 - M) : po0;
+          pn1 = newk ? expf(sn1 - M) : po1;
+          pi0 = vp ? -po0 : pn0 - po0;
+          pi1 = vp ? -po1 : pn1 - po1;
+          lsum += (pn0 - po0) + (pn1 - po1);
+        }
+      }
+      sm.p[par][r][lane] = pi0;
+      sm.p[par][r][lane + 32] = pi1;
+      sm.pn[par][r][lane] = pn0;
+      sm.pn[par][r][lane + 32] = pn1;
       __syncthreads();
-      // ---- stage 2: p x V for the warp's value group ----
-      if (!vp) {
+      // ---- stage 2: weights x V for the warp's value group ----
+      {
         const uint4* vcp = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES) + (warp * 2) * 32 + lane;
         const uint4 C0 = __ldcs(vcp), C1 = __ldcs(vcp + 32);
         const uint4* svp = reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS + warp * BLK + 16 * tig);
-        const int r = gid >> 1;
-        const float* pr = &sm.p[par][r][16 * tig];
+        const int rr = gid >> 1;
+        const float* pr = &sm.p[par][rr][16 * tig];
         uint32_t bb0[4], bb1[4];
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
@@ -460,17 +245,18 @@ __global__ void __launch_bounds__(128) mixed_kernel(LayerView V, int round) {
                      nib_to_f16(w, 3), bb0[kk], bb1[kk]);
           }
         }
-      } else {
-        load_f16_block_dense(sm.u.st.vbuf, V.t2v + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
+      }
+      if (vp) {
+        load_f16_block_dense(sm.st.vbuf, V.t2v + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
         __syncthreads();
         const int c0 = 32 * warp + gid;
-        const float* pr = sm.p[par][tig];
+        const float* pr = sm.pn[par][tig];
         for (int t = 0; t < BLK; ++t) {
           const float pt = pr[t];
-          acc16[0] = fmaf(pt, __half2float(sm.u.st.vbuf[t][c0]), acc16[0]);
-          acc16[1] = fmaf(pt, __half2float(sm.u.st.vbuf[t][c0 + 8]), acc16[1]);
-          acc16[2] = fmaf(pt, __half2float(sm.u.st.vbuf[t][c0 + 16]), acc16[2]);
-          acc16[3] = fmaf(pt, __half2float(sm.u.st.vbuf[t][c0 + 24]), acc16[3]);
+          acc16[0] = fmaf(pt, __half2float(sm.st.vbuf[t][c0]), acc16[0]);
+          acc16[1] = fmaf(pt, __half2float(sm.st.vbuf[t][c0 + 8]), acc16[1]);
+          acc16[2] = fmaf(pt, __half2float(sm.st.vbuf[t][c0 + 16]), acc16[2]);
+          acc16[3] = fmaf(pt, __half2float(sm.st.vbuf[t][c0 + 24]), acc16[3]);
         }
       }
     }
@@ -480,7 +266,7 @@ __global__ void __launch_bounds__(128) mixed_kernel(LayerView V, int round) {
     off += __shfl_xor_sync(0xffffffffu, off, 2);
     const float offh = __shfl_sync(0xffffffffu, off, 8 * tig);  // head tig, hi lane
     const float inv = 1.f / pre_v;
-    float* pp = V.part + (((size_t)hs * NCH + ch) * MAXREP) * (D + 4);
+    float* pp = (round == 0 ? V.part : V.part1) + (((size_t)hs * NCH + ch) * MAXREP) * (D + 4);
     if (tig < V.n_rep) {
       float* pr = pp + tig * (D + 4);
       const int c0 = 32 * warp + gid;
@@ -493,19 +279,6 @@ __global__ void __launch_bounds__(128) mixed_kernel(LayerView V, int round) {
     if (lane == 0 && warp < V.n_rep) pp[warp * (D + 4) + D] = lsum;
 
     __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      const unsigned int old = atomicAdd(&cnt_group[hs], 1u);
-      sm.is_last = (old == (unsigned int)(nch - 1));
-    }
-    __syncthreads();
-    if (sm.is_last) {
-      __threadfence();
-      combine_group(V, hs, round, sm);
-      if (tid == 0) cnt_group[hs] = 0u;
-      cur_hs = -1;  // the union was reused by the combine
-    }
-    __syncthreads();
   }
   if (tid == 0) {
     const unsigned int old = atomicAdd(&V.counters[CNT_MIX_EXIT], 1u);
@@ -516,10 +289,224 @@ __global__ void __launch_bounds__(128) mixed_kernel(LayerView V, int round) {
   }
 }
 
+// One CTA of 256 threads per (sequence, query head): combine the chunk partials of a
+// pass for the head, add the partial block, write the output and the certificate and,
+// after the first pass, run the ranking check and plan rungs 1-2.
+__global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int round) {
+  extern __shared__ __align__(16) unsigned char comb_dsm[];
+  BlockSelSmem& ws = *reinterpret_cast<BlockSelSmem*>(comb_dsm);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(comb_dsm + sizeof(BlockSelSmem));   // [nb padded]
+  __shared__ float acc_s[2][D];
+  __shared__ float l_s[2];
+  __shared__ float tail_p[BLK];
+  const int tid = threadIdx.x;
+  const int bh = blockIdx.x;
+  const int b = bh / V.Hq, h = bh % V.Hq, g = h / V.n_rep, r = h % V.n_rep;
+  const int hs = b * V.Hkv + g;
+  const size_t hb = (size_t)bh;
+  const int nb = V.nb;
+  const int nch = max(1, (nb + CHUNK - 1) / CHUNK);
+  const int NCH = V.nbmax / CHUNK + 1;
+  const uint8_t* kfl = (round == 0 ? V.kprom0 : V.kprom1) + (size_t)hs * V.nbmax;
+  // first pass: no FP16 values yet (every head's rung 2 plans against this empty set,
+  // while its marks accumulate in vprom1 for the second pass)
+  const uint8_t* vfl = round == 0 ? nullptr : V.vprom1 + (size_t)hs * V.nbmax;
+  HeadState hsd = V.hst[hb];
+  if (round == 1) {
+    if (!V.gst[hs].need_round1) return;
+    int nk = 0, nv = 0;
+    for (int i16 = tid; i16 < (nb + 15) / 16; i16 += BS_THREADS) {
+      const uint4 a = reinterpret_cast<const uint4*>(V.kprom1 + (size_t)hs * V.nbmax)[i16];
+      const uint4 c = reinterpret_cast<const uint4*>(V.vprom1 + (size_t)hs * V.nbmax)[i16];
+      nk += __popc(a.x) + __popc(a.y) + __popc(a.z) + __popc(a.w);
+      nv += __popc(c.x) + __popc(c.y) + __popc(c.z) + __popc(c.w);
+    }
+    nk = block_sum_int(nk, ws.red);
+    nv = block_sum_int(nv, ws.red);
+    if (r == 0 && tid == 0) {
+      GroupState gs = V.gst[hs];
+      gs.n_kprom1 = nk;
+      gs.n_vprom1 = nv;
+      // the second pass pages in only the newly promoted key blocks and the value blocks
+      gs.bytes += (long long)(nk - gs.n_kprom0 + nv) * F16_BLOCK_BYTES;
+      V.gst[hs] = gs;
+    }
+    if (!(hsd.planned == 1 || hsd.planned == 2)) return;
+    hsd.n_vprom = nv;
+  }
+  // (1) chunk partials in a fixed order: thread = (channel, half of the chunks)
+  {
+    const int c = tid & (D - 1), half = tid >> 7;
+    float a = 0.f, l = 0.f;
+#pragma unroll 4
+    for (int ch = half; ch < nch; ch += 2) {
+      const size_t o = (((size_t)hs * NCH + ch) * MAXREP + r) * (D + 4);
+      a += V.part[o + c];
+      if (round == 1) a += V.part1[o + c];
+      if (c == 0) l += V.part[o + D] + (round == 1 ? V.part1[o + D] : 0.f);
+    }
+    acc_s[half][c] = a;
+    if (c == 0) l_s[half] = l;
+  }
+  // (2) the partial FP16 block with exact scores
+  float lt = 0.f;
+  if (tid < V.n_tail) {
+    const __half* q = V.q + hb * D;
+    const __half* k = V.tail_k + ((size_t)hs * BLK + tid) * D;
+    float sc = 0.f;
+    for (int c = 0; c < D; c += 2) {
+      const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(k + c));
+      const float2 qq = __half22float2(*reinterpret_cast<const __half2*>(q + c));
+      sc = fmaf(qq.x, kk.x, sc);
+      sc = fmaf(qq.y, kk.y, sc);
+    }
+    lt = expf(sc * INV_SQRT_D - hsd.M);
+    tail_p[tid] = lt;
+  }
+  lt = block_sum(lt, ws.red);   // synchronises acc_s, l_s and tail_p too
+  const float L = l_s[0] + l_s[1] + lt;
+  if (tid < D) {
+    float a = acc_s[0][tid] + acc_s[1][tid];
+    for (int t = 0; t < V.n_tail; ++t)
+      a += tail_p[t] * __half2float(V.tail_v[((size_t)hs * BLK + t) * D + tid]);
+    V.out[hb * D + tid] = __float2half_rn(a / L);
+  }
+  // value range R = max_c (vmax_c - vmin_c)
+  const float R = block_max(tid < D ? ord2f(V.vmax[hs * D + tid]) - ord2f(V.vmin[hs * D + tid]) : -INFINITY, ws.red);
+  // (3) certificate
+  const float LSEp = hsd.M + logf(L);
+  const float tail_mass = lt / L;
+  const float* lse8 = V.lse8 + hb * V.nbmax;
+  const float* lse16 = V.lse16 + hb * V.nbmax;
+  const float* dl = V.delta + hb * V.nbmax;
+  const float* eta = V.eta + (size_t)hs * V.nbmax;
+  float S = 0.f, A = 0.f, Ev = 0.f;
+  for (int i = tid; i < nb; i += BS_THREADS) {
+    const bool kp = kfl[i] != 0;
+    const float pm = expf((kp ? lse16[i] : lse8[i]) - LSEp);
+    if (kp) {
+      A += pm;
+    } else {
+      S += pm * expm1f(dl[i]);
+      A += pm * expf(-dl[i]);
+    }
+    if (!vfl || !vfl[i]) Ev += pm * eta[i];
+  }
+  S = block_sum(S, ws.red);
+  A = block_sum(A, ws.red) + tail_mass;
+  Ev = block_sum(Ev, ws.red);
+  const float e_key = S / A * R;
+  const float e_val = Ev;
+  hsd.e_key = e_key;
+  hsd.e_val = e_val;
+  if (round == 1) {
+    hsd.level1 = (e_key + e_val <= V.eps) ? hsd.planned : 3;
+    if (tid == 0) V.hst[hb] = hsd;
+    return;
+  }
+  // (4) ranking-consistency check over S_h: top-R positions by INT8 and FP16 log-mass
+  const uint8_t* sel = V.sel + hb * V.nbmax;
+  bool ok = true;
+  if (hsd.k_star > 1) {
+    float last8 = INFINITY, last16 = INFINITY;
+    int idx8 = -1, idx16 = -1;
+    const int R_rank = min(V.rank_positions, hsd.k_star);
+    for (int pos = 0; pos < R_rank && ok; ++pos) {
+      float b8 = -INFINITY, b16 = -INFINITY;
+      int i8 = 0x7fffffff, i16 = 0x7fffffff;
+      for (int i = tid; i < nb; i += BS_THREADS) {
+        if (!sel[i]) continue;
+        const float x8 = lse8[i], x16 = lse16[i];
+        const bool after8 = (x8 < last8) || (x8 == last8 && i > idx8);
+        const bool after16 = (x16 < last16) || (x16 == last16 && i > idx16);
+        if (after8 && (x8 > b8 || (x8 == b8 && i < i8))) { b8 = x8; i8 = i; }
+        if (after16 && (x16 > b16 || (x16 == b16 && i < i16))) { b16 = x16; i16 = i; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ob8 = __shfl_xor_sync(0xffffffffu, b8, o);
+        const int oi8 = __shfl_xor_sync(0xffffffffu, i8, o);
+        if (ob8 > b8 || (ob8 == b8 && oi8 < i8)) { b8 = ob8; i8 = oi8; }
+        const float ob16 = __shfl_xor_sync(0xffffffffu, b16, o);
+        const int oi16 = __shfl_xor_sync(0xffffffffu, i16, o);
+        if (ob16 > b16 || (ob16 == b16 && oi16 < i16)) { b16 = ob16; i16 = oi16; }
+      }
+      __syncthreads();
+      if ((tid & 31) == 0) {
+        ws.red.f[tid >> 5] = b8;
+        ws.red.i[tid >> 5] = i8;
+        ws.cidx[tid >> 5] = i16;
+        ws.ckey[tid >> 5] = __float_as_uint(b16);
+      }
+      __syncthreads();
+      for (int w = 0; w < BS_WARPS; ++w) {
+        const float ob8 = ws.red.f[w], ob16 = __uint_as_float(ws.ckey[w]);
+        const int oi8 = ws.red.i[w], oi16 = ws.cidx[w];
+        if (ob8 > b8 || (ob8 == b8 && oi8 < i8)) { b8 = ob8; i8 = oi8; }
+        if (ob16 > b16 || (ob16 == b16 && oi16 < i16)) { b16 = ob16; i16 = oi16; }
+      }
+      ok = (i8 == i16);
+      last8 = b8; idx8 = i8; last16 = b16; idx16 = i16;
+    }
+    __syncthreads();
+  }
+  if (V.debug & 0x1) ok = false;
+  hsd.rank_ok = ok ? 1 : 0;
+  int planned = 0;
+  if (!ok) {
+    planned = 3;
+  } else if (!(e_key + e_val <= V.eps)) {
+    const float eps = V.eps;
+    float S_proj = S;
+    uint8_t* k1 = V.kprom1 + (size_t)hs * V.nbmax;
+    uint8_t* v1 = V.vprom1 + (size_t)hs * V.nbmax;
+    if (e_key > eps * 0.5f) {
+      planned = 1;
+      // rung 1: INT8 blocks by descending mass_b (e^Delta_b - 1) until the removed share
+      // of S reaches 1 - eps A / (2 R S)
+      const double need = 1.0 - (double)eps * (double)A / (2.0 * (double)R * (double)S);
+      for (int i = tid; i < nb; i += BS_THREADS)
+        keys[i] = kfl[i] ? 0u : __float_as_uint(expf(lse8[i] - LSEp) * expm1f(dl[i]) / S);
+      __syncthreads();
+      unsigned long long taken = 0;
+      block_select_top(nb, keys, fixed62(need), [&](int i) { k1[i] = 1; }, ws, &taken);
+      S_proj = (float)((double)S * (1.0 - (double)taken / 4611686018427387904.0));
+      if (S_proj < 0.f) S_proj = 0.f;
+      __syncthreads();
+    }
+    const float ekey_proj = S_proj / A * R;
+    if (!(ekey_proj + e_val <= eps)) {
+      planned = 2;
+      if (e_val > 0.f) {
+        // rung 2: FP16 values by descending mass_b eta_b until the projected
+        // E_key + E_val <= eps (every block is a candidate: no values are FP16 yet)
+        const double need = 1.0 - ((double)eps - (double)ekey_proj) / (double)e_val;
+        for (int i = tid; i < nb; i += BS_THREADS)
+          keys[i] = __float_as_uint(expf((kfl[i] ? lse16[i] : lse8[i]) - LSEp) * eta[i] / e_val);
+        __syncthreads();
+        unsigned long long taken = 0;
+        block_select_top(nb, keys, fixed62(need), [&](int i) { v1[i] = 1; }, ws, &taken);
+      }
+    }
+    if (tid == 0 && planned > 0) V.gst[hs].need_round1 = 1;
+  }
+  hsd.planned = planned;
+  hsd.level1 = planned;   // rungs 1/2 are confirmed, or raised to 3, by the second pass
+  if (tid == 0) V.hst[hb] = hsd;
+}
+
 int mixed_grid(int num_sms) { return num_sms * 4; }
 
 cudaError_t launch_mixed(const LayerView& V, int round, int grid, cudaStream_t st) {
   mixed_kernel<<<grid, 128, 0, st>>>(V, round);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const LayerView& V, int round, cudaStream_t st) {
+  const size_t dyn = sizeof(BlockSelSmem) + (size_t)((V.nb + 15) & ~15) * 4;
+  cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  combine_kernel<<<V.B * V.Hq, BS_THREADS, dyn, st>>>(V, round);
   return cudaGetLastError();
 }
 

@@ -15,12 +15,13 @@
 // exact fp32 product q_c s_{b,c} (scaled by a power of two), so the f16 MMA reproduces
 // the fp32 product exactly.  The INT8 codes convert to f16 exactly in registers.
 //
-// The CTA that finishes the last block of a (sequence, KV head) selects, per query head,
+// A second kernel (one CTA per sequence and query head) selects, per query head,
 // the fewest blocks covering tau_cov of exp(lse8_b - LSE) (descending mass, ties to the
 // lower block index; the partial FP16 block counts as covered), with fixed-point sums so
 // the choice does not depend on summation order; the union over the group is the set of
 // blocks whose FP16 keys are paged in.
 #include "kvq_common.cuh"
+#include "kvq_blocksel.cuh"
 #include "kvq_launch.h"
 
 namespace kvq {
@@ -33,142 +34,22 @@ struct ScoreSmem {
   float red_m[2][4][MAXREP];         // per-warp block max  [parity][warp][head]
   float red_l[2][4][MAXREP];
   float qmax[MAXREP];
-  unsigned long long hist[4][256];   // selection histograms, one per warp
-  float tail_s[MAXREP][BLK];
   int item;
-  int is_last;
-  int cnt[4];
 };
+
 
 __device__ __forceinline__ size_t head_row(const LayerView& V, int b, int g, int r) {
   return (size_t)b * V.Hq + (size_t)g * V.n_rep + r;
 }
 
-// Exact scores of the partial (FP16) block for head slot r, kept in shared memory;
-// returns the log-sum-exp over them (-inf if the block is empty) and their max.
-__device__ void tail_scores(const LayerView& V, int hs, int b, int g, int r, ScoreSmem& sm,
-                            float& tail_lse, float& tail_max) {
-  const int lane = threadIdx.x & 31;
-  const __half* q = V.q + head_row(V, b, g, r) * D;
-  float m = -INFINITY;
-  for (int t = lane; t < V.n_tail; t += 32) {
-    const __half* k = V.tail_k + ((size_t)hs * BLK + t) * D;
-    float s = 0.f;
-    for (int c = 0; c < D; c += 2) {
-      const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(k + c));
-      const float2 qq = __half22float2(*reinterpret_cast<const __half2*>(q + c));
-      s = fmaf(qq.x, kk.x, s);
-      s = fmaf(qq.y, kk.y, s);
-    }
-    s *= INV_SQRT_D;
-    sm.tail_s[r][t] = s;
-    m = fmaxf(m, s);
-  }
-  m = warp_max(m);
-  float l = 0.f;
-  for (int t = lane; t < V.n_tail; t += 32) l += expf(sm.tail_s[r][t] - m);
-  l = warp_sum(l);
-  tail_max = m;
-  tail_lse = (V.n_tail > 0) ? m + logf(l) : -INFINITY;
-}
-
-__device__ __forceinline__ unsigned long long weight_of_key(uint32_t key) {
-  // key = bits of a mass in [0, 1]; weight = mass * 2^62, exact for mass >= 2^-38
-  return (unsigned long long)((double)__uint_as_float(key) * 4611686018427387904.0);
-}
-
-// Selection for one (sequence, KV head): warp r handles query head slot r.
-__device__ void select_group(const LayerView& V, int hs, ScoreSmem& sm) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = hs / V.Hkv, g = hs % V.Hkv;
-  const int nb = V.nb;
-  int kstar = 0;
-  if (warp < V.n_rep) {
-    const int r = warp;
-    const size_t hb = head_row(V, b, g, r);
-    float tail_lse, tail_max;
-    tail_scores(V, hs, b, g, r, sm, tail_lse, tail_max);
-    const float* lse8 = V.lse8 + hb * V.nbmax;
-    const float* dl = V.delta + hb * V.nbmax;
-    float m = tail_lse, mref = tail_max;
-    for (int i = lane; i < nb; i += 32) {
-      const float x = lse8[i];
-      m = fmaxf(m, x);
-      mref = fmaxf(mref, x + dl[i]);
-    }
-    m = warp_max(m);
-    mref = warp_max(mref);
-    float s = 0.f;
-    for (int i = lane; i < nb; i += 32) s += expf(lse8[i] - m);
-    s = warp_sum(s);
-    if (V.n_tail > 0) s += expf(tail_lse - m);
-    const float LSE = m + logf(s);
-    const double tail_mass = (V.n_tail > 0) ? (double)expf(tail_lse - LSE) : 0.0;
-    const double need = (double)V.tau - tail_mass;
-    unsigned long long target = 0ull;
-    if (need > 0.0) target = (unsigned long long)ceil(need * 4611686018427387904.0);
-    uint8_t* sel = V.sel + hb * V.nbmax;
-    for (int i = lane; i < nb; i += 32) sel[i] = 0;
-    __syncwarp();
-    auto key_of = [&](int i) -> uint32_t { return __float_as_uint(expf(lse8[i] - LSE)); };
-    auto w_of = [&](int i) -> unsigned long long { return weight_of_key(key_of(i)); };
-    auto mark = [&](int i) { sel[i] = 1; };
-    unsigned long long taken = 0;
-    kstar = warp_select_top(nb, target, key_of, w_of, mark, sm.hist[warp], &taken);
-    if (lane == 0) {
-      HeadState hsd;
-      hsd.M = mref;
-      hsd.lse_int8 = LSE;
-      hsd.tail_lse = tail_lse;
-      hsd.k_star = kstar;
-      hsd.rank_ok = 1;
-      hsd.planned = 0;
-      hsd.level1 = 0;
-      hsd.level = -1;
-      hsd.e_key = 0.f;
-      hsd.e_val = 0.f;
-      hsd.n_vprom = 0;
-      hsd.pad = 0;
-      V.hst[hb] = hsd;
-    }
-  }
-  __syncthreads();
-  // union of the selected sets over the group: the blocks whose FP16 keys are paged in
-  int cnt = 0;
-  for (int i = tid; i < nb; i += blockDim.x) {
-    uint8_t u = 0;
-    for (int r = 0; r < V.n_rep; ++r) u |= V.sel[head_row(V, b, g, r) * V.nbmax + i];
-    V.kprom0[(size_t)hs * V.nbmax + i] = u;
-    V.kprom1[(size_t)hs * V.nbmax + i] = u;
-    V.vprom1[(size_t)hs * V.nbmax + i] = 0;
-    cnt += u;
-  }
-  cnt = (int)warp_sum((float)cnt);
-  if (lane == 0) sm.cnt[warp] = cnt;
-  __syncthreads();
-  if (tid == 0) {
-    const int n = sm.cnt[0] + sm.cnt[1] + sm.cnt[2] + sm.cnt[3];
-    GroupState gs;
-    gs.need_round1 = 0;
-    gs.need_dense = 0;
-    gs.n_kprom0 = n;
-    gs.n_kprom1 = n;
-    gs.n_vprom1 = 0;
-    gs.pad = 0;
-    gs.bytes = (long long)n * F16_BLOCK_BYTES;
-    V.gst[hs] = gs;
-  }
-}
-
 }  // namespace
 
-__global__ void __launch_bounds__(128) score_select_kernel(LayerView V) {
+__global__ void __launch_bounds__(128, 6) score_kernel(LayerView V) {
   __shared__ ScoreSmem sm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int nch = max(1, (V.nb + CHUNK - 1) / CHUNK);
+  const int nch = max(1, (V.nb + SCORE_CHUNK - 1) / SCORE_CHUNK);
   const int total = V.BG * nch;
-  unsigned int* cnt_group = V.counters + CNT_GROUP_BASE;  // stage 0
 
   int cur_hs = -1;
   uint4 qv = make_uint4(0, 0, 0, 0);  // q of head gid>>1, channels 32tig + 8warp + [0, 8)
@@ -209,14 +90,27 @@ __global__ void __launch_bounds__(128) score_select_kernel(LayerView V) {
       sc_out = (tig < V.n_rep) ? INV_SQRT_D / prescale_for(sm.qmax[tig] * smax) : 0.f;
     }
 
-    const int blk_end = min(V.nb, (ch + 1) * CHUNK);
-    for (int blk = ch * CHUNK; blk < blk_end; ++blk, par ^= 1) {
-      const size_t bi = (size_t)hs * V.nbmax + blk;
-      // A operand: this warp's 16 rows, 4 x 16 bytes per lane, coalesced
+    const int blk_begin = ch * SCORE_CHUNK;
+    const int blk_end = min(V.nb, blk_begin + SCORE_CHUNK);
+    // software pipeline: the next block's codes and scales are in flight while the
+    // current block is multiplied
+    uint4 N0, N1, N2, N3, NS;
+    if (blk_begin < blk_end) {
+      const size_t bi = (size_t)hs * V.nbmax + blk_begin;
       const uint4* kp = reinterpret_cast<const uint4*>(V.kc + bi * KC_BYTES) + (warp * 4) * 32 + lane;
-      const uint4 R0 = __ldcs(kp), R1 = __ldcs(kp + 32), R2 = __ldcs(kp + 64), R3 = __ldcs(kp + 96);
+      N0 = __ldcs(kp); N1 = __ldcs(kp + 32); N2 = __ldcs(kp + 64); N3 = __ldcs(kp + 96);
+      NS = *reinterpret_cast<const uint4*>(V.ks + bi * D + 32 * tig + 8 * warp);
+    }
+    for (int blk = blk_begin; blk < blk_end; ++blk, par ^= 1) {
+      // A operand: this warp's 16 rows, 4 x 16 bytes per lane, coalesced
+      const uint4 R0 = N0, R1 = N1, R2 = N2, R3 = N3, sv = NS;
+      if (blk + 1 < blk_end) {
+        const size_t bn = (size_t)hs * V.nbmax + blk + 1;
+        const uint4* kp = reinterpret_cast<const uint4*>(V.kc + bn * KC_BYTES) + (warp * 4) * 32 + lane;
+        N0 = __ldcs(kp); N1 = __ldcs(kp + 32); N2 = __ldcs(kp + 64); N3 = __ldcs(kp + 96);
+        NS = *reinterpret_cast<const uint4*>(V.ks + bn * D + 32 * tig + 8 * warp);
+      }
       // B operand: hi/lo halves of q_c s_c 2^e for the thread's 8 channels
-      const uint4 sv = *reinterpret_cast<const uint4*>(V.ks + bi * D + 32 * tig + 8 * warp);
       {
         const __half* qh = reinterpret_cast<const __half*>(&qv);
         const __half* sh = reinterpret_cast<const __half*>(&sv);
@@ -296,19 +190,6 @@ __global__ void __launch_bounds__(128) score_select_kernel(LayerView V) {
       }
     }
 
-    // completion of this item; the last item of a group runs the selection
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      const unsigned int old = atomicAdd(&cnt_group[hs], 1u);
-      sm.is_last = (old == (unsigned int)(nch - 1));
-    }
-    __syncthreads();
-    if (sm.is_last) {
-      __threadfence();
-      select_group(V, hs, sm);
-      if (tid == 0) cnt_group[hs] = 0u;
-    }
     __syncthreads();
   }
   if (tid == 0) {
@@ -320,10 +201,144 @@ __global__ void __launch_bounds__(128) score_select_kernel(LayerView V) {
   }
 }
 
+// One CTA of 256 threads per (sequence, query head): the top-K* selection.  The last
+// head of each KV group to finish forms the group's union of selected blocks.
+__global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
+  extern __shared__ __align__(16) unsigned char sel_dsm[];
+  BlockSelSmem& ws = *reinterpret_cast<BlockSelSmem*>(sel_dsm);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(sel_dsm + sizeof(BlockSelSmem));   // [nb padded]
+  float* xs = reinterpret_cast<float*>(keys);                                         // same storage
+  __shared__ float tail_s[BLK];
+  __shared__ int is_last;
+  const int tid = threadIdx.x;
+  const int bh = blockIdx.x;
+  const int b = bh / V.Hq, h = bh % V.Hq, g = h / V.n_rep;
+  const int hs = b * V.Hkv + g;
+  const int nb = V.nb, nbp = (nb + 15) & ~15;
+  const size_t hb = (size_t)bh;
+  // exact scores of the partial FP16 block (counts as covered)
+  float tmax = -INFINITY;
+  if (tid < V.n_tail) {
+    const __half* q = V.q + hb * D;
+    const __half* k = V.tail_k + ((size_t)hs * BLK + tid) * D;
+    float sc = 0.f;
+    for (int c = 0; c < D; c += 2) {
+      const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(k + c));
+      const float2 qq = __half22float2(*reinterpret_cast<const __half2*>(q + c));
+      sc = fmaf(qq.x, kk.x, sc);
+      sc = fmaf(qq.y, kk.y, sc);
+    }
+    sc *= INV_SQRT_D;
+    tail_s[tid] = sc;
+    tmax = sc;
+  }
+  tmax = block_max(tmax, ws.red);
+  const float tl = block_sum(tid < V.n_tail ? expf(tail_s[tid] - tmax) : 0.f, ws.red);
+  const float tail_lse = V.n_tail > 0 ? tmax + logf(tl) : -INFINITY;
+  // block log-masses: staged in shared memory (16-byte loads; rows padded to 16 blocks)
+  const float* lse8 = V.lse8 + hb * V.nbmax;
+  const float* dl = V.delta + hb * V.nbmax;
+  float m = -INFINITY, mref = -INFINITY;
+  for (int i4 = tid; i4 < nbp / 4; i4 += BS_THREADS) {
+    const float4 x = reinterpret_cast<const float4*>(lse8)[i4];
+    const float4 d = reinterpret_cast<const float4*>(dl)[i4];
+    const float xv[4] = {x.x, x.y, x.z, x.w}, dv[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (4 * i4 + j < nb) {
+        m = fmaxf(m, xv[j]);
+        mref = fmaxf(mref, xv[j] + dv[j]);
+      }
+    }
+    reinterpret_cast<float4*>(xs)[i4] = x;
+  }
+  m = block_max(fmaxf(m, tail_lse), ws.red);
+  mref = block_max(fmaxf(mref, tmax), ws.red);
+  float sp = 0.f;
+  for (int i = tid; i < nb; i += BS_THREADS) sp += expf(xs[i] - m);
+  float s = block_sum(sp, ws.red);
+  if (V.n_tail > 0) s += expf(tail_lse - m);
+  const float LSE = m + logf(s);
+  const double tail_mass = (V.n_tail > 0) ? (double)expf(tail_lse - LSE) : 0.0;
+  const double need = (double)V.tau - tail_mass;
+  unsigned long long target = 0ull;
+  if (need > 0.0) target = (unsigned long long)ceil(need * 4611686018427387904.0);
+  uint8_t* sel = V.sel + hb * V.nbmax;
+  for (int i16 = tid; i16 < nbp / 16; i16 += BS_THREADS) reinterpret_cast<uint4*>(sel)[i16] = make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < nb; i += BS_THREADS) keys[i] = __float_as_uint(expf(xs[i] - LSE));   // mass
+  __syncthreads();
+  unsigned long long taken = 0;
+  const int kstar = block_select_top(nb, keys, target, [&](int i) { sel[i] = 1; }, ws, &taken);
+  if (tid == 0) {
+    HeadState hsd;
+    hsd.M = mref;
+    hsd.lse_int8 = LSE;
+    hsd.tail_lse = tail_lse;
+    hsd.k_star = kstar;
+    hsd.rank_ok = 1;
+    hsd.planned = 0;
+    hsd.level1 = 0;
+    hsd.level = -1;
+    hsd.e_key = 0.f;
+    hsd.e_val = 0.f;
+    hsd.n_vprom = 0;
+    hsd.pad = 0;
+    V.hst[hb] = hsd;
+  }
+  // the last head of the group to finish forms the union (blocks whose FP16 keys are
+  // paged in); the padding bytes of every sel row are zero
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned int old = atomicAdd(&V.counters[CNT_GROUP_BASE + hs], 1u);
+    is_last = (old == (unsigned int)(V.n_rep - 1));
+  }
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  int cnt = 0;
+  for (int i16 = tid; i16 < nbp / 16; i16 += BS_THREADS) {
+    uint4 u = make_uint4(0, 0, 0, 0);
+    for (int r = 0; r < V.n_rep; ++r) {
+      const uint4 x = __ldcg(reinterpret_cast<const uint4*>(V.sel + ((size_t)b * V.Hq + g * V.n_rep + r) * V.nbmax) + i16);
+      u.x |= x.x; u.y |= x.y; u.z |= x.z; u.w |= x.w;
+    }
+    reinterpret_cast<uint4*>(V.kprom0 + (size_t)hs * V.nbmax)[i16] = u;
+    reinterpret_cast<uint4*>(V.kprom1 + (size_t)hs * V.nbmax)[i16] = u;
+    reinterpret_cast<uint4*>(V.vprom1 + (size_t)hs * V.nbmax)[i16] = make_uint4(0, 0, 0, 0);
+    cnt += __popc(u.x) + __popc(u.y) + __popc(u.z) + __popc(u.w);
+  }
+  cnt = block_sum_int(cnt, ws.red);
+  if (tid == 0) {
+    GroupState gs;
+    gs.need_round1 = 0;
+    gs.need_dense = 0;
+    gs.n_kprom0 = cnt;
+    gs.n_kprom1 = cnt;
+    gs.n_vprom1 = 0;
+    gs.pad = 0;
+    gs.bytes = (long long)cnt * F16_BLOCK_BYTES;
+    V.gst[hs] = gs;
+    V.counters[CNT_GROUP_BASE + hs] = 0u;
+  }
+}
+
+size_t select_smem_bytes(int nb) {
+  return sizeof(BlockSelSmem) + (size_t)((nb + 15) & ~15) * 4;
+}
+
 int score_grid(int num_sms) { return num_sms * 6; }
 
-cudaError_t launch_score_select(const LayerView& V, int grid, cudaStream_t st) {
-  score_select_kernel<<<grid, 128, 0, st>>>(V);
+cudaError_t launch_score(const LayerView& V, int grid, cudaStream_t st) {
+  score_kernel<<<grid, 128, 0, st>>>(V);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(const LayerView& V, cudaStream_t st) {
+  const size_t dyn = select_smem_bytes(V.nb);
+  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  select_kernel<<<V.B * V.Hq, BS_THREADS, dyn, st>>>(V);
   return cudaGetLastError();
 }
 

@@ -63,7 +63,7 @@ typedef struct kvq_config {
   int head_dim;
   int block_tokens;
   int value_group;
-  int max_ctx;             /* tokens per sequence and layer */
+  int max_ctx;             /* tokens per sequence and layer, at most 2097152 */
   int rank_positions;      /* ranking check compares the top-R blocks (R >= 1; default 1) */
   float l4_head_fraction;  /* rung 4 when >= this fraction of a sequence's heads are at
                               rung 3 (in (0, 1]; default 0.5) */

@@ -34,7 +34,7 @@ def _check(q, K, V, tau, eps, chunks=None, **kw):
 # Method §1: quantise-and-append, bit-exact, any append pattern
 # ---------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("chunks", [None, [1, 63, 64, 100, 1, 500], [64] * 12 + [17], [7] * 115])
+@pytest.mark.parametrize("chunks", [None, [1, 63, 64, 100, 1, 576], [64] * 12 + [37], [7] * 115])
 def test_tier1_bit_exact(chunks):
     q, K, V = W.tiny(seed=3, ctx=805, Hq=8, Hkv=2, batch=2, kscale=3.0)
     g = gpu_run(q, K, V, 0.9, 0.25, chunks=chunks)
@@ -67,7 +67,7 @@ def test_decode_c1_shape():
     assert st["strict"] >= 24, st
 
 
-@pytest.mark.parametrize("ctx", [64 * 16, 64 * 16 + 1, 64 * 33 + 63, 37, 64])
+@pytest.mark.parametrize("ctx", [64 * 16, 64 * 16 + 1, 64 * 33 + 63, 37, 64, 64 * 700 + 5, 64 * 2100])
 def test_decode_ragged(ctx):
     q, K, V = W.tiny(seed=5, ctx=ctx, Hq=8, Hkv=2, batch=2, kscale=3.0)
     _check(q, K, V, 0.95, 0.25, chunks=[ctx // 3, ctx - ctx // 3])
