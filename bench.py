@@ -179,6 +179,24 @@ def _config(wl):
 # our arm
 # ---------------------------------------------------------------------------------
 
+def aggregate_ranks(ms_local: float, units_local: int, device=None):
+    """Whole-job timing over ranks: the slowest rank's time and the units of all ranks.
+
+    Every rank runs an independent replica (no data exchange on the path), so the job's
+    throughput is the total units over the max time.  Single-process runs pass through.
+    """
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms_local, units_local
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    u = torch.tensor([units_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    dist.barrier()
+    return float(t.item()), int(u.item())
+
+
 def measure_h2d(torch):
     n = 256 << 20
     h = torch.empty(n, dtype=torch.uint8).pin_memory()
@@ -241,13 +259,9 @@ def our_arm(args, wl):
         e1.record(st)
         torch.cuda.synchronize()
     ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-        dist.barrier()
+    ms, units = aggregate_ranks(ms, B * L * args.steps, "cuda" if world > 1 else None)
     ms_per_step = ms / args.steps
-    value = world * B * L / (ms_per_step / 1e3)
+    value = units / (ms / 1e3)
 
     # certificates of the last step: ladder histogram, promoted bytes
     hist = [0] * 5

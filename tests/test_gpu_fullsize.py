@@ -1,0 +1,73 @@
+"""Full-size workloads on the GPU, checked against the oracle on sampled KV groups.
+
+The CUDA path decodes a whole 128K-token layer of the Llama-3.1-8B-shaped cache (and
+the 32K x 4 low-rank workload) in the same launch configuration as bench.py; the
+oracle then recomputes sampled (sequence, KV head) groups one by one.  Rung 4 depends
+on every head of a sequence, so the sampled comparison asserts it did not fire.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import certified_quantized_kv_gb300 as kvq  # noqa: E402
+import oracle as O  # noqa: E402
+import workloads as W  # noqa: E402
+from _parity import compare_decode  # noqa: E402
+
+
+def _run_full(q, K, V, tau, eps):
+    B, Hq, D = q.shape
+    Hkv, N = K.shape[1], K.shape[2]
+    cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=N)
+    try:
+        cache.append(0, K.contiguous(), V.contiguous())
+        out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+        cert = torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda")
+        lvl = torch.empty(B, dtype=torch.int32, device="cuda")
+        cache.decode(0, q.contiguous(), tau, eps, out, cert, lvl)
+        torch.cuda.synchronize()
+        t1 = {k: v.cpu() for k, v in cache.export_tier1(0).items()}
+        st = {k: v.cpu() for k, v in cache.export_decode_state(N // 64).items()}
+    finally:
+        cache.close()
+    return out.cpu(), kvq.certificates(cert).reshape(B, Hq), lvl.cpu().numpy(), t1, st
+
+
+def _check_groups(q, K, V, tau, eps, groups):
+    out, cert, lvl, t1g, st = _run_full(q, K, V, tau, eps)
+    assert np.all(lvl < 4), "rung 4 fired; sampled comparison does not apply"
+    n_rep = q.shape[1] // K.shape[1]
+    qc, Kc, Vc = q.cpu(), K.cpu(), V.cpu()
+    for b, g in groups:
+        hs = slice(g * n_rep, (g + 1) * n_rep)
+        qs = qc[b:b + 1, hs].numpy()
+        Ks, Vs = Kc[b:b + 1, g:g + 1].numpy(), Vc[b:b + 1, g:g + 1].numpy()
+        t1 = O.quantize_layer(Ks, Vs)
+        for name in ("kc", "vc", "eta"):
+            assert np.array_equal(t1g[name][b, g].numpy(), getattr(t1, name)[0, 0]), name
+        for name in ("ks", "vs", "vo"):
+            assert np.array_equal(t1g[name][b, g].numpy().view(np.uint16), getattr(t1, name)[0, 0].view(np.uint16)), name
+        r = O.decode_layer(qs, Ks, Vs, t1, tau, eps, O.OracleConfig(n_rep=n_rep))
+        g_res = dict(out=out[b:b + 1, hs], cert=cert[b:b + 1, hs],
+                     level=np.array([cert['level'][b, hs].max()]),   # rung over the sampled heads
+                     nb=Ks.shape[2] // 64,
+                     state={k: v[b:b + 1, hs] if v.shape[1] == q.shape[1] else v[b:b + 1, g:g + 1]
+                            for k, v in st.items()})
+        stats = compare_decode(g_res, t1, r, tau, eps, n_rep)
+        assert stats["strict"] + stats["excluded"] == n_rep
+
+
+def test_c3_layer_128k_sampled_groups():
+    q, K, V = W.c3_layer(0, device="cuda")
+    _check_groups(q, K, V, 0.995, 0.25, [(0, 0), (0, 5)])
+
+
+def test_c2_lowrank_32k_b4_sampled_groups():
+    q, K, V = W.c2(device="cuda")
+    _check_groups(q, K, V, 0.995, 0.25, [(0, 3), (3, 7)])
