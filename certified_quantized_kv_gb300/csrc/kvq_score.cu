@@ -10,7 +10,8 @@
 //   s_hat_t  = (1/sqrt(D)) sum_c q_c s_{b,c} code_{t,c}            (all 64 tokens)
 //   lse8_b   = log sum_t exp(s_hat_t)
 //   Delta_b  = kappa (1/sqrt(D)) sum_c |q_c| s_{b,c},   kappa = 1/2 + 2^-8
-// on the tensor cores: tokens are the MMA rows, channels the k dimension and the eight
+// on the tensor cores, one warp per block:
+// tokens are the MMA rows, channels the k dimension and the eight
 // MMA columns hold the four query heads twice, as the high and low fp16 halves of the
 // exact fp32 product q_c s_{b,c} (scaled by a power of two), so the f16 MMA reproduces
 // the fp32 product exactly.  The INT8 codes convert to f16 exactly in registers.
@@ -28,176 +29,151 @@ namespace kvq {
 
 namespace {
 
-struct ScoreSmem {
-  uint4 bfrag[2][32][4];             // B fragments per lane, double-buffered by block parity
-  float dsum[2][4][MAXREP];          // partial sum |q| s  [parity][warp][head]
-  float red_m[2][4][MAXREP];         // per-warp block max  [parity][warp][head]
-  float red_l[2][4][MAXREP];
-  float qmax[MAXREP];
-  int item;
-};
-
-
 __device__ __forceinline__ size_t head_row(const LayerView& V, int b, int g, int r) {
   return (size_t)b * V.Hq + (size_t)g * V.n_rep + r;
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(128, 6) score_kernel(LayerView V) {
-  __shared__ ScoreSmem sm;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// Warp-per-block scoring: every warp owns a contiguous range of the (KV group, block)
+// sequence and processes each block alone -- B fragments, 4 MMA row tiles, the block
+// log-mass by shuffles -- with no CTA barrier, so the SM keeps as many blocks in flight
+// as it holds warps.  The codes of the next row tile are loaded while the current one
+// is multiplied.
+__global__ void __launch_bounds__(128, 4) score_kernel(LayerView V) {
+  const int lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int nch = max(1, (V.nb + SCORE_CHUNK - 1) / SCORE_CHUNK);
-  const int total = V.BG * nch;
+  const long long total = (long long)V.BG * V.nb;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long per = (total + nwarps - 1) / nwarps;
+  const long long g0 = wid * per;
+  const long long g1 = min(total, g0 + per);
 
   int cur_hs = -1;
-  uint4 qv = make_uint4(0, 0, 0, 0);  // q of head gid>>1, channels 32tig + 8warp + [0, 8)
-  float pre = 1.f;                     // prescale of head gid>>1
-  float sc_out = 0.f;                  // output scale of head tig
-  int par = 0;
-
-  for (;;) {
-    if (tid == 0) sm.item = (int)atomicAdd(&V.counters[CNT_SCORE_Q], 1u);
-    __syncthreads();
-    const int item = sm.item;
-    if (item >= total) break;
-    const int hs = item / nch, ch = item % nch;
+  __half2 qh2[16];             // q of head gid>>1 at channels 32tig + [0, 32)
+  float pre = 1.f, inv_pre = 1.f;   // 2^e of head gid>>1 and its inverse
+  float sc_out = 0.f;               // output scale of head tig
+  for (long long gi = g0; gi < g1; ++gi) {
+    const int hs = (int)(gi / V.nb), blk = (int)(gi % V.nb);
     const int b = hs / V.Hkv, g = hs % V.Hkv;
-
+    const size_t bi = (size_t)hs * V.nbmax + blk;
+    const uint4* kp = reinterpret_cast<const uint4*>(V.kc + bi * KC_BYTES) + lane;
+    // row tile 0 in flight first, then the scales
+    uint4 A0 = __ldcs(kp), A1 = __ldcs(kp + 32), A2 = __ldcs(kp + 64), A3 = __ldcs(kp + 96);
+    const uint4* sp = reinterpret_cast<const uint4*>(V.ks + bi * D + 32 * tig);
+    const uint4 S0 = sp[0], S1 = sp[1], S2 = sp[2], S3 = sp[3];
     if (hs != cur_hs) {
       cur_hs = hs;
-      // per-head max |q| (warp = head slot)
-      if (warp < V.n_rep) {
-        const __half* q = V.q + head_row(V, b, g, warp) * D;
-        float m = 0.f;
-        for (int c = lane; c < D; c += 32) m = fmaxf(m, fabsf(__half2float(q[c])));
-        m = warp_max(m);
-        if (lane == 0) sm.qmax[warp] = m;
-      } else if (lane == 0) {
-        sm.qmax[warp] = 0.f;
-      }
-      __syncthreads();
       const float smax = __half2float(__ushort_as_half((unsigned short)V.kscale_max[hs]));
+      // max |q| per head slot over 128 channels: lane holds 4 channels of each slot
+      float qm[MAXREP];
+#pragma unroll
+      for (int r = 0; r < MAXREP; ++r) {
+        float m = 0.f;
+        if (r < V.n_rep) {
+          const __half2 v = *reinterpret_cast<const __half2*>(V.q + head_row(V, b, g, r) * D + 4 * lane);
+          const __half2 w = *reinterpret_cast<const __half2*>(V.q + head_row(V, b, g, r) * D + 4 * lane + 2);
+          m = fmaxf(fmaxf(fabsf(__low2float(v)), fabsf(__high2float(v))),
+                    fmaxf(fabsf(__low2float(w)), fabsf(__high2float(w))));
+        }
+        qm[r] = warp_max(m);
+      }
       const int r = gid >> 1;
+      float qmr = 0.f, qmt = 0.f;
+#pragma unroll
+      for (int k = 0; k < MAXREP; ++k) {
+        qmr = (k == r) ? qm[k] : qmr;
+        qmt = (k == tig) ? qm[k] : qmt;
+      }
       if (r < V.n_rep) {
-        qv = *reinterpret_cast<const uint4*>(V.q + head_row(V, b, g, r) * D + 32 * tig + 8 * warp);
-        pre = prescale_for(sm.qmax[r] * smax);
+        const uint4* qp = reinterpret_cast<const uint4*>(V.q + head_row(V, b, g, r) * D + 32 * tig);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 u = qp[i];
+          qh2[4 * i] = u32_as_h2(u.x); qh2[4 * i + 1] = u32_as_h2(u.y);
+          qh2[4 * i + 2] = u32_as_h2(u.z); qh2[4 * i + 3] = u32_as_h2(u.w);
+        }
+        pre = prescale_for(qmr * smax);
       } else {
-        qv = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) qh2[i] = __float2half2_rn(0.f);
         pre = 1.f;
       }
-      sc_out = (tig < V.n_rep) ? INV_SQRT_D / prescale_for(sm.qmax[tig] * smax) : 0.f;
+      inv_pre = 1.f / pre;
+      sc_out = (tig < V.n_rep) ? INV_SQRT_D / prescale_for(qmt * smax) : 0.f;
     }
-
-    const int blk_begin = ch * SCORE_CHUNK;
-    const int blk_end = min(V.nb, blk_begin + SCORE_CHUNK);
-    // software pipeline: the next block's codes and scales are in flight while the
-    // current block is multiplied
-    uint4 N0, N1, N2, N3, NS;
-    if (blk_begin < blk_end) {
-      const size_t bi = (size_t)hs * V.nbmax + blk_begin;
-      const uint4* kp = reinterpret_cast<const uint4*>(V.kc + bi * KC_BYTES) + (warp * 4) * 32 + lane;
-      N0 = __ldcs(kp); N1 = __ldcs(kp + 32); N2 = __ldcs(kp + 64); N3 = __ldcs(kp + 96);
-      NS = *reinterpret_cast<const uint4*>(V.ks + bi * D + 32 * tig + 8 * warp);
-    }
-    for (int blk = blk_begin; blk < blk_end; ++blk, par ^= 1) {
-      // A operand: this warp's 16 rows, 4 x 16 bytes per lane, coalesced
-      const uint4 R0 = N0, R1 = N1, R2 = N2, R3 = N3, sv = NS;
-      if (blk + 1 < blk_end) {
-        const size_t bn = (size_t)hs * V.nbmax + blk + 1;
-        const uint4* kp = reinterpret_cast<const uint4*>(V.kc + bn * KC_BYTES) + (warp * 4) * 32 + lane;
-        N0 = __ldcs(kp); N1 = __ldcs(kp + 32); N2 = __ldcs(kp + 64); N3 = __ldcs(kp + 96);
-        NS = *reinterpret_cast<const uint4*>(V.ks + bn * D + 32 * tig + 8 * warp);
-      }
-      // B operand: hi/lo halves of q_c s_c 2^e for the thread's 8 channels
-      {
-        const __half* qh = reinterpret_cast<const __half*>(&qv);
-        const __half* sh = reinterpret_cast<const __half*>(&sv);
-        uint32_t bw[4];
-        float dp = 0.f;
+    // B fragments for k-steps 0..7: channels 32tig + 4kk + {0,1} (b0) and {2,3} (b1),
+    // column gid = (head gid>>1, hi or lo half of q_c s_c 2^e)
+    uint32_t bf[16];
+    float dp = 0.f;
+    {
+      const uint4 Sv[4] = {S0, S1, S2, S3};
 #pragma unroll
-        for (int i = 0; i < 8; i += 2) {
-          const float w0 = __half2float(qh[i]) * __half2float(sh[i]);        // exact
-          const float w1 = __half2float(qh[i + 1]) * __half2float(sh[i + 1]);
-          dp += fabsf(w0) + fabsf(w1);
-          __half h0, l0, h1, l1;
-          split_hl(w0 * pre, h0, l0);
-          split_hl(w1 * pre, h1, l1);
-          const __half2 pk = (gid & 1) ? __halves2half2(l0, l1) : __halves2half2(h0, h1);
-          bw[i >> 1] = h2_as_u32(pk);
-        }
-        sm.bfrag[par][lane][warp ^ ((lane >> 1) & 3)] = make_uint4(bw[0], bw[1], bw[2], bw[3]);
-        dp += __shfl_xor_sync(0xffffffffu, dp, 1);
-        dp += __shfl_xor_sync(0xffffffffu, dp, 2);
-        if (tig == 0 && (gid & 1) == 0) sm.dsum[par][warp][gid >> 1] = dp;
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t sw = (i & 3) == 0 ? Sv[i >> 2].x : (i & 3) == 1 ? Sv[i >> 2].y : (i & 3) == 2 ? Sv[i >> 2].z : Sv[i >> 2].w;
+        const float2 s2 = __half22float2(u32_as_h2(sw));
+        const float2 q2 = __half22float2(qh2[i]);
+        const float w0 = q2.x * pre * s2.x, w1 = q2.y * pre * s2.y;   // exact products
+        dp += fabsf(w0) + fabsf(w1);
+        const __half2 hi = __floats2half2_rn(w0, w1);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(w0 - hf.x, w1 - hf.y);   // exact remainders
+        bf[i] = (gid & 1) ? h2_as_u32(lo) : h2_as_u32(hi);
       }
-      __syncthreads();
+    }
+    float x[8];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {        // MMA row tile w: tokens 16w .. 16w+15
+      const uint4 R0 = A0, R1 = A1, R2 = A2, R3 = A3;
+      if (w < 3) {
+        const uint4* np = kp + (w + 1) * 128;
+        A0 = __ldcs(np); A1 = __ldcs(np + 32); A2 = __ldcs(np + 64); A3 = __ldcs(np + 96);
+      }
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int kq = 0; kq < 4; ++kq) {
-        const uint4 bv = sm.bfrag[par][lane][kq ^ ((lane >> 1) & 3)];
-        // k-steps 2kq and 2kq+1
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint4& ra = (kk < 4) ? R0 : R1;
+        const uint4& rb = (kk < 4) ? R2 : R3;
+        const int wi = kk & 3;
+        const uint32_t wa = (wi == 0) ? ra.x : (wi == 1) ? ra.y : (wi == 2) ? ra.z : ra.w;
+        const uint32_t wb = (wi == 0) ? rb.x : (wi == 1) ? rb.y : (wi == 2) ? rb.z : rb.w;
+        uint32_t a0, a2, a1, a3;
+        i8x4_to_f16(wa, a0, a2);
+        i8x4_to_f16(wb, a1, a3);
+        mma16816(acc, a0, a1, a2, a3, bf[2 * kk], bf[2 * kk + 1]);
+      }
+      x[2 * w] = (acc[0] + acc[1]) * sc_out;       // head tig, token 16w + gid
+      x[2 * w + 1] = (acc[2] + acc[3]) * sc_out;   // head tig, token 16w + gid + 8
+    }
+    if (tig < V.n_rep) {
+      float* sh = V.shat + head_row(V, b, g, tig) * ((size_t)V.nbmax * BLK) + (size_t)blk * BLK + gid;
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const int kk = 2 * kq + s;
-          const uint4& ra = (kk < 4) ? R0 : R1;
-          const uint4& rb = (kk < 4) ? R2 : R3;
-          const int wi = kk & 3;
-          const uint32_t wa = (wi == 0) ? ra.x : (wi == 1) ? ra.y : (wi == 2) ? ra.z : ra.w;
-          const uint32_t wb = (wi == 0) ? rb.x : (wi == 1) ? rb.y : (wi == 2) ? rb.z : rb.w;
-          uint32_t a0, a2, a1, a3;
-          i8x4_to_f16(wa, a0, a2);
-          i8x4_to_f16(wb, a1, a3);
-          const uint32_t b0 = s ? bv.z : bv.x;
-          const uint32_t b1 = s ? bv.w : bv.y;
-          mma16816(acc, a0, a1, a2, a3, b0, b1);
-        }
-      }
-      // epilogue: thread holds head tig, tokens 16warp+gid and 16warp+gid+8
-      const float x0 = (acc[0] + acc[1]) * sc_out;
-      const float x1 = (acc[2] + acc[3]) * sc_out;
-      if (tig < V.n_rep) {
-        float* sh = V.shat + head_row(V, b, g, tig) * ((size_t)V.nbmax * BLK) + (size_t)blk * BLK + 16 * warp + gid;
-        sh[0] = x0;
-        sh[8] = x1;
-      }
-      float m = fmaxf(x0, x1);
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-      float l = expf(x0 - m) + expf(x1 - m);
-      l += __shfl_xor_sync(0xffffffffu, l, 4);
-      l += __shfl_xor_sync(0xffffffffu, l, 8);
-      l += __shfl_xor_sync(0xffffffffu, l, 16);
-      if (gid == 0) {
-        sm.red_m[par][warp][tig] = m;
-        sm.red_l[par][warp][tig] = l;
-      }
-      __syncthreads();
-      if (tid < V.n_rep) {
-        const int r = tid;
-        float M = sm.red_m[par][0][r];
-        for (int w = 1; w < 4; ++w) M = fmaxf(M, sm.red_m[par][w][r]);
-        float L = 0.f, ds = 0.f;
-        for (int w = 0; w < 4; ++w) {
-          L += sm.red_l[par][w][r] * expf(sm.red_m[par][w][r] - M);
-          ds += sm.dsum[par][w][r];
-        }
-        const size_t hb = head_row(V, b, g, r);
-        V.lse8[hb * V.nbmax + blk] = M + logf(L);
-        V.delta[hb * V.nbmax + blk] = KAPPA * INV_SQRT_D * ds;
+      for (int w = 0; w < 4; ++w) {
+        sh[16 * w] = x[2 * w];
+        sh[16 * w + 8] = x[2 * w + 1];
       }
     }
-
-    __syncthreads();
-  }
-  if (tid == 0) {
-    const unsigned int old = atomicAdd(&V.counters[CNT_SCORE_EXIT], 1u);
-    if (old == gridDim.x - 1) {
-      V.counters[CNT_SCORE_Q] = 0u;
-      V.counters[CNT_SCORE_EXIT] = 0u;
-    }
+    // block log-mass of head tig over its 64 tokens (8 per lane, 8 lanes per head)
+    float m = x[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) m = fmaxf(m, x[i]);
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+    float l = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) l += __expf(x[i] - m);   // relative error ~2^-22: inside the selection band
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    dp += __shfl_xor_sync(0xffffffffu, dp, 1);
+    dp += __shfl_xor_sync(0xffffffffu, dp, 2);
+    // lane 4r (gid 2r... tig 0) holds Delta of head r = gid>>1; lane tig (gid 0) holds lse of head tig
+    if (gid == 0 && tig < V.n_rep)
+      V.lse8[head_row(V, b, g, tig) * V.nbmax + blk] = m + logf(l);
+    if (tig == 0 && (gid & 1) == 0 && (gid >> 1) < V.n_rep)
+      V.delta[head_row(V, b, g, gid >> 1) * V.nbmax + blk] = KAPPA * INV_SQRT_D * (dp * inv_pre);
   }
 }
 
@@ -327,9 +303,12 @@ size_t select_smem_bytes(int nb) {
   return sizeof(BlockSelSmem) + (size_t)((nb + 15) & ~15) * 4;
 }
 
-int score_grid(int num_sms) { return num_sms * 6; }
+int score_grid(int num_sms) { return num_sms * 4; }
 
 cudaError_t launch_score(const LayerView& V, int grid, cudaStream_t st) {
+  const long long total = (long long)V.BG * V.nb;
+  if (total == 0) return cudaSuccess;   // nothing to score (only a partial block)
+  if ((long long)grid * 4 > total) grid = (int)((total + 3) / 4);
   score_kernel<<<grid, 128, 0, st>>>(V);
   return cudaGetLastError();
 }
