@@ -416,6 +416,63 @@ def our_arm(args, wl):
         dist.destroy_process_group()
 
 
+C5_CTX = (4096, 8192, 16384, 32768, 65536, 131072)
+C5_BATCH = (1, 8, 32)
+C5_TAU = (0.99, 0.995, 0.999)
+
+
+def sweep_c5(args):
+    """Ladder sweep: one layer per (context, batch) point, keys with four x20 channels and
+    values with four x8 channels per KV head, at three coverage targets.  One JSON line per
+    (context, batch, tau_cov): time per decode call, the ladder histogram over the query
+    heads, the promoted host-link bytes and the mean K*.  Inputs are drawn on the device
+    (this sweep has no oracle leg)."""
+    import torch
+    import certified_quantized_kv_gb300 as kvq
+    import workloads as W
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    Hq, Hkv, D, eps = WORKLOAD["q_heads"], WORKLOAD["kv_heads"], WORKLOAD["head_dim"], WORKLOAD["eps"]
+    ctxs = [args.ctx] if args.ctx else C5_CTX
+    batches = [args.batch] if args.batch else C5_BATCH
+    point = 0
+    for N in ctxs:
+        for B in batches:
+            q, K, V = W.c5_point(N, B, device="cuda", seed=4 + point)
+            point += 1
+            cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=N)
+            cache.append(0, K, V)
+            del K, V
+            out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+            cert = torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda")
+            lvl = torch.empty(B, dtype=torch.int32, device="cuda")
+            for tau in C5_TAU:
+                for _ in range(max(1, args.warmup)):
+                    cache.decode(0, q, tau, eps, out, cert, lvl)
+                times = []
+                for _ in range(max(1, args.steps)):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    cache.decode(0, q, tau, eps, out, cert, lvl)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    times.append(e0.elapsed_time(e1))
+                ms = sorted(times)[len(times) // 2]
+                c = kvq.certificates(cert).reshape(B, Hq)
+                hist = [int(x) for x in np.bincount(c["level"].ravel(), minlength=5)]
+                prom = int(c["promoted_bytes"][:, :: Hq // Hkv].sum())
+                print(json.dumps({
+                    "sweep": "c5", "ctx": N, "batch": B, "tau_cov": tau, "eps": eps,
+                    "ms_per_call": ms, "tokens_per_s_per_layer": B / (ms / 1e3),
+                    "ladder_histogram": hist, "promoted_bytes": prom,
+                    "promoted_fraction_of_tier2": prom / (B * Hkv * N * 2 * D * 2),
+                    "host_gbs": prom / (ms / 1e3) / 1e9, "k_star_mean": float(c["k_star"].mean()),
+                    "blocks": N // 64}), flush=True)
+            cache.close()
+            del q
+            torch.cuda.empty_cache()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -426,7 +483,12 @@ def main():
     ap.add_argument("--ctx", type=int, default=None, help="override the context (not the headline)")
     ap.add_argument("--batch", type=int, default=None, help="override the batch (not the headline)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--sweep", choices=["c5"], default=None,
+                    help="run the ladder sweep instead of the headline (one JSON line per point)")
     args = ap.parse_args()
+    if args.sweep == "c5":
+        sweep_c5(args)
+        return
     wl = dict(WORKLOAD)
     for k in ("layers", "ctx", "batch"):
         v = getattr(args, k)
