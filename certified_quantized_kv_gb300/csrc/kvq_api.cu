@@ -63,6 +63,7 @@ void set_last_error(const std::string& msg) { g_err = msg; }
 struct kvq_cache {
   kvq_config cfg;
   int device = 0, num_sms = 0;
+  int nslot = 0;      // partial slots per KV group of the split-K passes
   int B = 0, Hq = 0, Hkv = 0, n_rep = 0, BG = 0, nbmax = 0, nbmax_used = 0, L = 0;
   long long cap = 0;  // tier-2 tokens per (sequence, KV head)
   std::vector<int> n_tokens;
@@ -191,6 +192,15 @@ void free_all(kvq_cache* c) {
 
 }  // namespace
 
+// Blocks per work item of the split-K passes: at least ITEMS_PER_CTA items per resident
+// CTA when the layer is small (short contexts are latency-bound: every item reads its
+// blocks one after another), at most CHUNK blocks per item otherwise.
+static int decode_split(const kvq_cache* c, int nb) {
+  const long long target = (long long)ITEMS_PER_CTA * kvq::mixed_grid(c->num_sms);
+  const long long per = ((long long)c->BG * nb + target - 1) / target;
+  return (int)std::min<long long>(kvq::CHUNK, std::max<long long>(1, per));
+}
+
 extern "C" {
 
 const char* kvq_last_error(void) { return g_err.c_str(); }
@@ -275,7 +285,10 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
 
   // ---- scratch ----
   const size_t HQ = (size_t)c->B * c->Hq;
-  const size_t NCH = nbm / CHUNK + 1;
+  // partial slots per group: enough for every split decode_split() can choose
+  const size_t target = (size_t)ITEMS_PER_CTA * mixed_grid(c->num_sms);
+  const size_t NCH = std::max(nbm / CHUNK + 1, (target + BG - 1) / BG + 1);
+  c->nslot = (int)NCH;
   o = 0;
   const size_t s_shat = o;  o = align_up(o + HQ * nbm * BLK * 4, 256);
   const size_t s_lse8 = o;  o = align_up(o + HQ * nbm * 4, 256);
@@ -416,6 +429,7 @@ kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q, float ta
   LayerView V;
   V.B = c->B; V.Hq = c->Hq; V.Hkv = c->Hkv; V.n_rep = c->n_rep; V.BG = c->BG;
   V.nb = N / BLK; V.n_tail = N % BLK; V.nbmax = c->nbmax; V.cap = c->cap;
+  V.chunk = decode_split(c, V.nb); V.nslot = c->nslot;
   V.kc = layer_kc(c, layer); V.ks = layer_ks(c, layer); V.vc = layer_vc(c, layer);
   V.vsv = layer_vsv(c, layer); V.eta = layer_eta(c, layer);
   V.vmin = layer_vmin(c, layer); V.vmax = layer_vmax(c, layer);

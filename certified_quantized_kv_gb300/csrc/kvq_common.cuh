@@ -35,8 +35,8 @@ constexpr int KC_BYTES = BLK * D;          // 8192
 constexpr int VC_BYTES = BLK * D / 2;      // 4096
 constexpr int VSV_WORDS = BLK * NG;        // 256 half2
 constexpr int F16_BLOCK_BYTES = BLK * D * 2;  // 16384 bytes of FP16 per block (K or V)
-constexpr int CHUNK = 16;        // blocks per work item of the mixed and dense passes
-constexpr int SCORE_CHUNK = 8;   // blocks per work item of the scoring pass
+constexpr int CHUNK = 16;        // most blocks per work item of the mixed and dense passes
+constexpr int ITEMS_PER_CTA = 4; // work items per resident CTA the split aims for
 constexpr float KAPPA = 0.5f + 1.0f / 256.0f;
 constexpr float INV_SQRT_D = 0.088388347648318440550f;  // 1/sqrt(128), rounded to fp32
 
@@ -71,6 +71,8 @@ struct LayerView {
   int nb;          // full blocks of the layer
   int n_tail;      // tokens in the partial block (0..63)
   int nbmax;       // block capacity per (sequence, KV head), a multiple of 16
+  int chunk;       // blocks per work item of the mixed and dense passes (1..CHUNK)
+  int nslot;       // partial slots per KV group (>= the work items of a group)
   long long cap;   // token capacity of tier 2 per (sequence, KV head)
   // tier 1 of this layer
   const int8_t* kc;      // [BG][nbmax][8192]
@@ -105,20 +107,20 @@ struct LayerView {
   uint8_t* vprom1;
   HeadState* hst;        // [B*Hq]
   GroupState* gst;       // [BG]
-  float* part;           // [BG][nbmax/CHUNK+1][MAXREP][D+4] partials of the mixed pass
+  float* part;           // [BG][nslot][MAXREP][D+4] partials of the mixed pass
   float* part1;          // same shape: deltas of the second mixed pass
-  float* dpart;          // [BG][nbmax/CHUNK+1][MAXREP][D+4] partials of the dense pass
+  float* dpart;          // [BG][nslot][MAXREP][D+4] partials of the dense pass
   uint32_t* mkey;        // [B][Hq][nbmax] selection keys (normalised values, fp32 bits)
   unsigned int* counters;  // work queues and completion counters (self-resetting)
 };
 
 // counters layout
-constexpr int CNT_SCORE_Q = 0;      // work queue of the scoring pass
-constexpr int CNT_SCORE_EXIT = 1;
 constexpr int CNT_MIX_Q = 2;
 constexpr int CNT_MIX_EXIT = 3;
 constexpr int CNT_DENSE_Q = 4;
 constexpr int CNT_DENSE_EXIT = 5;
+constexpr int CNT_ANY_DENSE = 6;    // set when a head reaches rung 3 (reset by the finaliser)
+constexpr int CNT_NEED_R1 = 7;      // set when a head plans rung 1 or 2 (reset by the finaliser)
 constexpr int CNT_GROUP_BASE = 16;  // + stage*BG + hs: per-group completion counters
 constexpr int N_STAGE_COUNTERS = 3;
 

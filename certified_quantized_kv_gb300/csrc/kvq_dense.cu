@@ -12,7 +12,7 @@
 // (rung 4).  Dense heads report E_key = E_val = 0.
 //
 // The kernel reads FP16 keys and values straight from pinned host memory over the host
-// link (split-K over 16-block chunks, online softmax per chunk), which is the bound of
+// link (split-K over runs of up to 16 blocks, online softmax per run), which is the bound of
 // this path; the CUDA cores keep up with the link, so no tensor-core tiling is used.
 #include "kvq_common.cuh"
 #include "kvq_launch.h"
@@ -54,8 +54,8 @@ __device__ int dense_mask(const LayerView& V, int hs, int all_dense) {
 __device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dense, DenseSmem& sm) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = hs / V.Hkv, g = hs % V.Hkv;
-  const int nch = max(1, (V.nb + CHUNK - 1) / CHUNK);
-  const int NCH = V.nbmax / CHUNK + 1;
+  const int nch = max(1, (V.nb + V.chunk - 1) / V.chunk);
+  const int NCH = V.nslot;
   // partial block exact scores (warp = head slot)
   if (warp < V.n_rep) {
     const __half* q = V.q + head_row(V, b, g, warp) * D;
@@ -129,11 +129,12 @@ __device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dens
 __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) {
   __shared__ DenseSmem sm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nch = max(1, (V.nb + CHUNK - 1) / CHUNK);
-  const int NCH = V.nbmax / CHUNK + 1;
+  const int nch = max(1, (V.nb + V.chunk - 1) / V.chunk);
+  const int NCH = V.nslot;
   const int total = V.BG * nch;
   unsigned int* cnt_group = V.counters + CNT_GROUP_BASE + 3 * V.BG;
   int cur_hs = -1;
+  if (!all_dense && V.counters[CNT_ANY_DENSE] == 0u) return;   // no head reached rung 3
 
   for (;;) {
     if (tid == 0) {
@@ -159,16 +160,21 @@ __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) 
     // online softmax over the chunk; thread = channel, all four head slots
     float m[MAXREP], l[MAXREP], a[MAXREP];
     for (int r = 0; r < MAXREP; ++r) { m[r] = -INFINITY; l[r] = 0.f; a[r] = 0.f; }
-    const int blk_end = min(V.nb, (ch + 1) * CHUNK);
-    for (int blk = ch * CHUNK; blk < blk_end; ++blk) {
+    const int blk_end = min(V.nb, (ch + 1) * V.chunk);
+    for (int blk = ch * V.chunk; blk < blk_end; ++blk) {
       const size_t src = ((size_t)hs * V.cap + (size_t)blk * BLK) * D;
       {
+        // all sixteen 16-byte loads of a thread in flight before the first store
         const uint4* ks = reinterpret_cast<const uint4*>(V.t2k + src);
         const uint4* vs = reinterpret_cast<const uint4*>(V.t2v + src);
-        for (int i = tid; i < BLK * D / 8; i += blockDim.x) {
-          const int row = i >> 4, col = (i & 15) * 8;
-          *reinterpret_cast<uint4*>(&sm.kbuf[row][col]) = ks[i];
-          *reinterpret_cast<uint4*>(&sm.vbuf[row][col]) = vs[i];
+        uint4 rk[8], rv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { rk[j] = ks[tid + 128 * j]; rv[j] = vs[tid + 128 * j]; }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int i = tid + 128 * j, row = i >> 4, col = (i & 15) * 8;
+          *reinterpret_cast<uint4*>(&sm.kbuf[row][col]) = rk[j];
+          *reinterpret_cast<uint4*>(&sm.vbuf[row][col]) = rv[j];
         }
       }
       __syncthreads();
@@ -267,6 +273,10 @@ __global__ void finalize_kernel(LayerView V, kvq_certificate* cert, int32_t* lev
   }
   __syncthreads();
   if (threadIdx.x == 0 && level) level[b] = mx;
+  if (b == 0 && threadIdx.x == 0) {   // the flags of this call have been consumed
+    V.counters[CNT_ANY_DENSE] = 0u;
+    V.counters[CNT_NEED_R1] = 0u;
+  }
 }
 
 int dense_grid(int num_sms) { return num_sms * 3; }

@@ -18,7 +18,8 @@
 //   mass_b (e^Delta_b - 1) until the projected E_key <= eps/2; rung 2 pages in FP16
 //   values in descending mass_b eta_b until the projected E_key + E_val <= eps.
 //
-// Work split: a persistent grid takes (KV group, 16-block chunk) items from a queue.
+// Work split: a persistent grid takes (KV group, run of up to 16 blocks) items from a
+// queue; short layers use shorter runs so that every CTA gets several items.
 // For each block the CTA first produces p_t = exp(s'_t - M) for the four query heads in
 // shared memory -- from the stored INT8 scores, or from FP16 keys read from tier 2 -- and
 // then each warp (one 32-channel value group) multiplies them into V: INT4 codes on the
@@ -62,19 +63,19 @@ __device__ __forceinline__ unsigned long long fixed62(double x) {
   return (unsigned long long)(x * 4611686018427387904.0);
 }
 
-// Copy one FP16 block (64 x 128) from tier 2 into shared memory with row stride KROW.
-__device__ __forceinline__ void load_f16_block(__half (*dst)[KROW], const __half* src) {
+// Copy one FP16 block (64 x 128, 16 KiB) from tier 2 into shared memory rows of `stride`
+// halves (128 threads).  A thread issues all eight of its 16-byte loads before the first
+// store, so the block costs one host-link round trip instead of eight.
+template <int STRIDE>
+__device__ __forceinline__ void load_f16_block(__half* dst, const __half* src) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
-  for (int i = threadIdx.x; i < BLK * D / 8; i += blockDim.x) {
-    const int row = i >> 4, col = (i & 15) * 8;
-    *reinterpret_cast<uint4*>(&dst[row][col]) = s[i];
-  }
-}
-__device__ __forceinline__ void load_f16_block_dense(__half (*dst)[D], const __half* src) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-  for (int i = threadIdx.x; i < BLK * D / 8; i += blockDim.x) {
-    const int row = i >> 4, col = (i & 15) * 8;
-    *reinterpret_cast<uint4*>(&dst[row][col]) = s[i];
+  uint4 r[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) r[j] = s[threadIdx.x + 128 * j];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = threadIdx.x + 128 * j, row = i >> 4, col = (i & 15) * 8;
+    *reinterpret_cast<uint4*>(dst + row * STRIDE + col) = r[j];
   }
 }
 
@@ -84,12 +85,13 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
   __shared__ MixSmem sm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int nch = max(1, (V.nb + CHUNK - 1) / CHUNK);
-  const int NCH = V.nbmax / CHUNK + 1;
+  const int nch = max(1, (V.nb + V.chunk - 1) / V.chunk);
+  const int NCH = V.nslot;
   const int total = V.BG * nch;
   int par = 0;
   int cur_hs = -1;
   float pre_v = 1.f;
+  if (round == 1 && V.counters[CNT_NEED_R1] == 0u) return;   // no head planned rung 1 or 2
 
   for (;;) {
     if (tid == 0) {
@@ -126,8 +128,8 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
     float off = 0.f;     // sum p * offset for head gid>>1, group = warp
     float lsum = 0.f;    // sum p for head = warp
 
-    const int blk_end = min(V.nb, (ch + 1) * CHUNK);
-    for (int blk = ch * CHUNK; blk < blk_end; ++blk) {
+    const int blk_end = min(V.nb, (ch + 1) * V.chunk);
+    for (int blk = ch * V.chunk; blk < blk_end; ++blk) {
       const size_t bi = (size_t)hs * V.nbmax + blk;
       const bool kp0 = V.kprom0[bi] != 0;
       bool newk = false, vp = false;
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
       }
       float sn0 = so0, sn1 = so1;
       if (need_k16) {
-        load_f16_block(sm.st.kbuf, V.t2k + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
+        load_f16_block<KROW>(&sm.st.kbuf[0][0], V.t2k + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
         __syncthreads();
         {
           const int t = tid & 63, rp = (tid >> 6) * 2;  // heads rp, rp+1
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
         }
       }
       if (vp) {
-        load_f16_block_dense(sm.st.vbuf, V.t2v + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
+        load_f16_block<D>(&sm.st.vbuf[0][0], V.t2v + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
         __syncthreads();
         const int c0 = 32 * warp + gid;
         const float* pr = sm.pn[par][tig];
@@ -296,8 +298,8 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   extern __shared__ __align__(16) unsigned char comb_dsm[];
   BlockSelSmem& ws = *reinterpret_cast<BlockSelSmem*>(comb_dsm);
   uint32_t* keys = reinterpret_cast<uint32_t*>(comb_dsm + sizeof(BlockSelSmem));   // [nb padded]
-  __shared__ float acc_s[2][D];
-  __shared__ float l_s[2];
+  __shared__ __align__(16) float acc_s[BS_WARPS][D];
+  __shared__ float l_s[BS_WARPS];
   __shared__ float tail_p[BLK];
   const int tid = threadIdx.x;
   const int bh = blockIdx.x;
@@ -305,8 +307,8 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   const int hs = b * V.Hkv + g;
   const size_t hb = (size_t)bh;
   const int nb = V.nb;
-  const int nch = max(1, (nb + CHUNK - 1) / CHUNK);
-  const int NCH = V.nbmax / CHUNK + 1;
+  const int nch = max(1, (nb + V.chunk - 1) / V.chunk);
+  const int NCH = V.nslot;
   const uint8_t* kfl = (round == 0 ? V.kprom0 : V.kprom1) + (size_t)hs * V.nbmax;
   // first pass: no FP16 values yet (every head's rung 2 plans against this empty set,
   // while its marks accumulate in vprom1 for the second pass)
@@ -334,19 +336,26 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
     if (!(hsd.planned == 1 || hsd.planned == 2)) return;
     hsd.n_vprom = nv;
   }
-  // (1) chunk partials in a fixed order: thread = (channel, half of the chunks)
+  // (1) work-item partials in a fixed order: warp w sums items w, w + 8, ... (lane = four
+  //     channels), then the eight warp sums are added in warp order
   {
-    const int c = tid & (D - 1), half = tid >> 7;
-    float a = 0.f, l = 0.f;
+    const int warp = tid >> 5, lane = tid & 31;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    float l = 0.f;
 #pragma unroll 4
-    for (int ch = half; ch < nch; ch += 2) {
+    for (int ch = warp; ch < nch; ch += BS_WARPS) {
       const size_t o = (((size_t)hs * NCH + ch) * MAXREP + r) * (D + 4);
-      a += V.part[o + c];
-      if (round == 1) a += V.part1[o + c];
-      if (c == 0) l += V.part[o + D] + (round == 1 ? V.part1[o + D] : 0.f);
+      const float4 x = *reinterpret_cast<const float4*>(V.part + o + 4 * lane);
+      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
+      if (lane == 0) l += V.part[o + D];
+      if (round == 1) {
+        const float4 y = *reinterpret_cast<const float4*>(V.part1 + o + 4 * lane);
+        a.x += y.x; a.y += y.y; a.z += y.z; a.w += y.w;
+        if (lane == 0) l += V.part1[o + D];
+      }
     }
-    acc_s[half][c] = a;
-    if (c == 0) l_s[half] = l;
+    *reinterpret_cast<float4*>(&acc_s[warp][4 * lane]) = a;
+    if (lane == 0) l_s[warp] = l;
   }
   // (2) the partial FP16 block with exact scores
   float lt = 0.f;
@@ -364,9 +373,13 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
     tail_p[tid] = lt;
   }
   lt = block_sum(lt, ws.red);   // synchronises acc_s, l_s and tail_p too
-  const float L = l_s[0] + l_s[1] + lt;
+  float L = lt;
+#pragma unroll
+  for (int w = 0; w < BS_WARPS; ++w) L += l_s[w];
   if (tid < D) {
-    float a = acc_s[0][tid] + acc_s[1][tid];
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < BS_WARPS; ++w) a += acc_s[w][tid];
     for (int t = 0; t < V.n_tail; ++t)
       a += tail_p[t] * __half2float(V.tail_v[((size_t)hs * BLK + t) * D + tid]);
     V.out[hb * D + tid] = __float2half_rn(a / L);
@@ -401,7 +414,10 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   hsd.e_val = e_val;
   if (round == 1) {
     hsd.level1 = (e_key + e_val <= V.eps) ? hsd.planned : 3;
-    if (tid == 0) V.hst[hb] = hsd;
+    if (tid == 0) {
+      V.hst[hb] = hsd;
+      if (hsd.level1 == 3) V.counters[CNT_ANY_DENSE] = 1u;
+    }
     return;
   }
   // (4) ranking-consistency check over S_h: top-R positions by INT8 and FP16 log-mass
@@ -488,11 +504,17 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
         block_select_top(nb, keys, fixed62(need), [&](int i) { v1[i] = 1; }, ws, &taken);
       }
     }
-    if (tid == 0 && planned > 0) V.gst[hs].need_round1 = 1;
+    if (tid == 0 && planned > 0) {
+      V.gst[hs].need_round1 = 1;
+      V.counters[CNT_NEED_R1] = 1u;
+    }
   }
   hsd.planned = planned;
   hsd.level1 = planned;   // rungs 1/2 are confirmed, or raised to 3, by the second pass
-  if (tid == 0) V.hst[hb] = hsd;
+  if (tid == 0) {
+    V.hst[hb] = hsd;
+    if (planned == 3) V.counters[CNT_ANY_DENSE] = 1u;
+  }
 }
 
 int mixed_grid(int num_sms) { return num_sms * 4; }
