@@ -127,6 +127,8 @@ __device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dens
 }  // namespace
 
 __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) {
+  pdl_trigger();
+  pdl_wait();   // ladder levels of the combine kernels
   __shared__ DenseSmem sm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nch = max(1, (V.nb + V.chunk - 1) / V.chunk);
@@ -252,6 +254,7 @@ __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) 
 
 // Final certificates and per-sequence ladder level; one CTA per sequence.
 __global__ void finalize_kernel(LayerView V, kvq_certificate* cert, int32_t* level) {
+  pdl_wait();   // every head's state
   const int b = blockIdx.x;
   __shared__ int mx;
   if (threadIdx.x == 0) mx = 0;
@@ -282,14 +285,12 @@ __global__ void finalize_kernel(LayerView V, kvq_certificate* cert, int32_t* lev
 int dense_grid(int num_sms) { return num_sms * 3; }
 
 cudaError_t launch_dense(const LayerView& V, int all_dense, int grid, cudaStream_t st) {
-  dense_kernel<<<grid, 128, 0, st>>>(V, all_dense);
-  return cudaGetLastError();
+  return launch_dependent(dense_kernel, dim3(grid), dim3(128), 0, st, V, all_dense);
 }
 
 cudaError_t launch_finalize(const LayerView& V, kvq_certificate* cert, int32_t* level,
                             cudaStream_t st) {
-  finalize_kernel<<<V.B, 128, 0, st>>>(V, cert, level);
-  return cudaGetLastError();
+  return launch_dependent(finalize_kernel, dim3(V.B), dim3(128), 0, st, V, cert, level);
 }
 
 }  // namespace kvq

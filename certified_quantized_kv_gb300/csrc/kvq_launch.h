@@ -25,6 +25,24 @@ cudaError_t launch_export_tier1(const LayerAppend& L, int nb, void* kc, void* ks
                                 void* vs, void* vo, float* eta, float* vmin, float* vmax,
                                 cudaStream_t st);
 
+// Launch `k` as a programmatic dependent of the previous kernel in `st`: its CTAs may be
+// scheduled while that kernel drains and wait in pdl_wait() for its results.
+template <typename... P, typename... A>
+cudaError_t launch_dependent(void (*k)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             A&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, static_cast<A&&>(args)...);
+}
+
 // Decode pipeline (kvq_score.cu, kvq_mixed.cu, kvq_dense.cu).
 int score_grid(int num_sms);
 int mixed_grid(int num_sms);

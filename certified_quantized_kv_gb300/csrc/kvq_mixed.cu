@@ -82,6 +82,8 @@ __device__ __forceinline__ void load_f16_block(__half* dst, const __half* src) {
 }  // namespace
 
 __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
+  pdl_trigger();
+  pdl_wait();   // selection (round 0) or ladder plan (round 1)
   __shared__ MixSmem sm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -295,6 +297,8 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
 // pass for the head, add the partial block, write the output and the certificate and,
 // after the first pass, run the ranking check and plan rungs 1-2.
 __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int round) {
+  pdl_trigger();
+  pdl_wait();   // partials of the mixed pass
   extern __shared__ __align__(16) unsigned char comb_dsm[];
   BlockSelSmem& ws = *reinterpret_cast<BlockSelSmem*>(comb_dsm);
   uint32_t* keys = reinterpret_cast<uint32_t*>(comb_dsm + sizeof(BlockSelSmem));   // [nb padded]
@@ -520,16 +524,14 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
 int mixed_grid(int num_sms) { return num_sms * 4; }
 
 cudaError_t launch_mixed(const LayerView& V, int round, int grid, cudaStream_t st) {
-  mixed_kernel<<<grid, 128, 0, st>>>(V, round);
-  return cudaGetLastError();
+  return launch_dependent(mixed_kernel, dim3(grid), dim3(128), 0, st, V, round);
 }
 
 cudaError_t launch_combine(const LayerView& V, int round, cudaStream_t st) {
   const size_t dyn = sizeof(BlockSelSmem) + (size_t)((V.nb + 15) & ~15) * 4;
   cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
-  combine_kernel<<<V.B * V.Hq, BS_THREADS, dyn, st>>>(V, round);
-  return cudaGetLastError();
+  return launch_dependent(combine_kernel, dim3(V.B * V.Hq), dim3(BS_THREADS), dyn, st, V, round);
 }
 
 }  // namespace kvq

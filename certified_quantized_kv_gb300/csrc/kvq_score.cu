@@ -41,6 +41,7 @@ __device__ __forceinline__ size_t head_row(const LayerView& V, int b, int g, int
 // as it holds warps.  The codes of the next row tile are loaded while the current one
 // is multiplied.
 __global__ void __launch_bounds__(128, 4) score_kernel(LayerView V) {
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const long long total = (long long)V.BG * V.nb;
@@ -180,6 +181,8 @@ __global__ void __launch_bounds__(128, 4) score_kernel(LayerView V) {
 // One CTA of 256 threads per (sequence, query head): the top-K* selection.  The last
 // head of each KV group to finish forms the group's union of selected blocks.
 __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
+  pdl_trigger();
+  pdl_wait();   // scores of the scoring pass
   extern __shared__ __align__(16) unsigned char sel_dsm[];
   BlockSelSmem& ws = *reinterpret_cast<BlockSelSmem*>(sel_dsm);
   uint32_t* keys = reinterpret_cast<uint32_t*>(sel_dsm + sizeof(BlockSelSmem));   // [nb padded]
@@ -317,8 +320,7 @@ cudaError_t launch_select(const LayerView& V, cudaStream_t st) {
   const size_t dyn = select_smem_bytes(V.nb);
   cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
-  select_kernel<<<V.B * V.Hq, BS_THREADS, dyn, st>>>(V);
-  return cudaGetLastError();
+  return launch_dependent(select_kernel, dim3(V.B * V.Hq), dim3(BS_THREADS), dyn, st, V);
 }
 
 }  // namespace kvq
