@@ -41,4 +41,6 @@ from .kvq_oracle import (  # noqa: F401
     ranking_consistent,
     plan_ladder,
     decode_layer,
+    UncertifiedResult,
+    uncertified_decode_layer,
 )

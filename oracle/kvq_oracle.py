@@ -542,3 +542,44 @@ def decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Tier1,
         sel=sel_all, cum=cum_all, mass=mass_all, lse8=lse8_all, lse16=lse16_all,
         delta=delta_all, kprom0=kprom0, kprom1=kprom1, vprom1=vprom1, round1=round1,
         planned=planned, e_key0=e_key0, e_val0=e_val0)
+
+
+@dataclass
+class UncertifiedResult:
+    out: np.ndarray          # float16 [B, Hq, D]
+    out64: np.ndarray        # float64 [B, Hq, D] before the final rounding
+    e_key: np.ndarray        # [B, Hq] bound of the returned output (not enforced)
+    e_val: np.ndarray
+
+
+def uncertified_decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Tier1,
+                             cfg: OracleConfig = OracleConfig()) -> UncertifiedResult:
+    """The plain INT8/INT4 baseline the paper compares against (Experiments, retrieval):
+    INT8 key scores and INT4 values on every full block, the FP16 originals on the
+    partial block, nothing promoted and no ladder.  Its output is mixed_attention with
+    empty promotion sets; the bounds are those of that output, reported only."""
+    B, Hq, D = q.shape
+    _, Hkv, N, _ = K.shape
+    assert Hq % Hkv == 0
+    n_rep = Hq // Hkv
+    nb = N // BLOCK
+    inv = 1.0 / math.sqrt(D)
+    none = np.zeros(nb, bool)
+    out64 = np.zeros((B, Hq, D))
+    e_key = np.zeros((B, Hq)); e_val = np.zeros((B, Hq))
+    for b in range(B):
+        for g in range(Hkv):
+            Kg, Vg = K[b, g], V[b, g]
+            v_hat = dequantize_values(t1.vc[b, g], t1.vs[b, g], t1.vo[b, g])
+            R = float(np.max(t1.vmax[b, g].astype(np.float64) - t1.vmin[b, g].astype(np.float64)))
+            for h in range(g * n_rep, (g + 1) * n_rep):
+                qh = q[b, h]
+                s_ex = Kg.astype(np.float64) @ qh.astype(np.float64) * inv
+                s_hat = int8_scores(qh, t1.kc[b, g], t1.ks[b, g])
+                delta = score_perturbation(qh, t1.ks[b, g], cfg.kappa)
+                r = mixed_attention(s_ex, s_hat, Vg, v_hat, delta, t1.eta[b, g], R, none, none)
+                out64[b, h] = r.out
+                e_key[b, h] = r.e_key
+                e_val[b, h] = r.e_val
+    return UncertifiedResult(out64.astype(np.float16), out64, e_key, e_val)
+

@@ -526,3 +526,66 @@ def test_c2_mass_concentrated():
         fr.append(top[: max(1, int(round(0.05 * len(blk))))].sum())
     del gen
     assert min(fr) >= 0.99, fr
+
+
+# ---------------------------------------------------------------------------------
+# uncertified INT8/INT4 baseline (Experiments: the plain quantized comparison)
+# ---------------------------------------------------------------------------------
+
+def test_uncertified_is_softmax_attention_over_reconstructions():
+    """Brute force: textbook softmax attention over the explicitly reconstructed cache
+    (s * code keys, s * code + o values on full blocks, FP16 on the partial block)."""
+    for seed, ctx, Hq, Hkv in ((0, 200, 4, 1), (5, 321, 8, 2), (9, 64, 4, 1), (11, 40, 4, 1)):
+        q, K, V = _case(seed=seed, ctx=ctx, Hq=Hq, Hkv=Hkv, kscale=2.0)
+        t1 = O.quantize_layer(K, V)
+        res = O.uncertified_decode_layer(q, K, V, t1)
+        nb = ctx // 64
+        for g in range(Hkv):
+            Kr = K[0, g].astype(np.float64).copy()
+            Vr = V[0, g].astype(np.float64).copy()
+            for b in range(nb):
+                Kr[64 * b:64 * b + 64] = O.dequantize_keys(t1.kc[0, g, b], t1.ks[0, g, b])
+                Vr[64 * b:64 * b + 64] = O.dequantize_values(t1.vc[0, g, b], t1.vs[0, g, b],
+                                                             t1.vo[0, g, b])
+            for h in range(g * (Hq // Hkv), (g + 1) * (Hq // Hkv)):
+                qh = q[0, h].astype(np.float64)
+                s = Kr @ qh / math.sqrt(128)
+                p = np.exp(s - s.max()); p /= p.sum()
+                np.testing.assert_allclose(res.out64[0, h], p @ Vr, rtol=1e-11, atol=1e-12)
+
+
+def test_uncertified_grid_aligned_cache_is_exact():
+    """Keys on their INT8 grid and values on their INT4 grid reconstruct exactly, so the
+    uncertified output equals dense attention and E_val = 0."""
+    rng = np.random.default_rng(21)
+    nb, D = 3, 128
+    s0 = 2.0 ** -4
+    codes = rng.integers(-126, 127, (nb * 64, D))
+    codes[::64] = 127                                  # every block's scale is exactly s0
+    K = (codes * s0).astype(np.float16)[None, None]
+    vcode = rng.integers(0, 16, (nb * 64, D))
+    vcode[:, ::32] = 0
+    vcode[:, 1::32] = 15                               # each group spans 0..15 steps
+    V = (vcode * 2.0 ** -3 - 1.0).astype(np.float16)[None, None]
+    q = rng.standard_normal((1, 4, D)).astype(np.float16)
+    t1 = O.quantize_layer(K, V)
+    res = O.uncertified_decode_layer(q, K, V, t1)
+    for h in range(4):
+        ref = O.dense_attention(q[0, h], K[0, 0], V[0, 0])
+        np.testing.assert_allclose(res.out64[0, h], ref, rtol=1e-12, atol=1e-13)
+    assert np.all(res.e_val == 0.0)
+
+
+def test_uncertified_bound_is_sound():
+    """The reported (unenforced) bound still covers the uncertified output's error."""
+    rng = np.random.default_rng(13)
+    for seed in range(6):
+        q, K, V = _case(seed=300 + seed, ctx=int(rng.integers(64, 600)), Hq=16, Hkv=1,
+                        kscale=float(rng.choice([1.0, 4.0])))
+        t1 = O.quantize_layer(K, V)
+        res = O.uncertified_decode_layer(q, K, V, t1)
+        for h in range(16):
+            ref = O.dense_attention(q[0, h], K[0, 0], V[0, 0])
+            err = np.max(np.abs(res.out64[0, h] - ref))
+            assert err <= res.e_key[0, h] + res.e_val[0, h] + 1e-9
+
