@@ -37,6 +37,8 @@ TIER1_BYTES_PER_TOKEN_HEAD = 212        # 128 K codes + 4 K scales + 64 V codes 
 SCORE_BYTES_PER_TOKEN_HEAD = 132        # K codes + K scales (scoring pass)
 MIX_BYTES_PER_TOKEN_HEAD = 80           # V codes + V scale/offset (mixed pass, tail blocks)
 F16_BLOCK = 16384
+F16_BYTES_PER_TOKEN_HEAD = 512          # FP16 key + value of one token (tier-2 mirror)
+APPEND_HBM_BYTES_PER_TOKEN_HEAD = 512 + 212   # FP16 K/V read + tier 1 written (quantiser)
 
 
 def _peaks():
@@ -235,6 +237,51 @@ def measure_h2d(torch):
     return n / best / 1e6   # GB/s
 
 
+def measure_d2h(torch):
+    n = 256 << 20
+    h = torch.empty(n, dtype=torch.uint8).pin_memory()
+    d = torch.empty(n, dtype=torch.uint8, device="cuda")
+    best = 1e9
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); h.copy_(d, non_blocking=True); e1.record(); e1.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    return n / best / 1e6   # GB/s
+
+
+def measure_append(torch, kvq, W, wl, hbm_peak, reps=2):
+    """Bulk prefill of one layer (the workload's batch and context) through kvq_append:
+    quantisation to tier 1 on the device plus the FP16 mirror to tier 2 over the host
+    link, both inside the timed call.  Best of `reps` fresh caches."""
+    B, N, Hq, Hkv = wl["batch"], wl["ctx"], wl["q_heads"], wl["kv_heads"]
+    _, K, V = W.c3_layer(0, device="cuda", seed=wl["seed"], batch=B, ctx=N, Hq=Hq, Hkv=Hkv)
+    K, V = K.contiguous(), V.contiguous()
+    best_ms, kern_us = 1e9, None
+    for _ in range(reps):
+        c = kvq.Cache(1, B, Hq, Hkv, max_ctx=N)
+        c.set_debug(kvq.DEBUG_PROFILE)
+        c.profile_read(reset=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); c.append(0, K, V); e1.record(); torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        prof = c.profile_read(reset=True)
+        c.close()
+        if ms < best_ms:
+            best_ms = ms
+            n, tot = prof.get("quantize_append", (1, float("nan")))
+            kern_us = 1e3 * tot / max(1, n)
+    units = B * Hkv * N
+    d2h = measure_d2h(torch)
+    hbm_bytes = units * APPEND_HBM_BYTES_PER_TOKEN_HEAD
+    return {"tokens": B * N, "ms": best_ms, "tokens_per_s": B * N / (best_ms / 1e3),
+            "mirror_bytes": units * F16_BYTES_PER_TOKEN_HEAD, "d2h_gbs_measured": d2h,
+            "mirror_frac_of_d2h": units * F16_BYTES_PER_TOKEN_HEAD / (best_ms / 1e3) / 1e9 / d2h,
+            "quantize_kernel_us": kern_us,
+            "quantize_kernel_hbm": {"bytes": hbm_bytes, "achieved_gbs": hbm_bytes / (kern_us * 1e-6) / 1e9,
+                                    "peak": hbm_peak, "frac": hbm_bytes / (kern_us * 1e-6) / 1e9 / hbm_peak}}
+
+
 def our_arm(args, wl):
     import torch
     import torch.distributed as dist
@@ -289,6 +336,24 @@ def our_arm(args, wl):
     ms_per_step = ms / args.steps
     value = units / (ms / 1e3)
 
+    # the uncertified INT8/INT4 baseline on the same caches: the speed ceiling of tier 1
+    def step_unc():
+        for layer in range(L):
+            cache.decode_uncertified(layer, qs[layer], outs[layer])
+
+    for _ in range(args.warmup):
+        step_unc()
+    torch.cuda.synchronize()
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record(st)
+    for _ in range(args.steps):
+        step_unc()
+    u1.record(st)
+    torch.cuda.synchronize()
+    unc_ms = u0.elapsed_time(u1) / args.steps
+    uncertified = {"value": world * B * L / (unc_ms / 1e3), "unit": UNIT, "ms_per_step": unc_ms,
+                   "what": "INT8 scores and INT4 values on every block: no page-in, no ladder"}
+
     # certificates of the last step: ladder histogram, promoted bytes
     hist = [0] * 5
     prom = 0
@@ -342,13 +407,14 @@ def our_arm(args, wl):
     d2h = L * (B * Hq * D * 2 + B * Hq * 32 + B * 4)
 
     h2d_gbs = measure_h2d(torch)
+    hbm_peak, peak_kind = _peaks()
+    append = measure_append(torch, kvq, W, wl, hbm_peak) if rank == 0 else None
     if rank != 0:
         cache.close()
         if world > 1:
             dist.destroy_process_group()
         return
 
-    hbm_peak, peak_kind = _peaks()
     kern = {}
     for name, (n, tot) in prof.items():
         kern[name] = {"launches": n, "avg_us": 1e3 * tot / max(1, n), "total_ms": tot}
@@ -399,6 +465,8 @@ def our_arm(args, wl):
         "host_link": {"h2d_gbs_measured": h2d_gbs, "bytes_per_layer": host_bytes,
                       "floor_us_per_layer": prom / L / (h2d_gbs * 1e3) if h2d_gbs else None},
         "fill_s": t_fill,
+        "append": append,
+        "uncertified_baseline": uncertified,
     }
     if args.cpu_baseline:
         try:

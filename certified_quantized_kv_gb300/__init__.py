@@ -74,6 +74,7 @@ def load_library() -> ctypes.CDLL:
         "kvq_cache_destroy": [vp],
         "kvq_append": [vp, i32, vp, vp, i32, vp],
         "kvq_decode_attention": [vp, i32, vp, f32, f32, vp, vp, vp, vp],
+        "kvq_decode_attention_uncertified": [vp, i32, vp, vp, vp, vp],
         "kvq_set_debug": [vp, i32],
         "kvq_cache_length": [vp, i32, ctypes.POINTER(i32)],
         "kvq_export_tier1": [vp, i32, vp, vp, vp, vp, vp, vp, vp, vp, vp],
@@ -161,6 +162,14 @@ class Cache:
         st = _stream(stream) if (q.is_cuda or out.is_cuda) else None
         _check(self.lib.kvq_decode_attention(self.handle, layer, _ptr(q), float(tau_cov), float(eps),
                                              _ptr(out), _ptr(cert), _ptr(ladder_level), st))
+
+    def decode_uncertified(self, layer: int, q, out, cert=None, stream=None):
+        """Plain INT8/INT4 decode attention, nothing paged in and no ladder
+        (kvq_decode_attention_uncertified); cert receives the unenforced bounds."""
+        assert q.is_contiguous() and out.is_contiguous()
+        st = _stream(stream) if (q.is_cuda or out.is_cuda) else None
+        _check(self.lib.kvq_decode_attention_uncertified(self.handle, layer, _ptr(q), _ptr(out),
+                                                         _ptr(cert), st))
 
     def export_tier1(self, layer: int, stream=None) -> dict:
         """Tier-1 contents of `layer` in canonical layout, as CUDA tensors."""

@@ -201,6 +201,10 @@ static int decode_split(const kvq_cache* c, int nb) {
   return (int)std::min<long long>(kvq::CHUNK, std::max<long long>(1, per));
 }
 
+static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau, float eps,
+                              void* out, kvq_certificate* cert, int32_t* ladder_level,
+                              void* stream, bool certified, const char* fn);
+
 extern "C" {
 
 const char* kvq_last_error(void) { return g_err.c_str(); }
@@ -404,13 +408,30 @@ kvq_status kvq_append(kvq_cache* c, int layer, const void* k, const void* v, int
 kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q, float tau, float eps,
                                 void* out, kvq_certificate* cert, int32_t* ladder_level,
                                 void* stream) {
-  if (!c) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: NULL cache");
-  if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: layer out of range");
-  if (!q || !out) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: NULL q or out");
   if (!(tau > 0.f && tau <= 1.f)) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: tau_cov must be in (0, 1]");
   if (!(eps >= 0.f)) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: eps must be >= 0");
+  return decode_impl(c, layer, q, tau, eps, out, cert, ladder_level, stream, true, "kvq_decode_attention");
+}
+
+kvq_status kvq_decode_attention_uncertified(kvq_cache* c, int layer, const void* q, void* out,
+                                            kvq_certificate* cert, void* stream) {
+  // an empty selection (tau_cov = 0) and no bound to meet (eps = +inf): INT8 scores and
+  // INT4 values on every full block
+  return decode_impl(c, layer, q, 0.f, INFINITY, out, cert, nullptr, stream, false,
+                     "kvq_decode_attention_uncertified");
+}
+
+}  // extern "C"
+
+static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau, float eps,
+                              void* out, kvq_certificate* cert, int32_t* ladder_level,
+                              void* stream, bool certified, const char* fn) {
+  const std::string f(fn);
+  if (!c) return fail(KVQ_ERR_INVALID, f + ": NULL cache");
+  if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, f + ": layer out of range");
+  if (!q || !out) return fail(KVQ_ERR_INVALID, f + ": NULL q or out");
   const int N = c->n_tokens[layer];
-  if (N == 0) return fail(KVQ_ERR_INVALID, "kvq_decode_attention: layer holds no tokens");
+  if (N == 0) return fail(KVQ_ERR_INVALID, f + ": layer holds no tokens");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t HQ = (size_t)c->B * c->Hq;
   const bool q_dev = is_device_ptr(q), out_dev = is_device_ptr(out);
@@ -438,32 +459,40 @@ kvq_status kvq_decode_attention(kvq_cache* c, int layer, const void* q, float ta
   V.tail_k = layer_tail(c, layer, p, 0); V.tail_v = layer_tail(c, layer, p, 1);
   V.t2k = c->t2k_dev[layer]; V.t2v = c->t2v_dev[layer];
   V.q = qd; V.out = od; V.tau = tau; V.eps = eps;
-  V.l4_frac = c->cfg.l4_head_fraction; V.rank_positions = c->cfg.rank_positions; V.debug = c->debug;
+  V.l4_frac = c->cfg.l4_head_fraction; V.rank_positions = c->cfg.rank_positions;
+  V.debug = certified ? c->debug : (c->debug & ~(KVQ_DEBUG_FORCE_RANK_FAIL | KVQ_DEBUG_FORCE_DENSE));
   V.shat = c->shat; V.lse8 = c->lse8; V.delta = c->delta; V.lse16 = c->lse16; V.sel = c->sel;
   V.kprom0 = c->kprom0; V.kprom1 = c->kprom1; V.vprom1 = c->vprom1;
   V.hst = c->hst; V.gst = c->gst; V.part = c->part; V.dpart = c->dpart; V.counters = c->counters;
   V.mkey = c->mkey; V.part1 = c->part1;
 
-  const bool all_dense = (tau >= 1.f) || (c->debug & KVQ_DEBUG_FORCE_DENSE);
+  const bool all_dense = certified && ((tau >= 1.f) || (c->debug & KVQ_DEBUG_FORCE_DENSE));
   if (!all_dense) {
     { KernelScope s(c, K_SCORE, st); KVQ_CUDA(s.done(launch_score(V, score_grid(c->num_sms), st)), "score"); }
     { KernelScope s(c, K_SELECT, st); KVQ_CUDA(s.done(launch_select(V, st)), "select"); }
     { KernelScope s(c, K_MIX0, st); KVQ_CUDA(s.done(launch_mixed(V, 0, mixed_grid(c->num_sms), st)), "mixed_round0"); }
     { KernelScope s(c, K_COMB0, st); KVQ_CUDA(s.done(launch_combine(V, 0, st)), "combine_round0"); }
-    { KernelScope s(c, K_MIX1, st); KVQ_CUDA(s.done(launch_mixed(V, 1, mixed_grid(c->num_sms), st)), "mixed_round1"); }
-    { KernelScope s(c, K_COMB1, st); KVQ_CUDA(s.done(launch_combine(V, 1, st)), "combine_round1"); }
+    if (certified) {
+      { KernelScope s(c, K_MIX1, st); KVQ_CUDA(s.done(launch_mixed(V, 1, mixed_grid(c->num_sms), st)), "mixed_round1"); }
+      { KernelScope s(c, K_COMB1, st); KVQ_CUDA(s.done(launch_combine(V, 1, st)), "combine_round1"); }
+    }
   }
-  { KernelScope s(c, K_DENSE, st); KVQ_CUDA(s.done(launch_dense(V, all_dense ? 1 : 0, dense_grid(c->num_sms), st)), "dense_fallback"); }
+  if (certified) {
+    KernelScope s(c, K_DENSE, st);
+    KVQ_CUDA(s.done(launch_dense(V, all_dense ? 1 : 0, dense_grid(c->num_sms), st)), "dense_fallback");
+  }
   { KernelScope s(c, K_FINAL, st); KVQ_CUDA(s.done(launch_finalize(V, cd, ld, st)), "finalize"); }
 
   if (!out_dev) KVQ_CUDA(cudaMemcpyAsync(out, od, HQ * D * 2, cudaMemcpyDeviceToHost, st), "copy out");
   if (cert && !cert_dev) KVQ_CUDA(cudaMemcpyAsync(cert, cd, HQ * sizeof(kvq_certificate), cudaMemcpyDeviceToHost, st), "copy cert");
   if (ladder_level && !lvl_dev) KVQ_CUDA(cudaMemcpyAsync(ladder_level, ld, c->B * 4, cudaMemcpyDeviceToHost, st), "copy level");
-  if (host_any) KVQ_CUDA(cudaStreamSynchronize(st), "kvq_decode_attention: sync");
+  if (host_any) KVQ_CUDA(cudaStreamSynchronize(st), (f + ": sync").c_str());
   c->last_layer = layer;
   c->last_nb = all_dense ? -1 : V.nb;
   return KVQ_OK;
 }
+
+extern "C" {
 
 kvq_status kvq_export_tier1(kvq_cache* c, int layer, void* kc, void* ks, void* vc, void* vs,
                             void* vo, float* eta, float* vmin, float* vmax, void* stream) {

@@ -21,6 +21,7 @@ namespace kvq {
 
 constexpr int BS_THREADS = 256;
 constexpr int BS_WARPS = BS_THREADS / 32;
+static_assert(SEL_CAND <= BS_THREADS, "one thread per exactly ranked candidate");
 
 struct BlockRed {
   float f[BS_WARPS];
@@ -95,11 +96,23 @@ __device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long 
   return before + incl - v;
 }
 
+// Exact 64-bit add to a shared-memory bucket with two native 32-bit atomics (a 64-bit
+// shared atomic add is a compare-and-swap loop, slow when many lanes hit one bucket):
+// the low word's wrap-around, seen in the value the atomic returns, carries into the
+// high word, so the bucket read as a 64-bit integer is the exact sum.
+__device__ __forceinline__ void hist_add(unsigned long long* bucket, unsigned long long w) {
+  uint32_t* h = reinterpret_cast<uint32_t*>(bucket);   // little endian: h[0] low, h[1] high
+  const uint32_t lo = (uint32_t)w, hi = (uint32_t)(w >> 32);
+  const uint32_t old = atomicAdd(&h[0], lo);
+  const uint32_t carry = (old + lo < old) ? 1u : 0u;
+  if (hi + carry) atomicAdd(&h[1], hi + carry);
+}
+
 // Shared-memory workspace of block_select_top (dynamic shared memory).
 struct BlockSelSmem {
   unsigned long long hist[BS_WARPS][1024];   // per-warp private histograms
-  int cidx[SEL_CAND];
-  uint32_t ckey[SEL_CAND];
+  alignas(16) int cidx[SEL_CAND];
+  alignas(16) uint32_t ckey[SEL_CAND];
   int order[SEL_CAND];
   unsigned long long above;
   uint32_t prefix;
@@ -139,7 +152,7 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
     for (int i = i0; i < i1; ++i) {
       const uint32_t k = keys[i];
       if (k != 0u && (level == 0 || (k >> (sh + 10)) == prefix))
-        atomicAdd(&ws.hist[warp][(k >> sh) & 1023u], key_weight(k));
+        hist_add(&ws.hist[warp][(k >> sh) & 1023u], key_weight(k));
     }
     __syncthreads();
     // thread t owns buckets 1023-4t .. 1020-4t (descending)
@@ -211,15 +224,25 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
     }
     __syncthreads();
     const int nc = ws.ncand;
-    for (int a = tid; a < nc; a += BS_THREADS) {
-      const uint32_t ka = ws.ckey[a];
-      const int ia = ws.cidx[a];
+    const int nc4 = (nc + 3) & ~3;
+    if (tid >= nc && tid < nc4) ws.ckey[tid] = 0u;   // padding ranks below every candidate
+    __syncthreads();
+    // rank of candidate a = number of candidates before it (key descending, index
+    // ascending); nc <= SEL_CAND = BS_THREADS, four candidates per 16-byte load
+    if (tid < nc) {
+      const uint32_t ka = ws.ckey[tid];
+      const int ia = ws.cidx[tid];
       int rank = 0;
-      for (int b2 = 0; b2 < nc; ++b2) {
-        const uint32_t kb = ws.ckey[b2];
-        rank += (kb > ka) || (kb == ka && ws.cidx[b2] < ia);
+#pragma unroll 4
+      for (int b4 = 0; b4 < nc4; b4 += 4) {
+        const uint4 kb = *reinterpret_cast<const uint4*>(&ws.ckey[b4]);
+        const int4 ib = *reinterpret_cast<const int4*>(&ws.cidx[b4]);
+        rank += (kb.x > ka) || (kb.x == ka && ib.x < ia);
+        rank += (kb.y > ka) || (kb.y == ka && ib.y < ia);
+        rank += (kb.z > ka) || (kb.z == ka && ib.z < ia);
+        rank += (kb.w > ka) || (kb.w == ka && ib.w < ia);
       }
-      ws.order[rank] = a;
+      ws.order[rank] = tid;
     }
     if (tid == 0) { ws.last = nc - 1; ws.take_w = 0ull; }
     __syncthreads();

@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
     const int warp = tid >> 5, lane = tid & 31;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     float l = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int ch = warp; ch < nch; ch += BS_WARPS) {
       const size_t o = (((size_t)hs * NCH + ch) * MAXREP + r) * (D + 4);
       const float4 x = *reinterpret_cast<const float4*>(V.part + o + 4 * lane);
@@ -398,16 +398,30 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   const float* dl = V.delta + hb * V.nbmax;
   const float* eta = V.eta + (size_t)hs * V.nbmax;
   float S = 0.f, A = 0.f, Ev = 0.f;
-  for (int i = tid; i < nb; i += BS_THREADS) {
-    const bool kp = kfl[i] != 0;
-    const float pm = expf((kp ? lse16[i] : lse8[i]) - LSEp);
-    if (kp) {
-      A += pm;
-    } else {
-      S += pm * expm1f(dl[i]);
-      A += pm * expf(-dl[i]);
+  // four blocks per thread and step (rows are padded to 16 blocks, 16-byte aligned)
+  for (int i4 = tid; i4 < (nb + 3) / 4; i4 += BS_THREADS) {
+    const uchar4 kf4 = reinterpret_cast<const uchar4*>(kfl)[i4];
+    const uchar4 vf4 = vfl ? reinterpret_cast<const uchar4*>(vfl)[i4] : make_uchar4(0, 0, 0, 0);
+    const float4 l8 = reinterpret_cast<const float4*>(lse8)[i4];
+    const float4 l16 = reinterpret_cast<const float4*>(lse16)[i4];
+    const float4 d4 = reinterpret_cast<const float4*>(dl)[i4];
+    const float4 e4 = reinterpret_cast<const float4*>(eta)[i4];
+    const unsigned char kf[4] = {kf4.x, kf4.y, kf4.z, kf4.w}, vf[4] = {vf4.x, vf4.y, vf4.z, vf4.w};
+    const float a8[4] = {l8.x, l8.y, l8.z, l8.w}, a16[4] = {l16.x, l16.y, l16.z, l16.w};
+    const float dd[4] = {d4.x, d4.y, d4.z, d4.w}, ee[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (4 * i4 + j >= nb) break;
+      const bool kp = kf[j] != 0;
+      const float pm = expf((kp ? a16[j] : a8[j]) - LSEp);
+      if (kp) {
+        A += pm;
+      } else {
+        S += pm * expm1f(dd[j]);
+        A += pm * expf(-dd[j]);
+      }
+      if (!vf[j]) Ev += pm * ee[j];
     }
-    if (!vfl || !vfl[i]) Ev += pm * eta[i];
   }
   S = block_sum(S, ws.red);
   A = block_sum(A, ws.red) + tail_mass;
@@ -434,13 +448,23 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
     for (int pos = 0; pos < R_rank && ok; ++pos) {
       float b8 = -INFINITY, b16 = -INFINITY;
       int i8 = 0x7fffffff, i16 = 0x7fffffff;
-      for (int i = tid; i < nb; i += BS_THREADS) {
-        if (!sel[i]) continue;
-        const float x8 = lse8[i], x16 = lse16[i];
-        const bool after8 = (x8 < last8) || (x8 == last8 && i > idx8);
-        const bool after16 = (x16 < last16) || (x16 == last16 && i > idx16);
-        if (after8 && (x8 > b8 || (x8 == b8 && i < i8))) { b8 = x8; i8 = i; }
-        if (after16 && (x16 > b16 || (x16 == b16 && i < i16))) { b16 = x16; i16 = i; }
+      for (int i4 = tid; i4 < (nb + 3) / 4; i4 += BS_THREADS) {
+        const uchar4 s4 = reinterpret_cast<const uchar4*>(sel)[i4];
+        if ((s4.x | s4.y | s4.z | s4.w) == 0) continue;
+        const float4 l8 = reinterpret_cast<const float4*>(lse8)[i4];
+        const float4 l16 = reinterpret_cast<const float4*>(lse16)[i4];
+        const unsigned char sv[4] = {s4.x, s4.y, s4.z, s4.w};
+        const float a8[4] = {l8.x, l8.y, l8.z, l8.w}, a16[4] = {l16.x, l16.y, l16.z, l16.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = 4 * i4 + j;
+          if (i >= nb || !sv[j]) continue;
+          const float x8 = a8[j], x16 = a16[j];
+          const bool after8 = (x8 < last8) || (x8 == last8 && i > idx8);
+          const bool after16 = (x16 < last16) || (x16 == last16 && i > idx16);
+          if (after8 && (x8 > b8 || (x8 == b8 && i < i8))) { b8 = x8; i8 = i; }
+          if (after16 && (x16 > b16 || (x16 == b16 && i < i16))) { b16 = x16; i16 = i; }
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {

@@ -131,6 +131,21 @@ kvq_status kvq_decode_attention(kvq_cache* cache, int layer, const void* q, floa
                                 float eps, void* out, kvq_certificate* cert,
                                 int32_t* ladder_level, void* stream);
 
+/* kvq_decode_attention_uncertified -- plain quantized decode attention: INT8 key scores
+ * and INT4 values on every full block, exact FP16 on the partial block.  No block is
+ * paged in from tier 2, no ranking check runs and no rung of the fallback ladder is
+ * taken.  This is the uncertified INT8/INT4 baseline that the paper sets against the
+ * certified path (Experiments, retrieval), and the speed ceiling of the tier-1 data.
+ *   q, out, stream  as kvq_decode_attention
+ *   cert            [B * Hq] (may be NULL): e_key and e_val are the bounds of this output,
+ *                   computed as in kvq_decode_attention but not enforced; rank_ok 1,
+ *                   level 0, k_star 0, n_val_promoted 0, promoted_bytes 0.
+ * Debug flags that force rungs are ignored.  The selection state it leaves (nothing
+ * selected) is what kvq_export_decode_state reports afterwards.
+ * Errors: KVQ_ERR_INVALID (layer out of range, empty layer, NULL q/out), KVQ_ERR_CUDA. */
+kvq_status kvq_decode_attention_uncertified(kvq_cache* cache, int layer, const void* q,
+                                            void* out, kvq_certificate* cert, void* stream);
+
 /* kvq_last_error -- text of the calling thread's last error ("" if none).  The pointer
  * stays valid until the thread's next failing call. */
 const char* kvq_last_error(void);

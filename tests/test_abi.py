@@ -38,6 +38,8 @@ def test_null_and_invalid_arguments_without_gpu():
     assert lib.kvq_cache_destroy(None) == kvq.KVQ_OK
     assert lib.kvq_append(None, 0, None, None, 1, None) == kvq.KVQ_ERR_INVALID
     assert lib.kvq_decode_attention(None, 0, None, 0.9, 0.25, None, None, None, None) == kvq.KVQ_ERR_INVALID
+    assert lib.kvq_decode_attention_uncertified(None, 0, None, None, None, None) == kvq.KVQ_ERR_INVALID
+    assert b"kvq_decode_attention_uncertified" in lib.kvq_last_error()
 
 
 def test_certificate_layout_matches_header():
