@@ -43,124 +43,189 @@ __device__ __forceinline__ void vc_offset(int t, int c, int& word_byte, int& bit
   word_byte = ((g * 2 + mt) * 32 + gid * 4 + tig) * 16 + kk * 4;
 }
 
-// One CTA per (touched block, sequence x KV head); 128 threads, thread = channel.
+constexpr int SROW = D + 8;   // padded shared row (272 bytes): fewer bank conflicts
+
+// One CTA per (touched block, sequence x KV head), 128 threads.  The block's FP16 tokens
+// (old partial-block tokens, then new ones) are staged in shared memory with 16-byte
+// loads (VEC; element loads when the caller's buffers are not 16-byte aligned).  A
+// completed block is quantised with each thread producing whole 16-byte key chunks and
+// whole 32-bit value words of the fragment-ordered layouts, written straight to tier 1.
+template <bool VEC>
 __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
-  __shared__ __half sk[BLK][D];
-  __shared__ __half sv[BLK][D];
-  __shared__ uint32_t kcode[KC_BYTES / 4];
-  __shared__ uint32_t vcode[VC_BYTES / 4];
+  __shared__ __align__(16) __half sk[BLK][SROW];
+  __shared__ __align__(16) __half sv[BLK][SROW];
+  __shared__ __align__(16) float kscale[D];
+  __shared__ float vsc[BLK][NG], voff[BLK][NG];
   __shared__ float red[4];
   __shared__ uint32_t smax_k, smax_v;
 
-  const int c = threadIdx.x;
+  const int tid = threadIdx.x;
   const int hs = blockIdx.y;
   const int blk = a.first_blk + blockIdx.x;
   const int t0 = blk * BLK;                         // first token of the block
   const int end = a.pos + a.n;                      // tokens after the append
   const int t_hi = min(t0 + BLK, end);
-  const bool complete = (t0 + BLK) <= end;
+  const int rows = t_hi - t0;
+  const bool complete = rows == BLK;
 
-  // gather the block's FP16 tokens: old partial-block tokens, then new ones
-  float lo = INFINITY, hi = -INFINITY;
-  for (int t = t0; t < t_hi; ++t) {
-    __half kv, vv;
-    if (t < a.pos) {
-      const size_t o = ((size_t)hs * BLK + (t - t0)) * D + c;
-      kv = a.tail_k_in[o];
-      vv = a.tail_v_in[o];
-    } else {
-      const size_t o = ((size_t)hs * a.n + (t - a.pos)) * D + c;
-      kv = a.k[o];
-      vv = a.v[o];
-      const float f = __half2float(vv);
-      lo = fminf(lo, f);
-      hi = fmaxf(hi, f);
+  // ---- gather the block's FP16 tokens ----
+  if (VEC) {
+    uint4 kr[8], vr[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = tid + 128 * j, row = i >> 4, col = (i & 15) * 8;
+      const int t = t0 + row;
+      kr[j] = make_uint4(0, 0, 0, 0);
+      vr[j] = kr[j];
+      if (row < rows) {
+        const size_t o = (t < a.pos) ? ((size_t)hs * BLK + row) * D + col
+                                     : ((size_t)hs * a.n + (t - a.pos)) * D + col;
+        const __half* kp = (t < a.pos) ? a.tail_k_in : a.k;
+        const __half* vp = (t < a.pos) ? a.tail_v_in : a.v;
+        kr[j] = *reinterpret_cast<const uint4*>(kp + o);
+        vr[j] = *reinterpret_cast<const uint4*>(vp + o);
+      }
     }
-    sk[t - t0][c] = kv;
-    sv[t - t0][c] = vv;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = tid + 128 * j, row = i >> 4, col = (i & 15) * 8;
+      *reinterpret_cast<uint4*>(&sk[row][col]) = kr[j];
+      *reinterpret_cast<uint4*>(&sv[row][col]) = vr[j];
+    }
+  } else {
+    for (int row = 0; row < rows; ++row) {
+      const int t = t0 + row;
+      const size_t o = (t < a.pos) ? ((size_t)hs * BLK + row) * D + tid
+                                   : ((size_t)hs * a.n + (t - a.pos)) * D + tid;
+      sk[row][tid] = (t < a.pos) ? a.tail_k_in[o] : a.k[o];
+      sv[row][tid] = (t < a.pos) ? a.tail_v_in[o] : a.v[o];
+    }
   }
-  if (t_hi > a.pos) {
-    atomicMin(&a.vmin[hs * D + c], f2ord(lo));
-    atomicMax(&a.vmax[hs * D + c], f2ord(hi));
+  __syncthreads();
+
+  // ---- value ranges over the new tokens (thread = channel) ----
+  {
+    const int r0 = max(a.pos, t0) - t0;
+    if (r0 < rows) {
+      float lo = INFINITY, hi = -INFINITY;
+      for (int row = r0; row < rows; ++row) {
+        const float f = __half2float(sv[row][tid]);
+        lo = fminf(lo, f);
+        hi = fmaxf(hi, f);
+      }
+      atomicMin(&a.vmin[hs * D + tid], f2ord(lo));
+      atomicMax(&a.vmax[hs * D + tid], f2ord(hi));
+    }
   }
 
   if (!complete) {
-    // the block stays FP16: write it (old and new tokens) to the outgoing partial buffer
-    for (int t = t0; t < t_hi; ++t) {
-      const size_t o = ((size_t)hs * BLK + (t - t0)) * D + c;
-      a.tail_k_out[o] = sk[t - t0][c];
-      a.tail_v_out[o] = sv[t - t0][c];
+    // the block stays FP16: copy it (old and new tokens) to the outgoing partial buffer
+    for (int i = tid; i < rows * (D / 8); i += 128) {
+      const int row = i >> 4, col = (i & 15) * 8;
+      const size_t o = ((size_t)hs * BLK + row) * D + col;
+      *reinterpret_cast<uint4*>(a.tail_k_out + o) = *reinterpret_cast<const uint4*>(&sk[row][col]);
+      *reinterpret_cast<uint4*>(a.tail_v_out + o) = *reinterpret_cast<const uint4*>(&sv[row][col]);
     }
     return;
   }
-
-  for (int i = c; i < KC_BYTES / 4; i += 128) kcode[i] = 0u;
-  for (int i = c; i < VC_BYTES / 4; i += 128) vcode[i] = 0u;
-  if (c == 0) { smax_k = 0u; smax_v = 0u; }
-  __syncthreads();
-
-  // ---- keys: one fp16 scale per channel, rounded up; symmetric INT8 codes ----
-  float amax = 0.f;
-  for (int t = 0; t < BLK; ++t) amax = fmaxf(amax, fabsf(__half2float(sk[t][c])));
-  const __half s_h = __float2half_ru(__fdiv_rn(amax, 127.f));
-  const float s = __half2float(s_h);
+  if (tid == 0) { smax_k = 0u; smax_v = 0u; }
   const size_t blk_index = (size_t)hs * a.nbmax + blk;
-  a.ks[blk_index * D + c] = s_h;
-  atomicMax(&smax_k, (uint32_t)__half_as_ushort(s_h));
-  for (int t = 0; t < BLK; ++t) {
-    int code = 0;
-    if (s > 0.f) {
-      const float r = rintf(__fdiv_rn(__half2float(sk[t][c]), s));
-      code = (int)fminf(fmaxf(r, -127.f), 127.f);
-    }
-    const int off = kc_offset(t, c);
-    atomicOr(&kcode[off >> 2], ((uint32_t)(code & 0xff)) << (8 * (off & 3)));
-  }
 
-  // ---- values: per (token, 32-channel group) offset = min, scale rounded up; INT4 ----
-  float errmax = 0.f;
-  for (int p = c; p < BLK * NG; p += 128) {
+  // ---- key scales: one fp16 per channel, rounded up (thread = channel) ----
+  {
+    float amax = 0.f;
+    for (int t = 0; t < BLK; ++t) amax = fmaxf(amax, fabsf(__half2float(sk[t][tid])));
+    const __half s_h = __float2half_ru(__fdiv_rn(amax, 127.f));
+    a.ks[blk_index * D + tid] = s_h;
+    kscale[tid] = __half2float(s_h);
+    __syncthreads();   // smax_k initialised, kscale complete
+    atomicMax(&smax_k, (uint32_t)__half_as_ushort(s_h));
+  }
+  // ---- value scale/offset per (token, 32-channel group): offset = min, scale rounded up ----
+  for (int p = tid; p < BLK * NG; p += 128) {
     const int t = p >> 2, g = p & 3;
     float mn = INFINITY, mx = -INFINITY;
-    for (int j = 0; j < VG; ++j) {
-      const float f = __half2float(sv[t][g * VG + j]);
-      mn = fminf(mn, f);
-      mx = fmaxf(mx, f);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = *reinterpret_cast<const uint4*>(&sv[t][g * VG + 8 * q]);
+      const __half2* h2 = reinterpret_cast<const __half2*>(&w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __half22float2(h2[e]);
+        mn = fminf(mn, fminf(f.x, f.y));
+        mx = fmaxf(mx, fmaxf(f.x, f.y));
+      }
     }
     const __half vs_h = __float2half_ru(__fdiv_rn(__fsub_rn(mx, mn), 15.f));
-    const float vs = __half2float(vs_h);
     const __half vo_h = __float2half_rn(mn);  // exact: mn is an fp16 value
-    atomicMax(&smax_v, (uint32_t)__half_as_ushort(vs_h));
     a.vsv[blk_index * VSV_WORDS + g * BLK + t] = __halves2half2(vs_h, vo_h);
-    for (int j = 0; j < VG; ++j) {
-      const int ch = g * VG + j;
-      const float f = __half2float(sv[t][ch]);
-      int code = 0;
-      if (vs > 0.f) {
-        const float r = rintf(__fdiv_rn(__fsub_rn(f, mn), vs));
-        code = (int)fminf(fmaxf(r, 0.f), 15.f);
-      }
-      const float vhat = __fadd_rn(__fmul_rn(vs, (float)code), mn);
-      errmax = fmaxf(errmax, fabsf(__fsub_rn(f, vhat)));
-      int wb, bit;
-      vc_offset(t, ch, wb, bit);
-      atomicOr(&vcode[wb >> 2], ((uint32_t)code) << bit);
-    }
+    vsc[t][g] = __half2float(vs_h);
+    voff[t][g] = mn;
+    atomicMax(&smax_v, (uint32_t)__half_as_ushort(vs_h));
   }
-  errmax = warp_max(errmax);
-  if ((c & 31) == 0) red[c >> 5] = errmax;
   __syncthreads();
 
-  // ---- write the block: coalesced 16-byte stores of the fragment-ordered codes ----
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(kcode);
-    uint4* dst = reinterpret_cast<uint4*>(a.kc + blk_index * KC_BYTES);
-    for (int i = c; i < KC_BYTES / 16; i += 128) dst[i] = src[i];
-    const uint4* srcv = reinterpret_cast<const uint4*>(vcode);
-    uint4* dstv = reinterpret_cast<uint4*>(a.vc + blk_index * VC_BYTES);
-    for (int i = c; i < VC_BYTES / 16; i += 128) dstv[i] = srcv[i];
+  // ---- key codes: 512 chunks of 16 codes (one token, 16 channels) in fragment order ----
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int q = tid + 128 * j;            // chunk index = ((w * 4 + jj) * 32 + gid * 4 + tig)
+    const int tig = q & 3, gid = (q >> 2) & 7, jj = (q >> 5) & 3, w = q >> 7;
+    const int t = w * 16 + (jj >> 1) * 8 + gid;
+    const int c0 = tig * 32 + (jj & 1) * 16;
+    uint32_t word[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint2 kh = *reinterpret_cast<const uint2*>(&sk[t][c0 + 4 * u]);
+      const float4 sc = *reinterpret_cast<const float4*>(&kscale[c0 + 4 * u]);
+      const __half2* h2 = reinterpret_cast<const __half2*>(&kh);
+      const float2 f01 = __half22float2(h2[0]), f23 = __half22float2(h2[1]);
+      const float fv[4] = {f01.x, f01.y, f23.x, f23.y}, sv4[4] = {sc.x, sc.y, sc.z, sc.w};
+      uint32_t packed = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int code = 0;
+        if (sv4[e] > 0.f) {
+          const float r = rintf(__fdiv_rn(fv[e], sv4[e]));
+          code = (int)fminf(fmaxf(r, -127.f), 127.f);
+        }
+        packed |= ((uint32_t)(code & 0xff)) << (8 * e);
+      }
+      word[u] = packed;
+    }
+    reinterpret_cast<uint4*>(a.kc + blk_index * KC_BYTES)[q] = make_uint4(word[0], word[1], word[2], word[3]);
   }
-  if (c == 0) {
+
+  // ---- value codes: 1024 words of 8 nibbles (4 tokens x 2 channels) in fragment order ----
+  float errmax = 0.f;
+#pragma unroll 2
+  for (int j = 0; j < 8; ++j) {
+    const int wi = tid + 128 * j;           // word = ((g * 2 + mt) * 32 + gid * 4 + tig) * 4 + kk
+    const int kk = wi & 3, tig = (wi >> 2) & 3, gid = (wi >> 4) & 7, mt = (wi >> 7) & 1, g = wi >> 8;
+    const int cb = g * VG + mt * 16 + gid;
+    uint32_t word = 0u;
+#pragma unroll
+    for (int tpos = 0; tpos < 4; ++tpos) {
+      const int t = tig * 16 + kk * 4 + tpos;
+      const float vs = vsc[t][g], mn = voff[t][g];
+#pragma unroll
+      for (int chhalf = 0; chhalf < 2; ++chhalf) {
+        const float f = __half2float(sv[t][cb + 8 * chhalf]);
+        int code = 0;
+        if (vs > 0.f) {
+          const float r = rintf(__fdiv_rn(__fsub_rn(f, mn), vs));
+          code = (int)fminf(fmaxf(r, 0.f), 15.f);
+        }
+        const float vhat = __fadd_rn(__fmul_rn(vs, (float)code), mn);
+        errmax = fmaxf(errmax, fabsf(__fsub_rn(f, vhat)));
+        word |= ((uint32_t)code) << (4 * ((tpos >> 1) * 2 + chhalf) + 16 * (tpos & 1));
+      }
+    }
+    reinterpret_cast<uint32_t*>(a.vc + blk_index * VC_BYTES)[wi] = word;
+  }
+  errmax = warp_max(errmax);
+  if ((tid & 31) == 0) red[tid >> 5] = errmax;
+  __syncthreads();
+  if (tid == 0) {
     a.eta[blk_index] = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     atomicMax(&a.kscale_max[hs], smax_k);
     atomicMax(&a.vscale_max[hs], smax_v);
@@ -223,7 +288,9 @@ cudaError_t launch_append(const LayerAppend& L, const void* k, const void* v, in
   a.tail_k_out = L.tail_k_out; a.tail_v_out = L.tail_v_out; a.nbmax = L.nbmax;
   const int last_blk = (pos + n - 1) / BLK;
   dim3 grid(last_blk - a.first_blk + 1, L.BG);
-  append_kernel<<<grid, 128, 0, st>>>(a);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
+  if (aligned) append_kernel<true><<<grid, 128, 0, st>>>(a);
+  else append_kernel<false><<<grid, 128, 0, st>>>(a);
   return cudaGetLastError();
 }
 
