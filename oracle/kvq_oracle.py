@@ -50,6 +50,11 @@ class OracleConfig:
     rank_positions: int = 1        # ranking check compares the top-R positions of S_h
     l4_head_fraction: float = 0.5  # L4 when >= this fraction of a sequence's heads reach L3
     kappa: float = KAPPA
+    # FP16-values configuration (the pages' ablation that replaces the INT4 values with
+    # FP16 values, Results: structured reasoning): values stay FP16 in VRAM, so every
+    # block counts as value-promoted from the start, E_val = 0, rung 2 has nothing to
+    # page in and tier 2 holds (and pages in) keys only.
+    value_fp16: bool = False
 
 
 # --------------------------------------------------------------------------------------
@@ -476,7 +481,7 @@ def decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Tier1,
                 U = np.zeros(nb, bool)
                 for h in heads:
                     U[per[h]["chosen"]] = True
-                Vp = np.zeros(nb, bool)
+                Vp = np.full(nb, cfg.value_fp16, bool)   # FP16 values resident in VRAM
                 kprom0[b, g] = U
                 group_bytes[b, g] += int(U.sum()) * blk_bytes
                 adds_k, adds_v, asking = [], [], []
@@ -501,8 +506,9 @@ def decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Tier1,
                     U1[adds_k] = True
                     V1[adds_v] = True
                     # each FP16 block is paged in once per call: rung 1 adds only the
-                    # new key blocks, rung 2 the value blocks
-                    group_bytes[b, g] += (int(U1.sum()) - int(U.sum()) + int(V1.sum())) * blk_bytes
+                    # new key blocks, rung 2 the new value blocks
+                    group_bytes[b, g] += (int(U1.sum()) - int(U.sum())
+                                          + int(V1.sum()) - int(Vp.sum())) * blk_bytes
                     for h in asking:
                         P = per[h]
                         r1 = mixed_attention(P["s_ex"], P["s_hat"], Vg, v_hat, P["delta"], eta, R, U1, V1)
@@ -510,7 +516,7 @@ def decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Tier1,
                         out64[b, h] = r1.out
                         e_key[b, h] = r1.e_key
                         e_val[b, h] = r1.e_val
-                        n_vprom[b, h] = int(V1.sum())
+                        n_vprom[b, h] = int(V1.sum()) - int(Vp.sum())   # paged in
                         if r1.e_key + r1.e_val > eps:
                             level[b, h] = 3
                 kprom1[b, g] = U1; vprom1[b, g] = V1
@@ -525,7 +531,8 @@ def decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Tier1,
         for g in range(Hkv):
             heads = range(g * cfg.n_rep, (g + 1) * cfg.n_rep)
             if any(level[b, h] >= 3 for h in heads):
-                group_bytes[b, g] += 2 * nb * blk_bytes
+                # K and V of every full block from tier 2 (K only with FP16 values)
+                group_bytes[b, g] += (1 if cfg.value_fp16 else 2) * nb * blk_bytes
             for h in heads:
                 if level[b, h] >= 3:
                     out64[b, h] = dense_attention(q[b, h], K[b, g], V[b, g])
@@ -557,7 +564,8 @@ def uncertified_decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Ti
     """The plain INT8/INT4 baseline the paper compares against (Experiments, retrieval):
     INT8 key scores and INT4 values on every full block, the FP16 originals on the
     partial block, nothing promoted and no ladder.  Its output is mixed_attention with
-    empty promotion sets; the bounds are those of that output, reported only."""
+    empty promotion sets (every block value-promoted with FP16 values, cfg.value_fp16);
+    the bounds are those of that output, reported only."""
     B, Hq, D = q.shape
     _, Hkv, N, _ = K.shape
     assert Hq % Hkv == 0
@@ -565,6 +573,7 @@ def uncertified_decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Ti
     nb = N // BLOCK
     inv = 1.0 / math.sqrt(D)
     none = np.zeros(nb, bool)
+    vprom = np.full(nb, cfg.value_fp16, bool)
     out64 = np.zeros((B, Hq, D))
     e_key = np.zeros((B, Hq)); e_val = np.zeros((B, Hq))
     for b in range(B):
@@ -577,7 +586,7 @@ def uncertified_decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Ti
                 s_ex = Kg.astype(np.float64) @ qh.astype(np.float64) * inv
                 s_hat = int8_scores(qh, t1.kc[b, g], t1.ks[b, g])
                 delta = score_perturbation(qh, t1.ks[b, g], cfg.kappa)
-                r = mixed_attention(s_ex, s_hat, Vg, v_hat, delta, t1.eta[b, g], R, none, none)
+                r = mixed_attention(s_ex, s_hat, Vg, v_hat, delta, t1.eta[b, g], R, none, vprom)
                 out64[b, h] = r.out
                 e_key[b, h] = r.e_key
                 e_val[b, h] = r.e_val

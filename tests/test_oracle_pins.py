@@ -589,3 +589,61 @@ def test_uncertified_bound_is_sound():
             err = np.max(np.abs(res.out64[0, h] - ref))
             assert err <= res.e_key[0, h] + res.e_val[0, h] + 1e-9
 
+
+# ---------------------------------------------------------------------------------
+# FP16-values configuration (Results: the ablation that replaces INT4 values by FP16)
+# ---------------------------------------------------------------------------------
+
+def _grid_keys(rng, n, D=128, s0=2.0 ** -5):
+    codes = rng.integers(-126, 127, (n, D))
+    codes[::64] = 127                                  # every block's scales are exactly s0
+    return (codes * s0).astype(np.float16)
+
+
+def test_fp16_values_on_grid_keys_equal_dense():
+    """Keys on their INT8 grid reconstruct exactly and the values are the FP16 originals,
+    so every certified head returns dense attention (the INT4 path would not: the values
+    here are off the INT4 grid) and E_val = 0."""
+    rng = np.random.default_rng(31)
+    for ctx in (64 * 5, 64 * 7 + 19):
+        K = _grid_keys(rng, ctx)[None, None]
+        V = rng.standard_normal((1, 1, ctx, 128)).astype(np.float16)
+        q = (rng.standard_normal((1, 4, 128)) * 0.3).astype(np.float16)
+        t1 = O.quantize_layer(K, V)
+        cfg = O.OracleConfig(n_rep=4, value_fp16=True)
+        r = O.decode_layer(q, K, V, t1, 0.9, float("inf"), cfg)
+        u = O.uncertified_decode_layer(q, K, V, t1, cfg)
+        assert np.all(r.e_val == 0.0) and np.all(u.e_val == 0.0)
+        assert np.all(r.level == 0) and np.all(r.n_val_promoted == 0)
+        for h in range(4):
+            ref = O.dense_attention(q[0, h], K[0, 0], V[0, 0])
+            np.testing.assert_allclose(r.out64[0, h], ref, rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(u.out64[0, h], ref, rtol=1e-12, atol=1e-13)
+        # the INT4 configuration differs on the same inputs
+        r4 = O.decode_layer(q, K, V, t1, 0.9, float("inf"), O.OracleConfig(n_rep=4))
+        assert np.max(np.abs(r4.out64 - r.out64)) > 1e-4
+
+
+def test_fp16_values_bound_sound_and_no_value_pages():
+    rng = np.random.default_rng(32)
+    for seed in range(5):
+        q, K, V = _case(seed=400 + seed, ctx=int(rng.integers(64, 900)), Hq=8, Hkv=2, kscale=4.0)
+        t1 = O.quantize_layer(K, V)
+        cfg = O.OracleConfig(n_rep=4, value_fp16=True)
+        r = O.decode_layer(q, K, V, t1, 0.9, 0.05, cfg)
+        nb = K.shape[2] // 64
+        assert np.all(r.e_val == 0.0) and np.all(r.n_val_promoted == 0)
+        assert np.all(r.vprom1 == (nb > 0))            # every block counts as FP16-valued
+        for h in range(8):
+            ref = O.dense_attention(q[0, h], K[0, h // 4], V[0, h // 4])
+            err = np.max(np.abs(r.out64[0, h] - ref))
+            assert err <= r.e_key[0, h] + 1e-9
+            if r.level[0, h] >= 3:
+                assert err <= 1e-12
+        for g in range(2):
+            heads = range(4 * g, 4 * g + 4)
+            k_blocks = int(r.kprom1[0, g].sum())
+            dense = any(r.level[0, h] >= 3 for h in heads)
+            want = (k_blocks + (nb if dense else 0)) * 64 * 128 * 2
+            assert int(r.promoted_bytes[0, 4 * g]) == want
+
