@@ -282,6 +282,51 @@ def measure_append(torch, kvq, W, wl, hbm_peak, reps=2):
                                     "peak": hbm_peak, "frac": hbm_bytes / (kern_us * 1e-6) / 1e9 / hbm_peak}}
 
 
+def measure_fp16_values(args, wl):
+    """The FP16-values configuration (value_bits 16) on the same synthetic caches: FP16
+    values resident in VRAM, keys-only tier 2.  Same timing protocol as the headline."""
+    import torch
+    import certified_quantized_kv_gb300 as kvq
+    import workloads as W
+    B, L, N = wl["batch"], wl["layers"], wl["ctx"]
+    Hq, Hkv, D = wl["q_heads"], wl["kv_heads"], wl["head_dim"]
+    tau, eps = wl["tau_cov"], wl["eps"]
+    cache = kvq.Cache(L, B, Hq, Hkv, max_ctx=N, value_bits=16)
+    qs = []
+    for layer in range(L):
+        q, K, V = W.c3_layer(layer, device="cuda", seed=wl["seed"], batch=B, ctx=N, Hq=Hq, Hkv=Hkv)
+        cache.append(layer, K.contiguous(), V.contiguous())
+        qs.append(q.contiguous())
+        del K, V
+    out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+    certs = [torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda") for _ in range(L)]
+
+    def step():
+        for layer in range(L):
+            cache.decode(layer, qs[layer], tau, eps, out, certs[layer])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    hist, prom = [0] * 5, 0
+    for layer in range(L):
+        c = kvq.certificates(certs[layer]).reshape(B, Hq)
+        for lv in c["level"].ravel():
+            hist[int(lv)] += 1
+        prom += int(c["promoted_bytes"][:, :: Hq // Hkv].sum())
+    cache.close()
+    return {"value": B * L / (ms / 1e3), "unit": UNIT, "ms_per_step": ms, "ladder_histogram": hist,
+            "promoted_bytes_per_step": prom, "vram_bytes_per_token_head": 128 + 4 + 256,
+            "what": "value_bits 16: INT8 keys, FP16 values in VRAM, keys-only tier 2"}
+
+
 def our_arm(args, wl):
     import torch
     import torch.distributed as dist
@@ -478,8 +523,9 @@ def our_arm(args, wl):
         except Exception as e:  # pragma: no cover
             line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
                                     "sample": f"failed: {e}"[:200]}
-    print(json.dumps(line), flush=True)
     cache.close()
+    line["fp16_values"] = measure_fp16_values(args, wl)
+    print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 

@@ -71,7 +71,8 @@ struct kvq_cache {
   // tier 1, all layers in one allocation
   char* t1 = nullptr;
   size_t off_kc = 0, off_ks = 0, off_vc = 0, off_vsv = 0, off_eta = 0, off_vmin = 0, off_vmax = 0,
-         off_ksm = 0, off_vsm = 0, off_tail = 0, t1_layer = 0;
+         off_ksm = 0, off_vsm = 0, off_tail = 0, off_v16 = 0, t1_layer = 0;
+  bool v16 = false;   // FP16 values in tier 1 (value_bits 16); tier 2 then holds keys only
   // tier 2: pinned, mapped host memory, per layer
   std::vector<__half*> t2k_host, t2v_host;
   std::vector<__half*> t2k_dev, t2v_dev;
@@ -110,6 +111,9 @@ uint32_t* layer_vmin(kvq_cache* c, int l) { return reinterpret_cast<uint32_t*>(c
 uint32_t* layer_vmax(kvq_cache* c, int l) { return reinterpret_cast<uint32_t*>(c->t1 + c->t1_layer * l + c->off_vmax); }
 uint32_t* layer_ksm(kvq_cache* c, int l) { return reinterpret_cast<uint32_t*>(c->t1 + c->t1_layer * l + c->off_ksm); }
 uint32_t* layer_vsm(kvq_cache* c, int l) { return reinterpret_cast<uint32_t*>(c->t1 + c->t1_layer * l + c->off_vsm); }
+__half* layer_v16(kvq_cache* c, int l) {
+  return c->v16 ? reinterpret_cast<__half*>(c->t1 + c->t1_layer * l + c->off_v16) : nullptr;
+}
 // partial-block buffers: [parity][K|V][BG][64][128]
 __half* layer_tail(kvq_cache* c, int l, int parity, int kv) {
   __half* base = reinterpret_cast<__half*>(c->t1 + c->t1_layer * l + c->off_tail);
@@ -123,6 +127,7 @@ LayerAppend append_view(kvq_cache* c, int l) {
   a.kc = layer_kc(c, l); a.ks = layer_ks(c, l); a.vc = layer_vc(c, l); a.vsv = layer_vsv(c, l);
   a.eta = layer_eta(c, l); a.vmin = layer_vmin(c, l); a.vmax = layer_vmax(c, l);
   a.kscale_max = layer_ksm(c, l); a.vscale_max = layer_vsm(c, l);
+  a.v16 = layer_v16(c, l);
   const int p = c->tail_parity[l];
   a.tail_k_in = layer_tail(c, l, p, 0); a.tail_v_in = layer_tail(c, l, p, 1);
   a.tail_k_out = layer_tail(c, l, 1 - p, 0); a.tail_v_out = layer_tail(c, l, 1 - p, 1);
@@ -225,6 +230,8 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
     return fail(KVQ_ERR_INVALID, "max_ctx must be <= 2097152 tokens");
   if (!(k.l4_head_fraction > 0.f && k.l4_head_fraction <= 1.f))
     return fail(KVQ_ERR_INVALID, "l4_head_fraction must be in (0, 1]");
+  if (k.value_bits != 0 && k.value_bits != 4 && k.value_bits != 16)
+    return fail(KVQ_ERR_INVALID, "value_bits must be 4 (or 0) or 16");
 
   kvq_cache* c = new kvq_cache();
   c->cfg = k;
@@ -237,14 +244,17 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   c->cap = (long long)((k.max_ctx + BLK - 1) / BLK) * BLK;
   c->n_tokens.assign(c->L, 0);
   c->tail_parity.assign(c->L, 0);
+  c->v16 = k.value_bits == 16;
 
-  // ---- tier 1 ----
+  // ---- tier 1 (INT4 value codes and scale/offset, or FP16 values) ----
   const size_t BG = c->BG, nbm = c->nbmax;
+  const size_t n4 = c->v16 ? 0 : BG * nbm, n16 = c->v16 ? BG * nbm : 0;
   size_t o = 0;
   c->off_kc = o;   o = align_up(o + BG * nbm * KC_BYTES, 256);
   c->off_ks = o;   o = align_up(o + BG * nbm * D * 2, 256);
-  c->off_vc = o;   o = align_up(o + BG * nbm * VC_BYTES, 256);
-  c->off_vsv = o;  o = align_up(o + BG * nbm * VSV_WORDS * 4, 256);
+  c->off_vc = o;   o = align_up(o + n4 * VC_BYTES, 256);
+  c->off_vsv = o;  o = align_up(o + n4 * VSV_WORDS * 4, 256);
+  c->off_v16 = o;  o = align_up(o + n16 * BLK * D * 2, 256);
   c->off_eta = o;  o = align_up(o + BG * nbm * 4, 256);
   c->off_vmin = o; o = align_up(o + BG * D * 4, 256);
   c->off_vmax = o; o = align_up(o + BG * D * 4, 256);
@@ -268,7 +278,7 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   c->t2k_host.assign(c->L, nullptr); c->t2v_host.assign(c->L, nullptr);
   c->t2k_dev.assign(c->L, nullptr); c->t2v_dev.assign(c->L, nullptr);
   for (int l = 0; l < c->L; ++l) {
-    for (int kv = 0; kv < 2; ++kv) {
+    for (int kv = 0; kv < (c->v16 ? 1 : 2); ++kv) {   // FP16 values need no tier-2 copy
       void* h = nullptr;
       if (cudaHostAlloc(&h, t2bytes, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
         cudaGetLastError();
@@ -392,8 +402,9 @@ kvq_status kvq_append(kvq_cache* c, int layer, const void* k, const void* v, int
   const size_t width = (size_t)n * D * sizeof(__half);
   KVQ_CUDA(cudaMemcpy2DAsync(c->t2k_host[layer] + (size_t)pos * D, dpitch, k, width, width, c->BG,
                              cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror K");
-  KVQ_CUDA(cudaMemcpy2DAsync(c->t2v_host[layer] + (size_t)pos * D, dpitch, v, width, width, c->BG,
-                             cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror V");
+  if (!c->v16)
+    KVQ_CUDA(cudaMemcpy2DAsync(c->t2v_host[layer] + (size_t)pos * D, dpitch, v, width, width, c->BG,
+                               cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror V");
   KVQ_CUDA(cudaEventRecord(c->ev_mirror, c->side), "kvq_append: event");
   {
     KernelScope ks(c, K_APPEND, st);
@@ -457,7 +468,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   V.kscale_max = layer_ksm(c, layer); V.vscale_max = layer_vsm(c, layer);
   const int p = c->tail_parity[layer];
   V.tail_k = layer_tail(c, layer, p, 0); V.tail_v = layer_tail(c, layer, p, 1);
-  V.t2k = c->t2k_dev[layer]; V.t2v = c->t2v_dev[layer];
+  V.t2k = c->t2k_dev[layer]; V.t2v = c->t2v_dev[layer]; V.v16 = layer_v16(c, layer);
   V.q = qd; V.out = od; V.tau = tau; V.eps = eps;
   V.l4_frac = c->cfg.l4_head_fraction; V.rank_positions = c->cfg.rank_positions;
   V.debug = certified ? c->debug : (c->debug & ~(KVQ_DEBUG_FORCE_RANK_FAIL | KVQ_DEBUG_FORCE_DENSE));

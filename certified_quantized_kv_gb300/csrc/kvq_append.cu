@@ -25,6 +25,7 @@ struct AppendArgs {
   __half* tail_k_out;       // [BG][64][128] partial block after it
   __half* tail_v_out;
   int nbmax;
+  __half* v16;              // FP16 values of full blocks (value_bits 16), or nullptr
 };
 
 __device__ __forceinline__ int kc_offset(int t, int c) {
@@ -141,8 +142,16 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
     __syncthreads();   // smax_k initialised, kscale complete
     atomicMax(&smax_k, (uint32_t)__half_as_ushort(s_h));
   }
+  if (a.v16) {
+    // FP16-values configuration: the block's values are stored as they are; eta = 0
+    __half* dst = a.v16 + blk_index * (BLK * D);
+    for (int i = tid; i < BLK * (D / 8); i += 128) {
+      const int row = i >> 4, col = (i & 15) * 8;
+      *reinterpret_cast<uint4*>(dst + row * D + col) = *reinterpret_cast<const uint4*>(&sv[row][col]);
+    }
+  }
   // ---- value scale/offset per (token, 32-channel group): offset = min, scale rounded up ----
-  for (int p = tid; p < BLK * NG; p += 128) {
+  for (int p = tid; p < BLK * NG && !a.v16; p += 128) {
     const int t = p >> 2, g = p & 3;
     float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
@@ -198,7 +207,7 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
   // ---- value codes: 1024 words of 8 nibbles (4 tokens x 2 channels) in fragment order ----
   float errmax = 0.f;
 #pragma unroll 2
-  for (int j = 0; j < 8; ++j) {
+  for (int j = 0; j < 8 && !a.v16; ++j) {
     const int wi = tid + 128 * j;           // word = ((g * 2 + mt) * 32 + gid * 4 + tig) * 4 + kk
     const int kk = wi & 3, tig = (wi >> 2) & 3, gid = (wi >> 4) & 7, mt = (wi >> 7) & 1, g = wi >> 8;
     const int cb = g * VG + mt * 16 + gid;
@@ -264,7 +273,7 @@ __global__ void __launch_bounds__(128) export_tier1_kernel(ExportArgs a) {
     }
   }
   if (a.oks) a.oks[dst * D + c] = a.ks[src * D + c];
-  for (int p = c; p < BLK * NG; p += 128) {
+  for (int p = c; p < BLK * NG && (a.ovs || a.ovo); p += 128) {
     const int t = p >> 2, g = p & 3;
     const __half2 so = a.vsv[src * VSV_WORDS + g * BLK + t];
     if (a.ovs) a.ovs[(dst * BLK + t) * NG + g] = __low2half(so);
@@ -286,6 +295,7 @@ cudaError_t launch_append(const LayerAppend& L, const void* k, const void* v, in
   a.vmin = L.vmin; a.vmax = L.vmax; a.kscale_max = L.kscale_max; a.vscale_max = L.vscale_max;
   a.tail_k_in = L.tail_k_in; a.tail_v_in = L.tail_v_in;
   a.tail_k_out = L.tail_k_out; a.tail_v_out = L.tail_v_out; a.nbmax = L.nbmax;
+  a.v16 = L.v16;
   const int last_blk = (pos + n - 1) / BLK;
   dim3 grid(last_blk - a.first_blk + 1, L.BG);
   const bool aligned = ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
@@ -303,6 +313,7 @@ cudaError_t launch_export_tier1(const LayerAppend& L, int nb, void* kc, void* ks
   a.okc = static_cast<int8_t*>(kc); a.oks = static_cast<__half*>(ks);
   a.ovc = static_cast<uint8_t*>(vc); a.ovs = static_cast<__half*>(vs);
   a.ovo = static_cast<__half*>(vo); a.oeta = eta; a.ovmin = vmin; a.ovmax = vmax;
+  if (L.v16) { a.ovc = nullptr; a.ovs = nullptr; a.ovo = nullptr; }   // no INT4 values exist
   a.nb = nb; a.nbmax = L.nbmax;
   dim3 grid(nb + 1, L.BG);
   export_tier1_kernel<<<grid, 128, 0, st>>>(a);

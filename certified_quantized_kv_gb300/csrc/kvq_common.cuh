@@ -88,7 +88,8 @@ struct LayerView {
   const __half* tail_v;
   // tier 2 of this layer (device addresses of mapped pinned host memory)
   const __half* t2k;     // [BG][cap][128]
-  const __half* t2v;
+  const __half* t2v;     // nullptr with FP16 values in tier 1
+  const __half* v16;     // [BG][nbmax][64][128] FP16 values in tier 1, or nullptr (INT4)
   // call inputs / outputs (device)
   const __half* q;       // [B][Hq][128]
   __half* out;           // [B][Hq][128]

@@ -120,7 +120,7 @@ __device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dens
       gs.need_round1 = 0; gs.n_kprom0 = 0; gs.n_kprom1 = 0; gs.n_vprom1 = 0; gs.bytes = 0;
     }
     gs.need_dense = 1;
-    gs.bytes += 2LL * V.nb * F16_BLOCK_BYTES;
+    gs.bytes += (V.v16 ? 1LL : 2LL) * V.nb * F16_BLOCK_BYTES;   // tier-2 keys (and values)
   }
 }
 
@@ -168,7 +168,8 @@ __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) 
       {
         // all sixteen 16-byte loads of a thread in flight before the first store
         const uint4* ks = reinterpret_cast<const uint4*>(V.t2k + src);
-        const uint4* vs = reinterpret_cast<const uint4*>(V.t2v + src);
+        const uint4* vs = reinterpret_cast<const uint4*>(
+            V.v16 ? V.v16 + ((size_t)hs * V.nbmax + blk) * (BLK * D) : V.t2v + src);   // FP16 values
         uint4 rk[8], rv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) { rk[j] = ks[tid + 128 * j]; rv[j] = vs[tid + 128 * j]; }

@@ -15,6 +15,7 @@ struct LayerAppend {
   int BG, nbmax;
   int8_t* kc; __half* ks; uint8_t* vc; __half2* vsv; float* eta;
   uint32_t* vmin; uint32_t* vmax; uint32_t* kscale_max; uint32_t* vscale_max;
+  __half* v16;   // FP16 values of full blocks (value_bits 16), or nullptr
   const __half* tail_k_in; const __half* tail_v_in;
   __half* tail_k_out; __half* tail_v_out;
 };

@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
   int par = 0;
   int cur_hs = -1;
   float pre_v = 1.f;
+  const bool v16 = V.v16 != nullptr;   // FP16 values in tier 1 (no INT4 codes)
   if (round == 1 && V.counters[CNT_NEED_R1] == 0u) return;   // no head planned rung 1 or 2
 
   for (;;) {
@@ -140,6 +141,8 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
         vp = V.vprom1[bi] != 0;
         if (!newk && !vp) continue;   // precision unchanged: contribution unchanged
       }
+      // FP16 values: paged in for this block (rung 2), or resident in tier 1
+      const bool use16 = vp || v16;
       par ^= 1;
       const int r = warp;
       const bool act = r < V.n_rep;
@@ -206,6 +209,10 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
           pi0 = vp ? -po0 : pn0 - po0;
           pi1 = vp ? -po1 : pn1 - po1;
           lsum += (pn0 - po0) + (pn1 - po1);
+          if (v16) {   // resident FP16 values: only the change of weight is added
+            pn0 -= po0;
+            pn1 -= po1;
+          }
         }
       }
       sm.p[par][r][lane] = pi0;
@@ -214,7 +221,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
       sm.pn[par][r][lane + 32] = pn1;
       __syncthreads();
       // ---- stage 2: weights x V for the warp's value group ----
-      {
+      if (!v16) {
         const uint4* vcp = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES) + (warp * 2) * 32 + lane;
         const uint4 C0 = __ldcs(vcp), C1 = __ldcs(vcp + 32);
         const uint4* svp = reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS + warp * BLK + 16 * tig);
@@ -250,8 +257,9 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
           }
         }
       }
-      if (vp) {
-        load_f16_block<D>(&sm.st.vbuf[0][0], V.t2v + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
+      if (use16) {
+        load_f16_block<D>(&sm.st.vbuf[0][0], v16 ? V.v16 + bi * (BLK * D)
+                                                 : V.t2v + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
         __syncthreads();
         const int c0 = 32 * warp + gid;
         const float* pr = sm.pn[par][tig];

@@ -67,6 +67,12 @@ typedef struct kvq_config {
   int rank_positions;      /* ranking check compares the top-R blocks (R >= 1; default 1) */
   float l4_head_fraction;  /* rung 4 when >= this fraction of a sequence's heads are at
                               rung 3 (in (0, 1]; default 0.5) */
+  int value_bits;          /* 4 (or 0): INT4 values in VRAM, FP16 values in tier 2 (the
+                              paper's configuration).  16: the paper's FP16-values ablation
+                              (Results, structured reasoning): values stay FP16 in VRAM,
+                              tier 2 holds keys only, E_val = 0 and rung 2 pages nothing
+                              in; VRAM per token and KV head 388 B instead of 212 B (dense
+                              FP16: 512 B) */
 } kvq_config;
 
 /* Per-head certificate of one decode call (Method §2, §3). */

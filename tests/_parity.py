@@ -30,12 +30,12 @@ BOUND_ATOL = 1e-6
 
 
 def gpu_run(q, K, V, tau, eps, chunks=None, debug=0, rank_positions=1, l4=0.5, max_ctx=None,
-            host_io=False, repeat=1):
+            host_io=False, repeat=1, value_bits=4):
     """Append K, V (CPU fp16 tensors [B, Hkv, N, D]) in `chunks` and decode once."""
     B, Hq, D = q.shape
     Hkv, N = K.shape[1], K.shape[2]
     cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=max_ctx or max(N, 1), rank_positions=rank_positions,
-                      l4_head_fraction=l4)
+                      l4_head_fraction=l4, value_bits=value_bits)
     try:
         cache.set_debug(debug)
         Kd, Vd = K.cuda(), V.cuda()
@@ -72,17 +72,21 @@ def gpu_run(q, K, V, tau, eps, chunks=None, debug=0, rank_positions=1, l4=0.5, m
     return dict(out=out, cert=cert, level=lvl, t1=t1, state=st, nb=nb, runs=outs)
 
 
-def oracle_run(q, K, V, tau, eps, rank_positions=1, l4=0.5):
+def oracle_run(q, K, V, tau, eps, rank_positions=1, l4=0.5, value_bits=4):
     qn, Kn, Vn = q.numpy(), K.numpy(), V.numpy()
     t1 = O.quantize_layer(Kn, Vn)
     cfg = O.OracleConfig(n_rep=q.shape[1] // K.shape[1], rank_positions=rank_positions,
-                         l4_head_fraction=l4)
+                         l4_head_fraction=l4, value_fp16=value_bits == 16)
     return t1, O.decode_layer(qn, Kn, Vn, t1, tau, eps, cfg)
 
 
-def compare_tier1(g, t1):
+def compare_tier1(g, t1, value_bits=4):
     assert np.array_equal(g["kc"].numpy(), t1.kc), "INT8 key codes differ"
     assert np.array_equal(g["ks"].numpy().view(np.uint16), t1.ks.view(np.uint16)), "key scales differ"
+    if value_bits == 16:   # FP16 values: no INT4 codes exist, eta is zero
+        assert np.all(g["eta"].numpy() == 0.0), "eta must be zero with FP16 values"
+        assert np.array_equal(g["vmin"].numpy(), t1.vmin) and np.array_equal(g["vmax"].numpy(), t1.vmax)
+        return
     assert np.array_equal(g["vc"].numpy(), t1.vc), "INT4 value codes differ"
     assert np.array_equal(g["vs"].numpy().view(np.uint16), t1.vs.view(np.uint16)), "value scales differ"
     assert np.array_equal(g["vo"].numpy().view(np.uint16), t1.vo.view(np.uint16)), "value offsets differ"
