@@ -21,10 +21,10 @@ import workloads as W  # noqa: E402
 from _parity import compare_decode  # noqa: E402
 
 
-def _run_full(q, K, V, tau, eps):
+def _run_full(q, K, V, tau, eps, value_bits=4):
     B, Hq, D = q.shape
     Hkv, N = K.shape[1], K.shape[2]
-    cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=N)
+    cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=N, value_bits=value_bits)
     try:
         cache.append(0, K.contiguous(), V.contiguous())
         out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
@@ -39,8 +39,8 @@ def _run_full(q, K, V, tau, eps):
     return out.cpu(), kvq.certificates(cert).reshape(B, Hq), lvl.cpu().numpy(), t1, st
 
 
-def _check_groups(q, K, V, tau, eps, groups):
-    out, cert, lvl, t1g, st = _run_full(q, K, V, tau, eps)
+def _check_groups(q, K, V, tau, eps, groups, value_bits=4):
+    out, cert, lvl, t1g, st = _run_full(q, K, V, tau, eps, value_bits)
     assert np.all(lvl < 4), "rung 4 fired; sampled comparison does not apply"
     n_rep = q.shape[1] // K.shape[1]
     qc, Kc, Vc = q.cpu(), K.cpu(), V.cpu()
@@ -49,11 +49,14 @@ def _check_groups(q, K, V, tau, eps, groups):
         qs = qc[b:b + 1, hs].numpy()
         Ks, Vs = Kc[b:b + 1, g:g + 1].numpy(), Vc[b:b + 1, g:g + 1].numpy()
         t1 = O.quantize_layer(Ks, Vs)
-        for name in ("kc", "vc", "eta"):
+        v4 = value_bits != 16
+        for name in ("kc", "vc", "eta") if v4 else ("kc",):
             assert np.array_equal(t1g[name][b, g].numpy(), getattr(t1, name)[0, 0]), name
-        for name in ("ks", "vs", "vo"):
+        for name in ("ks", "vs", "vo") if v4 else ("ks",):
             assert np.array_equal(t1g[name][b, g].numpy().view(np.uint16), getattr(t1, name)[0, 0].view(np.uint16)), name
-        r = O.decode_layer(qs, Ks, Vs, t1, tau, eps, O.OracleConfig(n_rep=n_rep))
+        if not v4:
+            assert np.all(t1g["eta"][b, g].numpy() == 0.0)
+        r = O.decode_layer(qs, Ks, Vs, t1, tau, eps, O.OracleConfig(n_rep=n_rep, value_fp16=not v4))
         g_res = dict(out=out[b:b + 1, hs], cert=cert[b:b + 1, hs],
                      level=np.array([cert['level'][b, hs].max()]),   # rung over the sampled heads
                      nb=Ks.shape[2] // 64,
@@ -71,3 +74,37 @@ def test_c3_layer_128k_sampled_groups():
 def test_c2_lowrank_32k_b4_sampled_groups():
     q, K, V = W.c2(device="cuda")
     _check_groups(q, K, V, 0.995, 0.25, [(0, 3), (3, 7)])
+
+
+def test_c3_layer_128k_fp16_values_sampled_groups():
+    q, K, V = W.c3_layer(0, device="cuda")
+    _check_groups(q, K, V, 0.995, 0.25, [(0, 2), (0, 6)], value_bits=16)
+
+
+def test_c3_layer_128k_uncertified_sampled_groups():
+    from _parity import BOUND_ATOL, BOUND_RTOL, OUT_ATOL, OUT_RTOL
+    q, K, V = W.c3_layer(0, device="cuda")
+    B, Hq, D = q.shape
+    Hkv, N = K.shape[1], K.shape[2]
+    cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=N)
+    try:
+        cache.append(0, K.contiguous(), V.contiguous())
+        out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+        cert = torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda")
+        cache.decode_uncertified(0, q.contiguous(), out, cert)
+        torch.cuda.synchronize()
+        c = kvq.certificates(cert).reshape(B, Hq)
+    finally:
+        cache.close()
+    n_rep = Hq // Hkv
+    qc, Kc, Vc = q.cpu(), K.cpu(), V.cpu()
+    for g in (1, 4):
+        hs = slice(g * n_rep, (g + 1) * n_rep)
+        Ks, Vs = Kc[0:1, g:g + 1].numpy(), Vc[0:1, g:g + 1].numpy()
+        u = O.uncertified_decode_layer(qc[0:1, hs].numpy(), Ks, Vs, O.quantize_layer(Ks, Vs))
+        err = np.abs(out[0, hs].cpu().float().numpy() - u.out64[0])
+        assert np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(u.out64[0]))
+        for name in ("e_key", "e_val"):
+            gv, ov = c[name][0, hs].astype(np.float64), getattr(u, name)[0]
+            assert np.all(np.abs(gv - ov) <= BOUND_RTOL * np.abs(ov) + BOUND_ATOL), name
+
