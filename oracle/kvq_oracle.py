@@ -55,6 +55,11 @@ class OracleConfig:
     # block counts as value-promoted from the start, E_val = 0, rung 2 has nothing to
     # page in and tier 2 holds (and pages in) keys only.
     value_fp16: bool = False
+    # Value tolerance v_tol (Results: tightening it closes the value-sensitive gap).  Our
+    # reading: a budget on E_val alone, on top of E_key + E_val <= eps; a head is
+    # certified only if both hold, and rung 2 pages in values until the projected E_val
+    # is within min(v_tol, eps - E_key).  Infinite by default (no separate budget).
+    v_tol: float = math.inf
 
 
 # --------------------------------------------------------------------------------------
@@ -332,19 +337,19 @@ def ranking_consistent(sel: list, lse8: np.ndarray, lse16: np.ndarray, positions
 
 
 def plan_ladder(res: MixedResult, kprom: np.ndarray, vprom: np.ndarray, delta: np.ndarray,
-                eta: np.ndarray, R: float, eps: float):
+                eta: np.ndarray, R: float, eps: float, v_tol: float = math.inf):
     """Rungs 1 and 2 of the fallback ladder for one head (Method §3).
 
     Reading A8.  Certified at level 0 when E_key + E_val <= eps.  Otherwise:
       rung 1 (expand coverage) when E_key > eps/2: add INT8 blocks in descending
         contribution mass_b (e^Delta_b - 1) (ties: lower index; zero contributions
         never) until the projected (S - sum added)/A * R <= eps/2;
-      rung 2 (value promotion) when projected E_key + E_val > eps: page in FP16 values
-        of blocks in descending mass_b * eta_b (same tie rule) until the projected
-        E_key + E_val <= eps.
+      rung 2 (value promotion) when projected E_key + E_val > eps, or E_val > v_tol:
+        page in FP16 values of blocks in descending mass_b * eta_b (same tie rule) until
+        the projected E_val <= min(v_tol, eps - projected E_key).
     Returns (level, blocks to add to the key set, blocks to add to the value set).
     """
-    if res.e_key + res.e_val <= eps:
+    if res.e_key + res.e_val <= eps and res.e_val <= v_tol:
         return 0, [], []
     level = 0
     add_k: list = []
@@ -361,14 +366,14 @@ def plan_ladder(res: MixedResult, kprom: np.ndarray, vprom: np.ndarray, delta: n
             S_proj -= contrib[b]
     ekey_proj = S_proj / res.A * R
     add_v: list = []
-    if ekey_proj + res.e_val > eps:
+    if ekey_proj + res.e_val > eps or res.e_val > v_tol:
         level = 2
         contrib_v = res.pmass * eta.astype(np.float64)
         cand = [b for b in range(len(contrib_v)) if not vprom[b] and contrib_v[b] > 0]
         cand.sort(key=lambda b: (-contrib_v[b], b))
         ev_proj = res.e_val
         for b in cand:
-            if ekey_proj + ev_proj <= eps:
+            if ekey_proj + ev_proj <= eps and ev_proj <= v_tol:
                 break
             add_v.append(b)
             ev_proj -= contrib_v[b]
@@ -497,7 +502,7 @@ def decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Tier1,
                     if not ok:
                         level[b, h] = planned[b, h] = 3
                         continue
-                    lv, ak, av = plan_ladder(r0, U, Vp, P["delta"], eta, R, eps)
+                    lv, ak, av = plan_ladder(r0, U, Vp, P["delta"], eta, R, eps, cfg.v_tol)
                     level[b, h] = planned[b, h] = lv
                     if lv > 0:
                         asking.append(h); adds_k += ak; adds_v += av
@@ -517,7 +522,7 @@ def decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Tier1,
                         e_key[b, h] = r1.e_key
                         e_val[b, h] = r1.e_val
                         n_vprom[b, h] = int(V1.sum()) - int(Vp.sum())   # paged in
-                        if r1.e_key + r1.e_val > eps:
+                        if r1.e_key + r1.e_val > eps or r1.e_val > cfg.v_tol:
                             level[b, h] = 3
                 kprom1[b, g] = U1; vprom1[b, g] = V1
 

@@ -647,3 +647,31 @@ def test_fp16_values_bound_sound_and_no_value_pages():
             want = (k_blocks + (nb if dense else 0)) * 64 * 128 * 2
             assert int(r.promoted_bytes[0, 4 * g]) == want
 
+
+# ---------------------------------------------------------------------------------
+# value tolerance v_tol (Results: tightening it closes the value-sensitive gap)
+# ---------------------------------------------------------------------------------
+
+def test_v_tol_budget_holds_and_tightening_pages_in_more_values():
+    q, K, V = W.c5_point(64 * 40 + 7, 1, Hq=8, Hkv=2)
+    q, K, V = q.numpy(), K.numpy(), V.numpy()
+    t1 = O.quantize_layer(K, V)
+    prev_v, prev_bytes = -1, -1
+    for v_tol in (math.inf, 0.2, 0.1, 0.05, 0.02):
+        cfg = O.OracleConfig(n_rep=4, v_tol=v_tol)
+        r = O.decode_layer(q, K, V, t1, 0.99, 0.5, cfg)
+        ok = r.level < 3
+        assert np.all(r.e_val[ok] <= v_tol) and np.all(r.e_key[ok] + r.e_val[ok] <= 0.5)
+        nv = int(r.vprom1.sum())
+        assert nv >= prev_v                         # a tighter budget never pages in less
+        assert int(r.promoted_bytes.sum()) >= prev_bytes
+        prev_v, prev_bytes = nv, int(r.promoted_bytes.sum())
+        for h in np.nonzero(ok[0])[0]:
+            ref = O.dense_attention(q[0, h], K[0, h // 4], V[0, h // 4])
+            assert np.max(np.abs(r.out64[0, h] - ref)) <= r.e_key[0, h] + r.e_val[0, h] + 1e-9
+    assert prev_v > 0
+    # an infinite v_tol is the plain eps rule
+    a = O.decode_layer(q, K, V, t1, 0.99, 0.5, O.OracleConfig(n_rep=4))
+    b = O.decode_layer(q, K, V, t1, 0.99, 0.5, O.OracleConfig(n_rep=4, v_tol=math.inf))
+    assert np.array_equal(a.level, b.level) and np.array_equal(a.out64, b.out64)
+
