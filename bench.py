@@ -587,6 +587,50 @@ def sweep_c5(args):
             torch.cuda.empty_cache()
 
 
+VTOL_SWEEP = (0.0, 0.2, 0.1, 0.05, 0.02)
+
+
+def sweep_vtol(args):
+    """Value-tolerance sweep on one layer of the headline workload: for each v_tol (0 = no
+    budget beyond eps) the time per decode call, the ladder histogram, the paged-in bytes
+    and the largest certified E_val."""
+    import torch
+    import certified_quantized_kv_gb300 as kvq
+    import workloads as W
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    wl = WORKLOAD
+    B, N = args.batch or wl["batch"], args.ctx or wl["ctx"]
+    Hq, Hkv, D, tau, eps = wl["q_heads"], wl["kv_heads"], wl["head_dim"], wl["tau_cov"], wl["eps"]
+    q, K, V = W.c3_layer(0, device="cuda", seed=wl["seed"], batch=B, ctx=N, Hq=Hq, Hkv=Hkv)
+    for v_tol in VTOL_SWEEP:
+        cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=N, v_tol=v_tol)
+        cache.append(0, K, V)
+        out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+        cert = torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda")
+        for _ in range(max(1, args.warmup)):
+            cache.decode(0, q, tau, eps, out, cert)
+        times = []
+        for _ in range(max(1, args.steps)):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            cache.decode(0, q, tau, eps, out, cert)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = sorted(times)[len(times) // 2]
+        c = kvq.certificates(cert).reshape(B, Hq)
+        ok = c["level"] < 3
+        print(json.dumps({
+            "sweep": "vtol", "v_tol": v_tol, "ctx": N, "batch": B, "tau_cov": tau, "eps": eps,
+            "ms_per_call": ms, "tokens_per_s_per_layer": B / (ms / 1e3),
+            "ladder_histogram": [int(x) for x in np.bincount(c["level"].ravel(), minlength=5)],
+            "promoted_bytes": int(c["promoted_bytes"][:, :: Hq // Hkv].sum()),
+            "max_certified_e_val": float(c["e_val"][ok].max()) if ok.any() else None,
+            "mean_certified_e_val": float(c["e_val"][ok].mean()) if ok.any() else None}), flush=True)
+        cache.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -597,11 +641,14 @@ def main():
     ap.add_argument("--ctx", type=int, default=None, help="override the context (not the headline)")
     ap.add_argument("--batch", type=int, default=None, help="override the batch (not the headline)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
-    ap.add_argument("--sweep", choices=["c5"], default=None,
-                    help="run the ladder sweep instead of the headline (one JSON line per point)")
+    ap.add_argument("--sweep", choices=["c5", "vtol"], default=None,
+                    help="run a sweep instead of the headline (one JSON line per point)")
     args = ap.parse_args()
     if args.sweep == "c5":
         sweep_c5(args)
+        return
+    if args.sweep == "vtol":
+        sweep_vtol(args)
         return
     wl = dict(WORKLOAD)
     for k in ("layers", "ctx", "batch"):

@@ -46,6 +46,7 @@ class kvq_config(ctypes.Structure):
         ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("block_tokens", ctypes.c_int),
         ("value_group", ctypes.c_int), ("max_ctx", ctypes.c_int), ("rank_positions", ctypes.c_int),
         ("l4_head_fraction", ctypes.c_float), ("value_bits", ctypes.c_int),
+        ("v_tol", ctypes.c_float),
     ]
 
 
@@ -121,10 +122,11 @@ class Cache:
 
     def __init__(self, n_layers, batch, n_q_heads, n_kv_heads, max_ctx, rank_positions=1,
                  l4_head_fraction=0.5, head_dim=HEAD_DIM, block_tokens=BLOCK,
-                 value_group=VALUE_GROUP, value_bits=4):
+                 value_group=VALUE_GROUP, value_bits=4, v_tol=0.0):
         self.lib = load_library()
         self.cfg = kvq_config(n_layers, batch, n_q_heads, n_kv_heads, head_dim, block_tokens,
-                              value_group, max_ctx, rank_positions, l4_head_fraction, value_bits)
+                              value_group, max_ctx, rank_positions, l4_head_fraction, value_bits,
+                              v_tol)
         self.value_bits = value_bits
         h = ctypes.c_void_p()
         _check(self.lib.kvq_cache_create(ctypes.byref(self.cfg), ctypes.byref(h)))

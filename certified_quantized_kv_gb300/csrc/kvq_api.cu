@@ -232,6 +232,7 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
     return fail(KVQ_ERR_INVALID, "l4_head_fraction must be in (0, 1]");
   if (k.value_bits != 0 && k.value_bits != 4 && k.value_bits != 16)
     return fail(KVQ_ERR_INVALID, "value_bits must be 4 (or 0) or 16");
+  if (!(k.v_tol >= 0.f)) return fail(KVQ_ERR_INVALID, "v_tol must be >= 0 (0: no value budget)");
 
   kvq_cache* c = new kvq_cache();
   c->cfg = k;
@@ -471,6 +472,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   V.t2k = c->t2k_dev[layer]; V.t2v = c->t2v_dev[layer]; V.v16 = layer_v16(c, layer);
   V.q = qd; V.out = od; V.tau = tau; V.eps = eps;
   V.l4_frac = c->cfg.l4_head_fraction; V.rank_positions = c->cfg.rank_positions;
+  V.v_tol = (certified && c->cfg.v_tol > 0.f) ? c->cfg.v_tol : INFINITY;
   V.debug = certified ? c->debug : (c->debug & ~(KVQ_DEBUG_FORCE_RANK_FAIL | KVQ_DEBUG_FORCE_DENSE));
   V.shat = c->shat; V.lse8 = c->lse8; V.delta = c->delta; V.lse16 = c->lse16; V.sel = c->sel;
   V.kprom0 = c->kprom0; V.kprom1 = c->kprom1; V.vprom1 = c->vprom1;

@@ -95,6 +95,7 @@ struct LayerView {
   __half* out;           // [B][Hq][128]
   float tau, eps;
   float l4_frac;
+  float v_tol;           // budget on E_val alone (+inf: none)
   int rank_positions;
   int debug;
   // scratch

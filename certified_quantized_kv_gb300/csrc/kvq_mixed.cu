@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   hsd.e_key = e_key;
   hsd.e_val = e_val;
   if (round == 1) {
-    hsd.level1 = (e_key + e_val <= V.eps) ? hsd.planned : 3;
+    hsd.level1 = (e_key + e_val <= V.eps && e_val <= V.v_tol) ? hsd.planned : 3;
     if (tid == 0) {
       V.hst[hb] = hsd;
       if (hsd.level1 == 3) V.counters[CNT_ANY_DENSE] = 1u;
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   int planned = 0;
   if (!ok) {
     planned = 3;
-  } else if (!(e_key + e_val <= V.eps)) {
+  } else if (!(e_key + e_val <= V.eps && e_val <= V.v_tol)) {
     const float eps = V.eps;
     float S_proj = S;
     uint8_t* k1 = V.kprom1 + (size_t)hs * V.nbmax;
@@ -527,12 +527,14 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
       __syncthreads();
     }
     const float ekey_proj = S_proj / A * R;
-    if (!(ekey_proj + e_val <= eps)) {
+    if (!(ekey_proj + e_val <= eps && e_val <= V.v_tol)) {
       planned = 2;
       if (e_val > 0.f) {
         // rung 2: FP16 values by descending mass_b eta_b until the projected
-        // E_key + E_val <= eps (every block is a candidate: no values are FP16 yet)
-        const double need = 1.0 - ((double)eps - (double)ekey_proj) / (double)e_val;
+        // E_key + E_val <= eps and E_val <= v_tol (every block is a candidate: no values
+        // are FP16 yet)
+        const double target = fmin((double)eps - (double)ekey_proj, (double)V.v_tol);
+        const double need = 1.0 - target / (double)e_val;
         for (int i = tid; i < nb; i += BS_THREADS)
           keys[i] = __float_as_uint(expf((kfl[i] ? lse16[i] : lse8[i]) - LSEp) * eta[i] / e_val);
         __syncthreads();

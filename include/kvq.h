@@ -73,6 +73,10 @@ typedef struct kvq_config {
                               tier 2 holds keys only, E_val = 0 and rung 2 pages nothing
                               in; VRAM per token and KV head 388 B instead of 212 B (dense
                               FP16: 512 B) */
+  float v_tol;             /* value tolerance: a head is certified only if also E_val <=
+                              v_tol, and rung 2 pages in values until it holds (the paper's
+                              v_tol, Results: structured reasoning).  0 (or +inf): no budget
+                              beyond eps.  Must not be negative or NaN. */
 } kvq_config;
 
 /* Per-head certificate of one decode call (Method §2, §3). */

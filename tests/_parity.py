@@ -30,12 +30,12 @@ BOUND_ATOL = 1e-6
 
 
 def gpu_run(q, K, V, tau, eps, chunks=None, debug=0, rank_positions=1, l4=0.5, max_ctx=None,
-            host_io=False, repeat=1, value_bits=4):
+            host_io=False, repeat=1, value_bits=4, v_tol=0.0):
     """Append K, V (CPU fp16 tensors [B, Hkv, N, D]) in `chunks` and decode once."""
     B, Hq, D = q.shape
     Hkv, N = K.shape[1], K.shape[2]
     cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=max_ctx or max(N, 1), rank_positions=rank_positions,
-                      l4_head_fraction=l4, value_bits=value_bits)
+                      l4_head_fraction=l4, value_bits=value_bits, v_tol=v_tol)
     try:
         cache.set_debug(debug)
         Kd, Vd = K.cuda(), V.cuda()
@@ -72,11 +72,12 @@ def gpu_run(q, K, V, tau, eps, chunks=None, debug=0, rank_positions=1, l4=0.5, m
     return dict(out=out, cert=cert, level=lvl, t1=t1, state=st, nb=nb, runs=outs)
 
 
-def oracle_run(q, K, V, tau, eps, rank_positions=1, l4=0.5, value_bits=4):
+def oracle_run(q, K, V, tau, eps, rank_positions=1, l4=0.5, value_bits=4, v_tol=0.0):
     qn, Kn, Vn = q.numpy(), K.numpy(), V.numpy()
     t1 = O.quantize_layer(Kn, Vn)
     cfg = O.OracleConfig(n_rep=q.shape[1] // K.shape[1], rank_positions=rank_positions,
-                         l4_head_fraction=l4, value_fp16=value_bits == 16)
+                         l4_head_fraction=l4, value_fp16=value_bits == 16,
+                         v_tol=v_tol if v_tol > 0 else math.inf)
     return t1, O.decode_layer(qn, Kn, Vn, t1, tau, eps, cfg)
 
 

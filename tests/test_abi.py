@@ -38,6 +38,9 @@ def test_null_and_invalid_arguments_without_gpu():
     cfg = kvq.kvq_config(1, 1, 32, 8, 128, 64, 32, 1024, 1, 0.5, 8)   # value_bits 8
     assert lib.kvq_cache_create(ctypes.byref(cfg), ctypes.byref(h)) == kvq.KVQ_ERR_INVALID
     assert b"value_bits" in lib.kvq_last_error()
+    cfg = kvq.kvq_config(1, 1, 32, 8, 128, 64, 32, 1024, 1, 0.5, 4, -1.0)   # v_tol < 0
+    assert lib.kvq_cache_create(ctypes.byref(cfg), ctypes.byref(h)) == kvq.KVQ_ERR_INVALID
+    assert b"v_tol" in lib.kvq_last_error()
     assert lib.kvq_cache_destroy(None) == kvq.KVQ_OK
     assert lib.kvq_append(None, 0, None, None, 1, None) == kvq.KVQ_ERR_INVALID
     assert lib.kvq_decode_attention(None, 0, None, 0.9, 0.25, None, None, None, None) == kvq.KVQ_ERR_INVALID

@@ -24,7 +24,7 @@ from _parity import (compare_decode, compare_tier1, gpu_run, oracle_run)  # noqa
 def _check(q, K, V, tau, eps, chunks=None, **kw):
     g = gpu_run(q, K, V, tau, eps, chunks=chunks, **kw)
     t1, r = oracle_run(q, K, V, tau, eps, rank_positions=kw.get("rank_positions", 1),
-                       l4=kw.get("l4", 0.5))
+                       l4=kw.get("l4", 0.5), v_tol=kw.get("v_tol", 0.0))
     compare_tier1(g["t1"], t1)
     st = compare_decode(g, t1, r, tau, eps, q.shape[1] // K.shape[1])
     return g, r, st
@@ -183,3 +183,18 @@ def test_errors():
     with pytest.raises(kvq.KvqError) as e:
         kvq.Cache(1, 1, 6, 1, max_ctx=128)           # n_rep = 6 unsupported
     assert e.value.status == kvq.KVQ_ERR_INVALID
+
+
+# ---------------------------------------------------------------------------------
+# value tolerance v_tol (Results: structured reasoning)
+# ---------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("v_tol", [0.1, 0.03])
+def test_value_tolerance(v_tol):
+    q, K, V = W.c5_point(64 * 120 + 9, 2, Hq=8, Hkv=2)
+    g, r, st = _check(q, K, V, 0.99, 0.5, v_tol=v_tol)
+    c = g["cert"]
+    ok = c["level"] < 3
+    assert np.all(c["e_val"][ok] <= v_tol * (1 + 1e-4))
+    assert np.any(c["level"] == 2)
+
