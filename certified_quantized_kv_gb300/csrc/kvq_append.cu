@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
           const float r = rintf(__fdiv_rn(fv[e], sv4[e]));
           code = (int)fminf(fmaxf(r, -127.f), 127.f);
         }
-        packed |= ((uint32_t)(code & 0xff)) << (8 * e);
+        packed |= ((uint32_t)(code + 128)) << (8 * e);   // offset binary: code + 128
       }
       word[u] = packed;
     }
@@ -264,7 +264,8 @@ __global__ void __launch_bounds__(128) export_tier1_kernel(ExportArgs a) {
   const size_t src = (size_t)hs * a.nbmax + blk;
   const size_t dst = (size_t)hs * a.nb + blk;
   for (int t = 0; t < BLK; ++t) {
-    if (a.okc) a.okc[(dst * BLK + t) * D + c] = a.kc[src * KC_BYTES + kc_offset(t, c)];
+    if (a.okc)   // stored offset binary (code + 128)
+      a.okc[(dst * BLK + t) * D + c] = (int8_t)((int)(uint8_t)a.kc[src * KC_BYTES + kc_offset(t, c)] - 128);
     if (a.ovc) {
       int wb, bit;
       vc_offset(t, c, wb, bit);

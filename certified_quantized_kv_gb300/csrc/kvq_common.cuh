@@ -6,7 +6,7 @@
 // register fragment of an mma.sync.m16n8k16 tile (no shared-memory staging, no bank
 // conflicts):
 //
-//  K codes (INT8), per 64-token block, 8192 bytes:
+//  K codes (INT8, stored offset binary: byte = code + 128), per 64-token block, 8192 bytes:
 //    offset((w*4 + j)*32 + lane)*16 + byte, w = token>>4 (MMA row tile), lane = gid*4+tig
 //    row  = 16w + gid + 8*(j>>1),   channel = 32*tig + 16*(j&1) + byte.
 //    In k-step kk (0..7) the MMA column 2tig(+1) is channel 32tig+4kk(+1) and column
@@ -151,13 +151,12 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// Four signed INT8 codes (one 32-bit word) -> two f16x2 registers, exactly.
-// Bias each byte to unsigned (b + 128), place it under the exponent pattern 0x64 so the
-// half reads 1024 + (b + 128), then subtract 1152.  Every step is exact in binary16.
+// Four INT8 codes stored offset binary (byte = code + 128; one 32-bit word) -> two
+// f16x2 registers, exactly: placed under the exponent pattern 0x64 a byte reads as the
+// half 1024 + byte, and subtracting 1152 leaves the code.  Every step is exact in binary16.
 __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t x = w ^ 0x80808080u;
-  const uint32_t l = __byte_perm(x, 0x64646464u, 0x4140);
-  const uint32_t h = __byte_perm(x, 0x64646464u, 0x4342);
+  const uint32_t l = __byte_perm(w, 0x64646464u, 0x4140);
+  const uint32_t h = __byte_perm(w, 0x64646464u, 0x4342);
   const __half2 bias = u32_as_h2(0x64806480u);  // (1152, 1152)
   lo = h2_as_u32(__hsub2(u32_as_h2(l), bias));
   hi = h2_as_u32(__hsub2(u32_as_h2(h), bias));
@@ -174,6 +173,29 @@ __device__ __forceinline__ uint32_t nib_to_f16(uint32_t w, int i) {
 __device__ __forceinline__ void split_hl(float x, __half& hi, __half& lo) {
   hi = __float2half_rn(x);
   lo = __float2half_rn(x - __half2float(hi));
+}
+
+// Packed fp32 pairs (two lanes of one 64-bit register pair per instruction).
+__device__ __forceinline__ unsigned long long f2_bits(float2 v) {
+  return ((unsigned long long)__float_as_uint(v.y) << 32) | __float_as_uint(v.x);
+}
+__device__ __forceinline__ float2 bits_f2(unsigned long long u) {
+  return make_float2(__uint_as_float((uint32_t)u), __uint_as_float((uint32_t)(u >> 32)));
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
 }
 
 // Programmatic dependent launch: a kernel launched with programmatic stream

@@ -115,11 +115,11 @@ __global__ void __launch_bounds__(128, 4) score_kernel(LayerView V) {
         const uint32_t sw = (i & 3) == 0 ? Sv[i >> 2].x : (i & 3) == 1 ? Sv[i >> 2].y : (i & 3) == 2 ? Sv[i >> 2].z : Sv[i >> 2].w;
         const float2 s2 = __half22float2(u32_as_h2(sw));
         const float2 q2 = __half22float2(qh2[i]);
-        const float w0 = q2.x * pre * s2.x, w1 = q2.y * pre * s2.y;   // exact products
-        dp += fabsf(w0) + fabsf(w1);
-        const __half2 hi = __floats2half2_rn(w0, w1);
-        const float2 hf = __half22float2(hi);
-        const __half2 lo = __floats2half2_rn(w0 - hf.x, w1 - hf.y);   // exact remainders
+        const float2 w = mul2(mul2(q2, make_float2(pre, pre)), s2);   // exact products
+        dp += fabsf(w.x) + fabsf(w.y);
+        const __half2 hi = __floats2half2_rn(w.x, w.y);
+        const float2 r = sub2(w, __half22float2(hi));                 // exact remainders
+        const __half2 lo = __floats2half2_rn(r.x, r.y);
         bf[i] = (gid & 1) ? h2_as_u32(lo) : h2_as_u32(hi);
       }
     }
@@ -144,8 +144,11 @@ __global__ void __launch_bounds__(128, 4) score_kernel(LayerView V) {
         i8x4_to_f16(wb, a1, a3);
         mma16816(acc, a0, a1, a2, a3, bf[2 * kk], bf[2 * kk + 1]);
       }
-      x[2 * w] = (acc[0] + acc[1]) * sc_out;       // head tig, token 16w + gid
-      x[2 * w + 1] = (acc[2] + acc[3]) * sc_out;   // head tig, token 16w + gid + 8
+      // head tig, tokens 16w + gid and 16w + gid + 8
+      const float2 xs = mul2(add2(make_float2(acc[0], acc[2]), make_float2(acc[1], acc[3])),
+                             make_float2(sc_out, sc_out));
+      x[2 * w] = xs.x;
+      x[2 * w + 1] = xs.y;
     }
     if (tig < V.n_rep) {
       float* sh = V.shat + head_row(V, b, g, tig) * ((size_t)V.nbmax * BLK) + (size_t)blk * BLK + gid;
