@@ -8,6 +8,7 @@
 // certificate write-out -- five stream-ordered launches with no host round trip; every
 // data-dependent decision is taken on the device.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -154,18 +155,26 @@ cudaEvent_t pooled_event(kvq_cache* c) {
   return e;
 }
 
+// One launch of the pipeline: an NVTX range named after the kernel (visible to any
+// attached profiler; a no-op otherwise), CUDA events around it in profiling mode, and a
+// synchronising error check in debug-sync mode.
 struct KernelScope {
   kvq_cache* c;
   int id;
   cudaStream_t st;
   cudaEvent_t a = nullptr;
+  bool open = true;
   KernelScope(kvq_cache* c_, int id_, cudaStream_t st_) : c(c_), id(id_), st(st_) {
+    nvtxRangePushA(kKernelNames[id]);
     if (c->debug & KVQ_DEBUG_PROFILE) {
       a = pooled_event(c);
       cudaEventRecord(a, st);
     }
   }
+  ~KernelScope() { if (open) nvtxRangePop(); }
   cudaError_t done(cudaError_t e) {
+    nvtxRangePop();
+    open = false;
     if (e != cudaSuccess) return e;
     if (c->debug & KVQ_DEBUG_PROFILE) {
       cudaEvent_t b = pooled_event(c);
