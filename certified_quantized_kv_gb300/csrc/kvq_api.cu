@@ -155,6 +155,17 @@ cudaEvent_t pooled_event(kvq_cache* c) {
   return e;
 }
 
+// Makes the cache's device current for the duration of a call and restores the
+// caller's device afterwards (a process may drive caches on several GPUs).
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+    else prev = -1;
+  }
+  ~DeviceGuard() { if (prev >= 0) cudaSetDevice(prev); }
+};
+
 // One launch of the pipeline: an NVTX range named after the kernel (visible to any
 // attached profiler; a no-op otherwise), CUDA events around it in profiling mode, and a
 // synchronising error check in debug-sync mode.
@@ -376,6 +387,8 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
 }
 
 kvq_status kvq_cache_destroy(kvq_cache* cache) {
+  if (!cache) return KVQ_OK;
+  DeviceGuard dg(cache->device);
   free_all(cache);
   return KVQ_OK;
 }
@@ -396,6 +409,7 @@ kvq_status kvq_cache_length(const kvq_cache* c, int layer, int* n) {
 kvq_status kvq_append(kvq_cache* c, int layer, const void* k, const void* v, int n, void* stream) {
   if (!c) return fail(KVQ_ERR_INVALID, "kvq_append: NULL cache");
   if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, "kvq_append: layer out of range");
+  DeviceGuard dg(c->device);
   if (n < 0) return fail(KVQ_ERR_INVALID, "kvq_append: n_tokens < 0");
   if (n == 0) return KVQ_OK;
   if (!k || !v) return fail(KVQ_ERR_INVALID, "kvq_append: NULL k or v");
@@ -449,6 +463,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
                               void* stream, bool certified, const char* fn) {
   const std::string f(fn);
   if (!c) return fail(KVQ_ERR_INVALID, f + ": NULL cache");
+  DeviceGuard dg(c->device);
   if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, f + ": layer out of range");
   if (!q || !out) return fail(KVQ_ERR_INVALID, f + ": NULL q or out");
   const int N = c->n_tokens[layer];
@@ -519,6 +534,7 @@ extern "C" {
 kvq_status kvq_export_tier1(kvq_cache* c, int layer, void* kc, void* ks, void* vc, void* vs,
                             void* vo, float* eta, float* vmin, float* vmax, void* stream) {
   if (!c) return fail(KVQ_ERR_INVALID, "kvq_export_tier1: NULL cache");
+  DeviceGuard dg(c->device);
   if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, "kvq_export_tier1: layer out of range");
   const int nb = c->n_tokens[layer] / BLK;
   KVQ_CUDA(launch_export_tier1(append_view(c, layer), nb, kc, ks, vc, vs, vo, eta, vmin, vmax,
@@ -529,6 +545,7 @@ kvq_status kvq_export_tier1(kvq_cache* c, int layer, void* kc, void* ks, void* v
 kvq_status kvq_export_decode_state(kvq_cache* c, uint8_t* sel, uint8_t* kprom0, uint8_t* kprom1,
                                    uint8_t* vprom1, float* lse8, float* delta, void* stream) {
   if (!c) return fail(KVQ_ERR_INVALID, "kvq_export_decode_state: NULL cache");
+  DeviceGuard dg(c->device);
   if (c->last_layer < 0 || c->last_nb < 0)
     return fail(KVQ_ERR_INVALID, "kvq_export_decode_state: no certified decode call yet");
   const int nb = c->last_nb;
@@ -550,6 +567,7 @@ kvq_status kvq_export_decode_state(kvq_cache* c, uint8_t* sel, uint8_t* kprom0, 
 
 kvq_status kvq_profile_read(kvq_cache* c, kvq_kernel_stat* stats, int max, int* n, int reset) {
   if (!c || !n || (max > 0 && !stats)) return fail(KVQ_ERR_INVALID, "kvq_profile_read: NULL argument");
+  DeviceGuard dg(c->device);
   for (auto& r : c->recs) {
     KVQ_CUDA(cudaEventSynchronize(r.b), "kvq_profile_read: sync");
     float ms = 0.f;
