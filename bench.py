@@ -587,6 +587,56 @@ def sweep_c5(args):
             torch.cuda.empty_cache()
 
 
+def decode_loop(args):
+    """Token-by-token decode on the headline cache shape: every step appends one new
+    token's K/V to each layer (quantiser + tier-2 mirror) and then decodes that layer's
+    new query, as a serving loop does.  The cache is prefilled to ctx - warmup - steps
+    tokens and ends at ctx.  Prints one JSON line."""
+    import torch
+    import certified_quantized_kv_gb300 as kvq
+    import workloads as W
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    wl = dict(WORKLOAD)
+    B, L, N = args.batch or wl["batch"], args.layers or wl["layers"], args.ctx or wl["ctx"]
+    Hq, Hkv, D, tau, eps = wl["q_heads"], wl["kv_heads"], wl["head_dim"], wl["tau_cov"], wl["eps"]
+    T, Wm = args.steps, args.warmup
+    n0 = N - T - Wm
+    cache = kvq.Cache(L, B, Hq, Hkv, max_ctx=N)
+    for layer in range(L):
+        _, K, V = W.c3_layer(layer, device="cuda", seed=wl["seed"], batch=B, ctx=n0, Hq=Hq, Hkv=Hkv)
+        cache.append(layer, K.contiguous(), V.contiguous())
+        del K, V
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(wl["seed"] + 77)
+    steps = T + Wm
+    knew = torch.randn(steps, L, B, Hkv, 1, D, generator=gen, device="cuda").half()
+    vnew = torch.randn(steps, L, B, Hkv, 1, D, generator=gen, device="cuda").half()
+    qnew = torch.randn(steps, L, B, Hq, D, generator=gen, device="cuda").half()
+    out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+    cert = torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda")
+
+    def step(t):
+        for layer in range(L):
+            cache.append(layer, knew[t, layer], vnew[t, layer])
+            cache.decode(layer, qnew[t, layer], tau, eps, out, cert)
+
+    for t in range(Wm):
+        step(t)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for t in range(Wm, steps):
+        step(t)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / T
+    print(json.dumps({"mode": "decode_loop", "metric": "tokens/s/layer (append + certified decode per token)",
+                      "value": B / (ms / L / 1e3), "ms_per_step": ms, "steps": T, "warmup": Wm,
+                      "layers": L, "batch": B, "ctx_end": N, "tau_cov": tau, "eps": eps}), flush=True)
+    cache.close()
+
+
 VTOL_SWEEP = (0.0, 0.2, 0.1, 0.05, 0.02)
 
 
@@ -641,6 +691,8 @@ def main():
     ap.add_argument("--ctx", type=int, default=None, help="override the context (not the headline)")
     ap.add_argument("--batch", type=int, default=None, help="override the batch (not the headline)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--loop", action="store_true",
+                    help="token-by-token decode loop (append + decode per layer and step)")
     ap.add_argument("--sweep", choices=["c5", "vtol"], default=None,
                     help="run a sweep instead of the headline (one JSON line per point)")
     args = ap.parse_args()
@@ -649,6 +701,9 @@ def main():
         return
     if args.sweep == "vtol":
         sweep_vtol(args)
+        return
+    if args.loop:
+        decode_loop(args)
         return
     wl = dict(WORKLOAD)
     for k in ("layers", "ctx", "batch"):

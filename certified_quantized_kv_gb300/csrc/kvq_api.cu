@@ -419,11 +419,41 @@ kvq_status kvq_append(kvq_cache* c, int layer, const void* k, const void* v, int
   if ((long long)pos + n > c->cfg.max_ctx)
     return fail(KVQ_ERR_CAPACITY, "kvq_append: cache capacity (max_ctx) exceeded");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // tier-2 mirror on the side stream, overlapped with quantisation
-  KVQ_CUDA(cudaEventRecord(c->ev_in, st), "kvq_append: event");
-  KVQ_CUDA(cudaStreamWaitEvent(c->side, c->ev_in, 0), "kvq_append: wait");
   const size_t dpitch = (size_t)c->cap * D * sizeof(__half);
   const size_t width = (size_t)n * D * sizeof(__half);
+  if (pos % BLK + n < BLK) {
+    // Every new token stays in the FP16 partial block, which no decode reads from tier 2.
+    // The mirror then copies the tokens from the partial-block buffer the kernel writes
+    // (not from the caller's buffers) and is not joined: the call costs one launch.
+    // Earlier mirrors may still read the buffer this kernel overwrites (the ping-pong
+    // partner of the last append): they are waited for first.
+    KVQ_CUDA(cudaStreamWaitEvent(st, c->ev_mirror, 0), "kvq_append: wait mirror");
+    {
+      KernelScope ks(c, K_APPEND, st);
+      KVQ_CUDA(ks.done(launch_append(append_view(c, layer), k, v, n, pos, st)), "quantize_append");
+    }
+    KVQ_CUDA(cudaEventRecord(c->ev_in, st), "kvq_append: event");
+    KVQ_CUDA(cudaStreamWaitEvent(c->side, c->ev_in, 0), "kvq_append: wait");
+    const int p_out = 1 - c->tail_parity[layer];
+    const size_t spitch = (size_t)BLK * D * sizeof(__half);
+    const size_t row0 = (size_t)(pos % BLK) * D;
+    KVQ_CUDA(cudaMemcpy2DAsync(c->t2k_host[layer] + (size_t)pos * D, dpitch,
+                               layer_tail(c, layer, p_out, 0) + row0, spitch, width, c->BG,
+                               cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror K");
+    if (!c->v16)
+      KVQ_CUDA(cudaMemcpy2DAsync(c->t2v_host[layer] + (size_t)pos * D, dpitch,
+                                 layer_tail(c, layer, p_out, 1) + row0, spitch, width, c->BG,
+                                 cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror V");
+    KVQ_CUDA(cudaEventRecord(c->ev_mirror, c->side), "kvq_append: event");
+    c->n_tokens[layer] = pos + n;
+    c->tail_parity[layer] ^= 1;
+    return KVQ_OK;
+  }
+  // tier-2 mirror of the caller's tokens on the side stream, overlapped with
+  // quantisation and joined before the call returns (a completed block may be paged in
+  // by the next decode, and the caller may reuse k and v)
+  KVQ_CUDA(cudaEventRecord(c->ev_in, st), "kvq_append: event");
+  KVQ_CUDA(cudaStreamWaitEvent(c->side, c->ev_in, 0), "kvq_append: wait");
   KVQ_CUDA(cudaMemcpy2DAsync(c->t2k_host[layer] + (size_t)pos * D, dpitch, k, width, width, c->BG,
                              cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror K");
   if (!c->v16)

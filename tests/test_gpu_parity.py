@@ -198,3 +198,17 @@ def test_value_tolerance(v_tol):
     assert np.all(c["e_val"][ok] <= v_tol * (1 + 1e-4))
     assert np.any(c["level"] == 2)
 
+
+def test_token_by_token_appends_feed_tier2():
+    """One token per append (the serving loop): tokens that stay in the partial block are
+    mirrored to tier 2 from the partial-block buffer without a join; blocks they later
+    complete are paged in correctly (tau = 1 reads every full block from tier 2), and the
+    certified path matches the oracle."""
+    q, K, V = W.tiny(seed=70, ctx=64 * 3 + 29, Hq=8, Hkv=2, kscale=3.0)
+    N = K.shape[2]
+    g = gpu_run(q, K, V, 1.0, 0.25, chunks=[1] * N)
+    for h in range(8):
+        dense = O.dense_attention(q[0, h].numpy(), K[0, h // 4].numpy(), V[0, h // 4].numpy())
+        assert np.allclose(g["out"][0, h].float().numpy(), dense, atol=2e-3, rtol=1e-2)
+    _check(q, K, V, 0.9, 0.25, chunks=[1] * 100 + [5] * 20 + [N - 200])
+
