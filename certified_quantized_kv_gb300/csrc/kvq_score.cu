@@ -37,10 +37,33 @@ __device__ __forceinline__ size_t head_row(const LayerView& V, int b, int g, int
 
 // Warp-per-block scoring: every warp owns a contiguous range of the (KV group, block)
 // sequence and processes each block alone -- B fragments, 4 MMA row tiles, the block
-// log-mass by shuffles -- with no CTA barrier, so the SM keeps as many blocks in flight
-// as it holds warps.  The codes of the next row tile are loaded while the current one
-// is multiplied.
-__global__ void __launch_bounds__(128, 4) score_kernel(LayerView V) {
+// log-mass by shuffles -- with no CTA barrier.  Codes and scales reach shared memory by
+// cp.async in half blocks (two row tiles) through a two-stage ring per warp: every lane
+// copies exactly the 16-byte chunks of its own MMA fragments, so the next half block is
+// in flight while the current one is multiplied and no registers hold it.  The stream
+// is read once, so the copies carry an L2 evict-first hint.
+constexpr int SCORE_CTAS_PER_SM = 4;
+constexpr int SCORE_STAGES = 2;
+
+struct __align__(16) ScoreHalf {   // row tiles 2h, 2h+1 of a block; the scales with h = 0
+  uint4 codes[256];
+  uint4 scales[16];
+};
+
+__device__ __forceinline__ void cp_async16_evict_first(void* dst_smem, const void* src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+               :: "r"(d), "l"(src), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+__global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView V) {
+  extern __shared__ __align__(16) unsigned char score_dsm[];
+  ScoreHalf* ring = reinterpret_cast<ScoreHalf*>(score_dsm) + (threadIdx.x >> 5) * SCORE_STAGES;
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -49,67 +72,94 @@ __global__ void __launch_bounds__(128, 4) score_kernel(LayerView V) {
   const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const long long per = (total + nwarps - 1) / nwarps;
   const long long g0 = wid * per;
-  const long long g1 = min(total, g0 + per);
+  const int count = (int)max(0ll, min(total, g0 + per) - g0);
+  const int units = 2 * count;   // half blocks
+
+  // producer: copies half block u into ring slot u % SCORE_STAGES (one commit group each)
+  int phs = (int)(g0 / V.nb), pblk = (int)(g0 % V.nb);
+  auto issue = [&](int u) {
+    if (u < units) {
+      const int h = u & 1;
+      if (h == 0 && pblk == V.nb) { pblk = 0; ++phs; }
+      const size_t pbi = (size_t)phs * V.nbmax + pblk;
+      ScoreHalf& st = ring[u % SCORE_STAGES];
+      const uint4* kp = reinterpret_cast<const uint4*>(V.kc + pbi * KC_BYTES) + 256 * h;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) cp_async16_evict_first(&st.codes[lane + 32 * j], kp + lane + 32 * j);
+      if (h == 0 && lane < 16)
+        cp_async16_evict_first(&st.scales[lane], reinterpret_cast<const uint4*>(V.ks + pbi * D) + lane);
+      if (h == 1) ++pblk;
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int u = 0; u < SCORE_STAGES - 1; ++u) issue(u);
 
   int cur_hs = -1;
-  __half2 qh2[16];             // q of head gid>>1 at channels 32tig + [0, 32)
+  __half2 qh2[16];                  // q of head gid>>1 at channels 32tig + [0, 32)
   float pre = 1.f, inv_pre = 1.f;   // 2^e of head gid>>1 and its inverse
   float sc_out = 0.f;               // output scale of head tig
-  for (long long gi = g0; gi < g1; ++gi) {
-    const int hs = (int)(gi / V.nb), blk = (int)(gi % V.nb);
-    const int b = hs / V.Hkv, g = hs % V.Hkv;
-    const size_t bi = (size_t)hs * V.nbmax + blk;
-    const uint4* kp = reinterpret_cast<const uint4*>(V.kc + bi * KC_BYTES) + lane;
-    // row tile 0 in flight first, then the scales
-    uint4 A0 = __ldcs(kp), A1 = __ldcs(kp + 32), A2 = __ldcs(kp + 64), A3 = __ldcs(kp + 96);
-    const uint4* sp = reinterpret_cast<const uint4*>(V.ks + bi * D + 32 * tig);
-    const uint4 S0 = sp[0], S1 = sp[1], S2 = sp[2], S3 = sp[3];
-    if (hs != cur_hs) {
-      cur_hs = hs;
-      const float smax = __half2float(__ushort_as_half((unsigned short)V.kscale_max[hs]));
-      // max |q| per head slot over 128 channels: lane holds 4 channels of each slot
-      float qm[MAXREP];
+  // the group's queries: max |q| per head, this lane's slice, the power-of-two prescale
+  auto setup_q = [&](int hs_q) {
+    cur_hs = hs_q;
+    const int hrow = hs_q * V.n_rep;
+    const float smax = __half2float(__ushort_as_half((unsigned short)V.kscale_max[hs_q]));
+    float qm[MAXREP];
 #pragma unroll
-      for (int r = 0; r < MAXREP; ++r) {
-        float m = 0.f;
-        if (r < V.n_rep) {
-          const __half2 v = *reinterpret_cast<const __half2*>(V.q + head_row(V, b, g, r) * D + 4 * lane);
-          const __half2 w = *reinterpret_cast<const __half2*>(V.q + head_row(V, b, g, r) * D + 4 * lane + 2);
-          m = fmaxf(fmaxf(fabsf(__low2float(v)), fabsf(__high2float(v))),
-                    fmaxf(fabsf(__low2float(w)), fabsf(__high2float(w))));
-        }
-        qm[r] = warp_max(m);
-      }
-      const int r = gid >> 1;
-      float qmr = 0.f, qmt = 0.f;
-#pragma unroll
-      for (int k = 0; k < MAXREP; ++k) {
-        qmr = (k == r) ? qm[k] : qmr;
-        qmt = (k == tig) ? qm[k] : qmt;
-      }
+    for (int r = 0; r < MAXREP; ++r) {
+      float m = 0.f;
       if (r < V.n_rep) {
-        const uint4* qp = reinterpret_cast<const uint4*>(V.q + head_row(V, b, g, r) * D + 32 * tig);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint4 u = qp[i];
-          qh2[4 * i] = u32_as_h2(u.x); qh2[4 * i + 1] = u32_as_h2(u.y);
-          qh2[4 * i + 2] = u32_as_h2(u.z); qh2[4 * i + 3] = u32_as_h2(u.w);
-        }
-        pre = prescale_for(qmr * smax);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) qh2[i] = __float2half2_rn(0.f);
-        pre = 1.f;
+        const __half2 v = *reinterpret_cast<const __half2*>(V.q + (size_t)(hrow + r) * D + 4 * lane);
+        const __half2 w = *reinterpret_cast<const __half2*>(V.q + (size_t)(hrow + r) * D + 4 * lane + 2);
+        m = fmaxf(fmaxf(fabsf(__low2float(v)), fabsf(__high2float(v))),
+                  fmaxf(fabsf(__low2float(w)), fabsf(__high2float(w))));
       }
-      inv_pre = 1.f / pre;
-      sc_out = (tig < V.n_rep) ? INV_SQRT_D / prescale_for(qmt * smax) : 0.f;
+      qm[r] = warp_max(m);
     }
-    // B fragments for k-steps 0..7: channels 32tig + 4kk + {0,1} (b0) and {2,3} (b1),
-    // column gid = (head gid>>1, hi or lo half of q_c s_c 2^e)
-    uint32_t bf[16];
-    float dp = 0.f;
-    {
-      const uint4 Sv[4] = {S0, S1, S2, S3};
+    const int r = gid >> 1;
+    float qmr = 0.f, qmt = 0.f;
+#pragma unroll
+    for (int k = 0; k < MAXREP; ++k) {
+      qmr = (k == r) ? qm[k] : qmr;
+      qmt = (k == tig) ? qm[k] : qmt;
+    }
+    if (r < V.n_rep) {
+      const uint4* qp = reinterpret_cast<const uint4*>(V.q + (size_t)(hrow + r) * D + 32 * tig);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 u = qp[i];
+        qh2[4 * i] = u32_as_h2(u.x); qh2[4 * i + 1] = u32_as_h2(u.y);
+        qh2[4 * i + 2] = u32_as_h2(u.z); qh2[4 * i + 3] = u32_as_h2(u.w);
+      }
+      pre = prescale_for(qmr * smax);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) qh2[i] = __float2half2_rn(0.f);
+      pre = 1.f;
+    }
+    inv_pre = 1.f / pre;
+    sc_out = (tig < V.n_rep) ? INV_SQRT_D / prescale_for(qmt * smax) : 0.f;
+  };
+  if (units > 0) setup_q((int)(g0 / V.nb));   // overlaps the first copy
+
+  int hs = (int)(g0 / V.nb), blk = (int)(g0 % V.nb) - 1;
+  uint32_t bf[16];
+  float dp = 0.f;
+  float x[8];
+  for (int u = 0; u < units; ++u) {
+    issue(u + SCORE_STAGES - 1);
+    cp_async_wait<SCORE_STAGES - 1>();   // half block u has landed (this lane's copies)
+    __syncwarp();                        // ... and every lane's (the scales are shared)
+    const ScoreHalf& cur = ring[u % SCORE_STAGES];
+    const int h = u & 1;
+    if (h == 0) {
+      if (++blk == V.nb) { blk = 0; ++hs; }
+      if (hs != cur_hs) setup_q(hs);
+      // B fragments for k-steps 0..7: channels 32tig + 4kk + {0,1} (b0) and {2,3} (b1),
+      // column gid = (head gid>>1, hi or lo half of q_c s_c 2^e)
+      dp = 0.f;
+      const uint4 Sv[4] = {cur.scales[4 * tig], cur.scales[4 * tig + 1], cur.scales[4 * tig + 2],
+                           cur.scales[4 * tig + 3]};
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const uint32_t sw = (i & 3) == 0 ? Sv[i >> 2].x : (i & 3) == 1 ? Sv[i >> 2].y : (i & 3) == 2 ? Sv[i >> 2].z : Sv[i >> 2].w;
@@ -118,19 +168,15 @@ __global__ void __launch_bounds__(128, 4) score_kernel(LayerView V) {
         const float2 w = mul2(mul2(q2, make_float2(pre, pre)), s2);   // exact products
         dp += fabsf(w.x) + fabsf(w.y);
         const __half2 hi = __floats2half2_rn(w.x, w.y);
-        const float2 r = sub2(w, __half22float2(hi));                 // exact remainders
-        const __half2 lo = __floats2half2_rn(r.x, r.y);
+        const float2 rem = sub2(w, __half22float2(hi));               // exact remainders
+        const __half2 lo = __floats2half2_rn(rem.x, rem.y);
         bf[i] = (gid & 1) ? h2_as_u32(lo) : h2_as_u32(hi);
       }
     }
-    float x[8];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {        // MMA row tile w: tokens 16w .. 16w+15
-      const uint4 R0 = A0, R1 = A1, R2 = A2, R3 = A3;
-      if (w < 3) {
-        const uint4* np = kp + (w + 1) * 128;
-        A0 = __ldcs(np); A1 = __ldcs(np + 32); A2 = __ldcs(np + 64); A3 = __ldcs(np + 96);
-      }
+    for (int ww = 0; ww < 2; ++ww) {     // MMA row tile 2h + ww: tokens 16(2h + ww) + [0, 16)
+      const uint4 R0 = cur.codes[lane + 128 * ww], R1 = cur.codes[lane + 128 * ww + 32];
+      const uint4 R2 = cur.codes[lane + 128 * ww + 64], R3 = cur.codes[lane + 128 * ww + 96];
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
@@ -144,41 +190,47 @@ __global__ void __launch_bounds__(128, 4) score_kernel(LayerView V) {
         i8x4_to_f16(wb, a1, a3);
         mma16816(acc, a0, a1, a2, a3, bf[2 * kk], bf[2 * kk + 1]);
       }
-      // head tig, tokens 16w + gid and 16w + gid + 8
+      // head tig, tokens 16w + gid and 16w + gid + 8 (w = 2h + ww)
       const float2 xs = mul2(add2(make_float2(acc[0], acc[2]), make_float2(acc[1], acc[3])),
                              make_float2(sc_out, sc_out));
-      x[2 * w] = xs.x;
-      x[2 * w + 1] = xs.y;
+      if (h == 0) { x[2 * ww] = xs.x; x[2 * ww + 1] = xs.y; }
+      else { x[4 + 2 * ww] = xs.x; x[5 + 2 * ww] = xs.y; }
     }
-    if (tig < V.n_rep) {
-      float* sh = V.shat + head_row(V, b, g, tig) * ((size_t)V.nbmax * BLK) + (size_t)blk * BLK + gid;
+    __syncwarp();   // every lane is done with this slot before it is refilled
+    if (h == 1) {
+      const int hrow = hs * V.n_rep;   // query-head row of slot 0 (b Hq + g n_rep)
+      if (tig < V.n_rep) {
+        float* sh = V.shat + (size_t)(hrow + tig) * ((size_t)V.nbmax * BLK) + (size_t)blk * BLK + gid;
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        sh[16 * w] = x[2 * w];
-        sh[16 * w + 8] = x[2 * w + 1];
+        for (int w = 0; w < 4; ++w) {
+          sh[16 * w] = x[2 * w];
+          sh[16 * w + 8] = x[2 * w + 1];
+        }
       }
+      // block log-mass of head tig over its 64 tokens (8 per lane, 8 lanes per head)
+      float m = x[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) m = fmaxf(m, x[i]);
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+      float l = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) l += __expf(x[i] - m);   // relative error ~2^-22: inside the selection band
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      float d2 = dp;
+      d2 += __shfl_xor_sync(0xffffffffu, d2, 1);
+      d2 += __shfl_xor_sync(0xffffffffu, d2, 2);
+      // lane tig (gid 0) holds lse of head tig; lane 8r (tig 0, gid 2r) holds Delta of head r
+      if (gid == 0 && tig < V.n_rep)
+        V.lse8[(size_t)(hrow + tig) * V.nbmax + blk] = m + logf(l);
+      if (tig == 0 && (gid & 1) == 0 && (gid >> 1) < V.n_rep)
+        V.delta[(size_t)(hrow + (gid >> 1)) * V.nbmax + blk] = KAPPA * INV_SQRT_D * (d2 * inv_pre);
     }
-    // block log-mass of head tig over its 64 tokens (8 per lane, 8 lanes per head)
-    float m = x[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) m = fmaxf(m, x[i]);
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-    float l = 0.f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) l += __expf(x[i] - m);   // relative error ~2^-22: inside the selection band
-    l += __shfl_xor_sync(0xffffffffu, l, 4);
-    l += __shfl_xor_sync(0xffffffffu, l, 8);
-    l += __shfl_xor_sync(0xffffffffu, l, 16);
-    dp += __shfl_xor_sync(0xffffffffu, dp, 1);
-    dp += __shfl_xor_sync(0xffffffffu, dp, 2);
-    // lane 4r (gid 2r... tig 0) holds Delta of head r = gid>>1; lane tig (gid 0) holds lse of head tig
-    if (gid == 0 && tig < V.n_rep)
-      V.lse8[head_row(V, b, g, tig) * V.nbmax + blk] = m + logf(l);
-    if (tig == 0 && (gid & 1) == 0 && (gid >> 1) < V.n_rep)
-      V.delta[head_row(V, b, g, gid >> 1) * V.nbmax + blk] = KAPPA * INV_SQRT_D * (dp * inv_pre);
   }
+  cp_async_wait<0>();
 }
 
 // One CTA of 256 threads per (sequence, query head): the top-K* selection.  The last
@@ -309,13 +361,16 @@ size_t select_smem_bytes(int nb) {
   return sizeof(BlockSelSmem) + (size_t)((nb + 15) & ~15) * 4;
 }
 
-int score_grid(int num_sms) { return num_sms * 4; }
+int score_grid(int num_sms) { return num_sms * SCORE_CTAS_PER_SM; }
 
 cudaError_t launch_score(const LayerView& V, int grid, cudaStream_t st) {
   const long long total = (long long)V.BG * V.nb;
   if (total == 0) return cudaSuccess;   // nothing to score (only a partial block)
   if ((long long)grid * 4 > total) grid = (int)((total + 3) / 4);
-  score_kernel<<<grid, 128, 0, st>>>(V);
+  const size_t dyn = sizeof(ScoreHalf) * SCORE_STAGES * 4;   // 4 warps
+  cudaError_t e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  score_kernel<<<grid, 128, dyn, st>>>(V);
   return cudaGetLastError();
 }
 
