@@ -108,3 +108,37 @@ def test_c3_layer_128k_uncertified_sampled_groups():
             gv, ov = c[name][0, hs].astype(np.float64), getattr(u, name)[0]
             assert np.all(np.abs(gv - ov) <= BOUND_RTOL * np.abs(ov) + BOUND_ATOL), name
 
+
+def test_max_context_2m_tokens():
+    """The largest cache a sequence may hold (max_ctx = 2,097,152 tokens: 32,768 blocks,
+    the selection keeps one key per block in shared memory), one KV group of four query
+    heads, plus a ragged partial block: the whole group is compared with the oracle."""
+    N = (1 << 21)
+    q, K, V = W.c3_layer(0, device="cuda", ctx=N, Hq=4, Hkv=1)
+    # leave the last 37 tokens for a second append: the partial block at maximum size
+    out, cert, lvl, t1g, st = None, None, None, None, None
+    cache = kvq.Cache(1, 1, 4, 1, max_ctx=N)
+    try:
+        cache.append(0, K[:, :, :N - 37].contiguous(), V[:, :, :N - 37].contiguous())
+        cache.append(0, K[:, :, N - 37:].contiguous(), V[:, :, N - 37:].contiguous())
+        assert cache.length(0) == N
+        o = torch.empty(1, 4, 128, dtype=torch.float16, device="cuda")
+        c = torch.empty(4 * 32, dtype=torch.uint8, device="cuda")
+        lv = torch.empty(1, dtype=torch.int32, device="cuda")
+        cache.decode(0, q, 0.995, 0.25, o, c, lv)
+        torch.cuda.synchronize()
+        out, cert, lvl = o.cpu(), kvq.certificates(c).reshape(1, 4), lv.cpu().numpy()
+        t1g = {k: v.cpu() for k, v in cache.export_tier1(0).items()}
+        st = {k: v.cpu() for k, v in cache.export_decode_state(N // 64).items()}
+    finally:
+        cache.close()
+    qc, Kc, Vc = q.cpu(), K.cpu(), V.cpu()
+    del K, V
+    t1 = O.quantize_layer(Kc.numpy(), Vc.numpy())
+    for name in ("kc", "vc", "eta"):
+        assert np.array_equal(t1g[name].numpy(), getattr(t1, name)), name
+    r = O.decode_layer(qc.numpy(), Kc.numpy(), Vc.numpy(), t1, 0.995, 0.25, O.OracleConfig(n_rep=4))
+    g_res = dict(out=out, cert=cert, level=lvl, nb=N // 64, state=st)
+    stats = compare_decode(g_res, t1, r, 0.995, 0.25, 4)
+    assert stats["strict"] + stats["excluded"] == 4
+
