@@ -49,10 +49,10 @@ __global__ void fill_u32(uint32_t* p, uint32_t v, size_t n) {
 }
 
 enum KernelId { K_SCORE = 0, K_SELECT, K_MIX0, K_COMB0, K_MIX1, K_COMB1, K_DENSE, K_FINAL,
-                K_APPEND, K_COUNT };
+                K_APPEND, K_TAIL, K_COUNT };
 const char* kKernelNames[K_COUNT] = {"score", "select", "mixed_round0", "combine_round0",
                                      "mixed_round1", "combine_round1", "dense_fallback",
-                                     "finalize", "quantize_append"};
+                                     "finalize", "quantize_append", "int4_tail"};
 
 }  // namespace
 
@@ -516,7 +516,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   LayerView V;
   V.B = c->B; V.Hq = c->Hq; V.Hkv = c->Hkv; V.n_rep = c->n_rep; V.BG = c->BG;
   V.nb = N / BLK; V.n_tail = N % BLK; V.nbmax = c->nbmax; V.cap = c->cap;
-  V.chunk = decode_split(c, V.nb); V.nslot = c->nslot;
+  V.chunk = decode_split(c, V.nb); V.nslot = c->nslot; V.nparts = 0;
   V.kc = layer_kc(c, layer); V.ks = layer_ks(c, layer); V.vc = layer_vc(c, layer);
   V.vsv = layer_vsv(c, layer); V.eta = layer_eta(c, layer);
   V.vmin = layer_vmin(c, layer); V.vmax = layer_vmax(c, layer);
@@ -537,7 +537,16 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   if (!all_dense) {
     { KernelScope s(c, K_SCORE, st); KVQ_CUDA(s.done(launch_score(V, score_grid(c->num_sms), st)), "score"); }
     { KernelScope s(c, K_SELECT, st); KVQ_CUDA(s.done(launch_select(V, st)), "select"); }
-    { KernelScope s(c, K_MIX0, st); KVQ_CUDA(s.done(launch_mixed(V, 0, mixed_grid(c->num_sms), st)), "mixed_round0"); }
+    if (certified || c->v16) {
+      KernelScope s(c, K_MIX0, st);
+      KVQ_CUDA(s.done(launch_mixed(V, 0, mixed_grid(c->num_sms), st)), "mixed_round0");
+    } else {
+      // nothing is paged in: the INT4 value pass over every block, one partial per run
+      const int runs = tail_runs(c->num_sms, V.BG);
+      KernelScope s(c, K_TAIL, st);
+      KVQ_CUDA(s.done(launch_tail(V, runs, c->num_sms, st)), "int4_tail");
+      V.nparts = runs;
+    }
     { KernelScope s(c, K_COMB0, st); KVQ_CUDA(s.done(launch_combine(V, 0, st)), "combine_round0"); }
     if (certified) {
       { KernelScope s(c, K_MIX1, st); KVQ_CUDA(s.done(launch_mixed(V, 1, mixed_grid(c->num_sms), st)), "mixed_round1"); }

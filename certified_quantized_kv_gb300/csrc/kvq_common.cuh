@@ -73,6 +73,7 @@ struct LayerView {
   int nbmax;       // block capacity per (sequence, KV head), a multiple of 16
   int chunk;       // blocks per work item of the mixed and dense passes (1..CHUNK)
   int nslot;       // partial slots per KV group (>= the work items of a group)
+  int nparts;      // partial slots the combine kernel adds (0: one per work item)
   long long cap;   // token capacity of tier 2 per (sequence, KV head)
   // tier 1 of this layer
   const int8_t* kc;      // [BG][nbmax][8192]
@@ -167,6 +168,21 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
 __device__ __forceinline__ uint32_t nib_to_f16(uint32_t w, int i) {
   const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
   return h2_as_u32(__hsub2(u32_as_h2(t), u32_as_h2(0x64006400u)));
+}
+
+// All four nibble pairs of a V-code word -> f16x2 registers a[0..3], exactly (the same
+// values as nib_to_f16(w, 0..3)) in nine instructions.  Pairs 0 and 2 sit at bits 0-3 and
+// 16-19 (of w, and of w with bytes 1 and 3 moved down by a byte permute): 0x6400 | n reads
+// 1024 + n.  Pairs 1 and 3 sit at bits 4-7 and 20-23: 0x6400 | 16 n reads 1024 + 16 n, and
+// (1024 + 16 n) / 16 - 64 = n; every step is exact in binary16.
+__device__ __forceinline__ void nib8_to_f16x4(uint32_t w, uint32_t& a0, uint32_t& a1, uint32_t& a2,
+                                              uint32_t& a3) {
+  const uint32_t x = __byte_perm(w, 0u, 0x4341);   // bytes 1 and 3 of w into bytes 0 and 2
+  const __half2 k1024 = u32_as_h2(0x64006400u), k16th = u32_as_h2(0x2C002C00u), km64 = u32_as_h2(0xD400D400u);
+  a0 = h2_as_u32(__hsub2(u32_as_h2((w & 0x000F000Fu) | 0x64006400u), k1024));
+  a1 = h2_as_u32(__hfma2(u32_as_h2((w & 0x00F000F0u) | 0x64006400u), k16th, km64));
+  a2 = h2_as_u32(__hsub2(u32_as_h2((x & 0x000F000Fu) | 0x64006400u), k1024));
+  a3 = h2_as_u32(__hfma2(u32_as_h2((x & 0x00F000F0u) | 0x64006400u), k16th, km64));
 }
 
 // x = hi + lo with hi = rn16(x), lo = rn16(x - hi); exact unless lo is subnormal.

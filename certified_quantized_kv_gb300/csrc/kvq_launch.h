@@ -52,6 +52,8 @@ cudaError_t launch_score(const LayerView& V, int grid, cudaStream_t st);
 cudaError_t launch_select(const LayerView& V, cudaStream_t st);
 cudaError_t launch_mixed(const LayerView& V, int round, int grid, cudaStream_t st);
 cudaError_t launch_combine(const LayerView& V, int round, cudaStream_t st);
+int tail_runs(int num_sms, int groups);
+cudaError_t launch_tail(const LayerView& V, int runs, int num_sms, cudaStream_t st);
 cudaError_t launch_dense(const LayerView& V, int all_dense, int grid, cudaStream_t st);
 cudaError_t launch_finalize(const LayerView& V, kvq_certificate* cert, int32_t* level,
                             cudaStream_t st);

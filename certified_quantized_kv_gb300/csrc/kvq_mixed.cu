@@ -252,8 +252,9 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t w = (kk == 0) ? C.x : (kk == 1) ? C.y : (kk == 2) ? C.z : C.w;
-            mma16816(acc[mt], nib_to_f16(w, 0), nib_to_f16(w, 1), nib_to_f16(w, 2),
-                     nib_to_f16(w, 3), bb0[kk], bb1[kk]);
+            uint32_t a0, a1, a2, a3;
+            nib8_to_f16x4(w, a0, a1, a2, a3);
+            mma16816(acc[mt], a0, a1, a2, a3, bb0[kk], bb1[kk]);
           }
         }
       }
@@ -319,7 +320,7 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   const int hs = b * V.Hkv + g;
   const size_t hb = (size_t)bh;
   const int nb = V.nb;
-  const int nch = max(1, (nb + V.chunk - 1) / V.chunk);
+  const int nch = V.nparts > 0 ? V.nparts : max(1, (nb + V.chunk - 1) / V.chunk);
   const int NCH = V.nslot;
   const uint8_t* kfl = (round == 0 ? V.kprom0 : V.kprom1) + (size_t)hs * V.nbmax;
   // first pass: no FP16 values yet (every head's rung 2 plans against this empty set,

@@ -1,0 +1,208 @@
+// kvq_tail.cu -- the INT4 value pass over blocks that keep their INT8 scores: softmax
+// weights from the stored INT8 scores times the INT4 value reconstructions.
+//
+// "Runtime-Certified Bounded-Error Quantized Attention" (gist.science technical summary),
+// Method §1 (INT4 values per 32-channel group with scale and offset) and Method §3 (the
+// tail of the context keeps its INT8 scores).  For a block b and query head h:
+//   p_t = exp(s_hat_t - M_h),  sum_t p_t v_hat_t = sum_t (p_t s_{t,g}) code_{t,c} + sum_t p_t o_{t,g}
+// with g the value group of channel c.  The first sum runs on the tensor cores as in the
+// mixed pass (channels as MMA rows, tokens as k, the eight columns = four heads x the hi
+// and lo halves of p s 2^e, exact in f16), the second on the CUDA cores.
+//
+// Work split: one warp per run of consecutive blocks of one KV group (runs per group =
+// warps / groups), no CTA barrier; each block's codes, scales/offsets and scores reach
+// shared memory by cp.async through a two-stage ring per warp, so the next block is in
+// flight while the current one is multiplied.  Each run writes one partial (sum p v_hat
+// and sum p per head) into its own slot, which the combine kernel adds in a fixed order.
+#include "kvq_common.cuh"
+#include "kvq_launch.h"
+
+namespace kvq {
+
+namespace {
+
+constexpr int TAIL_CTAS_PER_SM = 4;
+constexpr int TAIL_STAGES = 2;
+
+// One block's tail data in shared memory: INT4 codes (this lane's chunks at lane + 32 j),
+// (scale, offset) per value group and token, and the INT8 scores of the group's heads.
+struct __align__(16) TailStage {
+  uint4 codes[VC_BYTES / 16];          // 256 chunks
+  uint4 so[VSV_WORDS / 4];             // 64 x 4 half2: [group][token]
+  float4 s[MAXREP * BLK / 4];          // [head][token]
+};
+
+__device__ __forceinline__ void cp16(void* dst_smem, const void* src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+               :: "r"(d), "l"(src), "l"(pol) : "memory");
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V, int runs) {
+  extern __shared__ __align__(16) unsigned char tail_dsm[];
+  TailStage* ring = reinterpret_cast<TailStage*>(tail_dsm) + (threadIdx.x >> 5) * TAIL_STAGES;
+  pdl_trigger();
+  pdl_wait();   // scores of the scoring pass, reference maxima of the selection
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int r = gid >> 1;   // head of this lane's B column (hi half for even gid)
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int NCH = V.nslot;
+
+  for (int unit = wid; unit < V.BG * runs; unit += nwarps) {
+    const int hs = unit / runs, run = unit % runs;
+    const int b0 = (int)((long long)run * V.nb / runs);
+    const int b1 = (int)((long long)(run + 1) * V.nb / runs);
+    const int hrow = hs * V.n_rep;
+    const bool act = r < V.n_rep;
+    const float M = act ? V.hst[hrow + r].M : 0.f;
+    const float pre_v = prescale_for(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
+    const uint8_t* kp0 = V.kprom0 + (size_t)hs * V.nbmax;
+    // the run's blocks that keep INT8 scores (FP16-key blocks are the mixed pass's)
+    auto next_block = [&](int b) {
+      while (b < b1 && kp0[b]) ++b;
+      return b;
+    };
+    int pb = next_block(b0);   // producer: next block to copy
+    auto issue = [&](int st) {
+      if (pb < b1) {
+        const size_t bi = (size_t)hs * V.nbmax + pb;
+        TailStage& T = ring[st];
+        const uint4* vc = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) cp16(&T.codes[lane + 32 * j], vc + lane + 32 * j);
+        const uint4* so = reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS);
+        cp16(&T.so[lane], so + lane);
+        cp16(&T.so[lane + 32], so + lane + 32);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {   // 64 float4 of scores: head j * 2 + lane / 16
+          const int idx = lane + 32 * j, h = idx >> 4;
+          if (h < V.n_rep)
+            cp16(&T.s[idx], V.shat + (size_t)(hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)pb * BLK + 4 * (idx & 15));
+        }
+        pb = next_block(pb + 1);
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+
+    float acc[NG][2][4];
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[g][mt][j] = 0.f;
+    float off[NG] = {0.f, 0.f, 0.f, 0.f};   // sum p o per value group, head r
+    float lsum = 0.f;                        // sum p, head r
+
+    issue(0);
+    int it = 0;
+    for (int blk = next_block(b0); blk < b1; blk = next_block(blk + 1), ++it) {
+      issue((it + 1) % TAIL_STAGES);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      __syncwarp();
+      const TailStage& T = ring[it % TAIL_STAGES];
+      // weights of head r at tokens 16 tig + [0, 16) (k-step kk: tokens 16 tig + 4 kk + i)
+      float p[16];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 s4 = T.s[(act ? r : 0) * (BLK / 4) + 4 * tig + kk];
+        p[4 * kk] = act ? __expf(s4.x - M) : 0.f;
+        p[4 * kk + 1] = act ? __expf(s4.y - M) : 0.f;
+        p[4 * kk + 2] = act ? __expf(s4.z - M) : 0.f;
+        p[4 * kk + 3] = act ? __expf(s4.w - M) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) lsum += p[i];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        uint32_t bb0[4], bb1[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint4 so = T.so[g * (BLK / 4) + 4 * tig + kk];   // (scale, offset) of 4 tokens
+          const __half2* so2 = reinterpret_cast<const __half2*>(&so);
+          uint32_t bw[2];
+#pragma unroll
+          for (int i = 0; i < 4; i += 2) {   // tokens 4kk + i, 4kk + i + 1
+            const float2 a = __half22float2(so2[i]), c = __half22float2(so2[i + 1]);
+            const float2 pv = make_float2(p[4 * kk + i], p[4 * kk + i + 1]);
+            const float2 o2 = mul2(pv, make_float2(a.y, c.y));
+            off[g] += o2.x + o2.y;
+            // p s 2^e as hi + lo, both f16 (the fp32 remainder is exact)
+            const float2 w = mul2(mul2(pv, make_float2(a.x, c.x)), make_float2(pre_v, pre_v));
+            const __half2 hi = __floats2half2_rn(w.x, w.y);
+            const float2 rem = sub2(w, __half22float2(hi));
+            const __half2 lo = __floats2half2_rn(rem.x, rem.y);
+            bw[i >> 1] = (gid & 1) ? h2_as_u32(lo) : h2_as_u32(hi);
+          }
+          bb0[kk] = bw[0];
+          bb1[kk] = bw[1];
+        }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const uint4 Cw = T.codes[lane + 32 * (2 * g + mt)];
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t w = (kk == 0) ? Cw.x : (kk == 1) ? Cw.y : (kk == 2) ? Cw.z : Cw.w;
+            uint32_t a0, a1, a2, a3;
+            nib8_to_f16x4(w, a0, a1, a2, a3);
+            mma16816(acc[g][mt], a0, a1, a2, a3, bb0[kk], bb1[kk]);
+          }
+        }
+      }
+      __syncwarp();   // every lane is done with this slot before it is refilled
+    }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+
+    // head r's sums are spread over the four tig lanes of lane pair (2r, 2r+1): the hi
+    // lane (even gid) carries them once
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      off[g] += __shfl_xor_sync(0xffffffffu, off[g], 1);
+      off[g] += __shfl_xor_sync(0xffffffffu, off[g], 2);
+    }
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+    // this lane writes head tig: its offsets sit in lane 8 tig (gid 2 tig, tig 0)
+    float offh[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) offh[g] = __shfl_sync(0xffffffffu, off[g], 8 * tig);
+    const float inv = 1.f / pre_v;
+    float* pp = V.part + (((size_t)hs * NCH + run) * MAXREP) * (D + 4);
+    if (tig < V.n_rep) {
+      float* pr = pp + tig * (D + 4);
+#pragma unroll
+      for (int g = 0; g < NG; ++g)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int c0 = 32 * g + 16 * mt + gid;
+          pr[c0] = (acc[g][mt][0] + acc[g][mt][1]) * inv + offh[g];
+          pr[c0 + 8] = (acc[g][mt][2] + acc[g][mt][3]) * inv + offh[g];
+        }
+    }
+    if (tig == 0 && (gid & 1) == 0 && act) pp[r * (D + 4) + D] = lsum;
+  }
+}
+
+int tail_runs(int num_sms, int groups) {
+  const int warps = num_sms * TAIL_CTAS_PER_SM * 4;
+  return groups >= warps ? 1 : warps / groups;
+}
+
+cudaError_t launch_tail(const LayerView& V, int runs, int num_sms, cudaStream_t st) {
+  int grid = num_sms * TAIL_CTAS_PER_SM;
+  const int units = V.BG * runs;
+  if (grid * 4 > units) grid = (units + 3) / 4;
+  const size_t dyn = sizeof(TailStage) * TAIL_STAGES * 4;   // 4 warps
+  cudaError_t e = cudaFuncSetAttribute(tail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(tail_kernel, dim3(grid), dim3(128), dyn, st, V, runs);
+}
+
+}  // namespace kvq
