@@ -163,15 +163,8 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
   hi = h2_as_u32(__hsub2(u32_as_h2(h), bias));
 }
 
-// Nibble pair i of a V-code word (bits 4i..4i+3 and 16+4i..16+4i+3) -> f16x2, exactly:
-// 0x6400 | n reads 1024 + n; subtracting 1024 leaves n.
-__device__ __forceinline__ uint32_t nib_to_f16(uint32_t w, int i) {
-  const uint32_t t = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;
-  return h2_as_u32(__hsub2(u32_as_h2(t), u32_as_h2(0x64006400u)));
-}
-
-// All four nibble pairs of a V-code word -> f16x2 registers a[0..3], exactly (the same
-// values as nib_to_f16(w, 0..3)) in nine instructions.  Pairs 0 and 2 sit at bits 0-3 and
+// The four nibble pairs of a V-code word (pair i: bits 4i..4i+3 and 16+4i..16+4i+3) ->
+// f16x2 registers a0..a3, exactly, in nine instructions.  Pairs 0 and 2 sit at bits 0-3 and
 // 16-19 (of w, and of w with bytes 1 and 3 moved down by a byte permute): 0x6400 | n reads
 // 1024 + n.  Pairs 1 and 3 sit at bits 4-7 and 20-23: 0x6400 | 16 n reads 1024 + 16 n, and
 // (1024 + 16 n) / 16 - 64 = n; every step is exact in binary16.
