@@ -396,8 +396,9 @@ class DecodeResult:
     n_val_promoted: np.ndarray  # int [B, Hq]
     promoted_bytes: np.ndarray  # int64 [B, Hq]: tier-2 bytes paged in for the head's KV group
                                 # (FP16 key blocks of the union U, plus rung-1 key blocks,
-                                # rung-2 value blocks, and K and V of every full block
-                                # when a head of the group goes dense)
+                                # rung-2 value blocks, and, when a head of the group goes
+                                # dense, the values of every full block and the keys of
+                                # the blocks not paged in before)
     ladder_level: np.ndarray   # int [B]
     # diagnostics for parity tests
     sel: list = field(default_factory=list)      # [B][Hq] selected blocks in order
@@ -536,8 +537,11 @@ def decode_layer(q: np.ndarray, K: np.ndarray, V: np.ndarray, t1: Tier1,
         for g in range(Hkv):
             heads = range(g * cfg.n_rep, (g + 1) * cfg.n_rep)
             if any(level[b, h] >= 3 for h in heads):
-                # K and V of every full block from tier 2 (K only with FP16 values)
-                group_bytes[b, g] += (1 if cfg.value_fp16 else 2) * nb * blk_bytes
+                # values of every full block from tier 2 (none with FP16 values resident),
+                # keys of the blocks whose FP16 keys this call has not paged in already
+                # (the FP16 scores of those are reused; all of them at tau_cov >= 1)
+                k_new = nb - (int(kprom1[b, g].sum()) if tau_cov < 1.0 else 0)
+                group_bytes[b, g] += (k_new + (0 if cfg.value_fp16 else nb)) * blk_bytes
             for h in heads:
                 if level[b, h] >= 3:
                     out64[b, h] = dense_attention(q[b, h], K[b, g], V[b, g])
