@@ -419,17 +419,20 @@ def our_arm(args, wl):
     cache.set_debug(0)
     # FP16 blocks paged in per pass, from the selection state of every layer
     nb = N // 64
-    u0 = u1_new = v1 = dense_groups = 0
+    u0 = u1_new = v1 = dense_blocks = 0
     for layer in range(L):
         cache.decode(layer, qs[layer], tau, eps, outs[layer], certs[layer], lvls[layer])
         st = cache.export_decode_state(nb)
         k0, k1, vv = st["kprom0"].sum().item(), st["kprom1"].sum().item(), st["vprom1"].sum().item()
         u0 += k0; u1_new += k1 - k0; v1 += vv
         c = kvq.certificates(certs[layer]).reshape(B, Hq)
-        dense_groups += int((c["level"].reshape(B, Hkv, Hq // Hkv) >= 3).any(axis=2).sum())
+        dense = (c["level"].reshape(B, Hkv, Hq // Hkv) >= 3).any(axis=2)
+        # a dense group pages in every value block and the key blocks not paged in before
+        kp1 = st["kprom1"].sum(dim=2).cpu().numpy()
+        dense_blocks += int(((2 * nb - kp1) * dense).sum())
     torch.cuda.synchronize()
     host_bytes = {"mixed_round0": u0 * F16_BLOCK / L, "mixed_round1": (u1_new + v1) * F16_BLOCK / L,
-                  "dense_fallback": dense_groups * 2 * nb * F16_BLOCK / L}
+                  "dense_fallback": dense_blocks * F16_BLOCK / L}
 
     # end to end through the C ABI with host buffers (q in, out + certificate back)
     outs_h = [torch.empty(B, Hq, D, dtype=torch.float16).pin_memory() for _ in range(L)]

@@ -13,7 +13,9 @@
 //
 // The kernel reads FP16 keys and values straight from pinned host memory over the host
 // link (split-K over runs of up to 16 blocks, online softmax per run), which is the bound of
-// this path; the CUDA cores keep up with the link, so no tensor-core tiling is used.
+// this path; the CUDA cores keep up with the link, so no tensor-core tiling is used.  For
+// the key blocks this call already paged in, the exact scores kept by the mixed pass are
+// reused and only the values cross the link.
 #include "kvq_common.cuh"
 #include "kvq_launch.h"
 #include "kvq.h"
@@ -120,7 +122,9 @@ __device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dens
       gs.need_round1 = 0; gs.n_kprom0 = 0; gs.n_kprom1 = 0; gs.n_vprom1 = 0; gs.bytes = 0;
     }
     gs.need_dense = 1;
-    gs.bytes += (V.v16 ? 1LL : 2LL) * V.nb * F16_BLOCK_BYTES;   // tier-2 keys (and values)
+    // tier-2 values of every block (none when FP16 values are resident) and the keys of the
+    // blocks whose FP16 scores this call does not already hold
+    gs.bytes += ((long long)(V.nb - gs.n_kprom1) + (V.v16 ? 0LL : (long long)V.nb)) * F16_BLOCK_BYTES;
   }
 }
 
@@ -165,6 +169,8 @@ __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) 
     const int blk_end = min(V.nb, (ch + 1) * V.chunk);
     for (int blk = ch * V.chunk; blk < blk_end; ++blk) {
       const size_t src = ((size_t)hs * V.cap + (size_t)blk * BLK) * D;
+      // FP16 keys this call already paged in: their exact scores are in the score scratch
+      const bool have_s = !all_dense && V.kprom1[(size_t)hs * V.nbmax + blk];
       {
         // all sixteen 16-byte loads of a thread in flight before the first store
         const uint4* ks = reinterpret_cast<const uint4*>(V.t2k + src);
@@ -172,16 +178,25 @@ __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) 
             V.v16 ? V.v16 + ((size_t)hs * V.nbmax + blk) * (BLK * D) : V.t2v + src);   // FP16 values
         uint4 rk[8], rv[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) { rk[j] = ks[tid + 128 * j]; rv[j] = vs[tid + 128 * j]; }
+        for (int j = 0; j < 8; ++j) {
+          rv[j] = vs[tid + 128 * j];
+          if (!have_s) rk[j] = ks[tid + 128 * j];
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           const int i = tid + 128 * j, row = i >> 4, col = (i & 15) * 8;
-          *reinterpret_cast<uint4*>(&sm.kbuf[row][col]) = rk[j];
+          if (!have_s) *reinterpret_cast<uint4*>(&sm.kbuf[row][col]) = rk[j];
           *reinterpret_cast<uint4*>(&sm.vbuf[row][col]) = rv[j];
         }
       }
       __syncthreads();
-      {
+      if (have_s) {
+        const int t = tid & 63, rp = (tid >> 6) * 2;
+        const size_t o = (size_t)blk * BLK + t;
+        const size_t row = (size_t)V.nbmax * BLK;
+        sm.s[rp][t] = (rp < V.n_rep) ? V.shat[head_row(V, b, g, rp) * row + o] : 0.f;
+        sm.s[rp + 1][t] = (rp + 1 < V.n_rep) ? V.shat[head_row(V, b, g, rp + 1) * row + o] : 0.f;
+      } else {
         const int t = tid & 63, rp = (tid >> 6) * 2;
         float s0 = 0.f, s1 = 0.f;
         for (int c = 0; c < D; c += 8) {
