@@ -84,7 +84,7 @@ struct kvq_cache {
   uint32_t* mkey = nullptr;
   HeadState* hst = nullptr;
   GroupState* gst = nullptr;
-  float *part = nullptr, *part1 = nullptr, *dpart = nullptr;
+  float *part = nullptr, *part1 = nullptr, *dpart = nullptr, *red0 = nullptr;
   unsigned int* counters = nullptr;
   __half *q_stage = nullptr, *out_stage = nullptr;
   kvq_certificate* cert_stage = nullptr;
@@ -338,6 +338,7 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   const size_t s_gst = o;   o = align_up(o + BG * sizeof(GroupState), 256);
   const size_t s_part = o;  o = align_up(o + BG * NCH * MAXREP * (D + 4) * 4, 256);
   const size_t s_part1 = o; o = align_up(o + BG * NCH * MAXREP * (D + 4) * 4, 256);
+  const size_t s_red0 = o;  o = align_up(o + HQ * (D + 4) * 4, 256);
   const size_t s_dpart = o; o = align_up(o + BG * NCH * MAXREP * (D + 4) * 4, 256);
   const size_t s_cnt = o;   o = align_up(o + (CNT_GROUP_BASE + 4 * BG) * 4, 256);
   const size_t s_q = o;     o = align_up(o + HQ * D * 2, 256);
@@ -363,6 +364,7 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   c->gst = reinterpret_cast<GroupState*>(c->scr + s_gst);
   c->part = reinterpret_cast<float*>(c->scr + s_part);
   c->part1 = reinterpret_cast<float*>(c->scr + s_part1);
+  c->red0 = reinterpret_cast<float*>(c->scr + s_red0);
   c->dpart = reinterpret_cast<float*>(c->scr + s_dpart);
   c->counters = reinterpret_cast<unsigned int*>(c->scr + s_cnt);
   c->q_stage = reinterpret_cast<__half*>(c->scr + s_q);
@@ -531,7 +533,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   V.shat = c->shat; V.lse8 = c->lse8; V.delta = c->delta; V.lse16 = c->lse16; V.sel = c->sel;
   V.kprom0 = c->kprom0; V.kprom1 = c->kprom1; V.vprom1 = c->vprom1;
   V.hst = c->hst; V.gst = c->gst; V.part = c->part; V.dpart = c->dpart; V.counters = c->counters;
-  V.mkey = c->mkey; V.part1 = c->part1;
+  V.mkey = c->mkey; V.part1 = c->part1; V.red0 = c->red0;
 
   const bool all_dense = certified && ((tau >= 1.f) || (c->debug & KVQ_DEBUG_FORCE_DENSE));
   if (!all_dense) {

@@ -112,6 +112,7 @@ struct LayerView {
   GroupState* gst;       // [BG]
   float* part;           // [BG][nslot][MAXREP][D+4] partials of the mixed pass
   float* part1;          // same shape: deltas of the second mixed pass
+  float* red0;           // [B*Hq][D+4] the first pass's partials summed (channels, then l)
   float* dpart;          // [BG][nslot][MAXREP][D+4] partials of the dense pass
   uint32_t* mkey;        // [B][Hq][nbmax] selection keys (normalised values, fp32 bits)
   unsigned int* counters;  // work queues and completion counters (self-resetting)

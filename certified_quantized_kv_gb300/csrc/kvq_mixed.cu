@@ -349,23 +349,20 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
     if (!(hsd.planned == 1 || hsd.planned == 2)) return;
     hsd.n_vprom = nv;
   }
-  // (1) work-item partials in a fixed order: warp w sums items w, w + 8, ... (lane = four
-  //     channels), then the eight warp sums are added in warp order
+  // (1) work-item partials of this pass in a fixed order: warp w sums items w, w + 8, ...
+  //     (lane = four channels), then the eight warp sums are added in warp order; the
+  //     second pass adds its deltas to the first pass's sums
   {
     const int warp = tid >> 5, lane = tid & 31;
+    const float* P = (round == 0) ? V.part : V.part1;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
     float l = 0.f;
 #pragma unroll 8
     for (int ch = warp; ch < nch; ch += BS_WARPS) {
       const size_t o = (((size_t)hs * NCH + ch) * MAXREP + r) * (D + 4);
-      const float4 x = *reinterpret_cast<const float4*>(V.part + o + 4 * lane);
+      const float4 x = *reinterpret_cast<const float4*>(P + o + 4 * lane);
       a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
-      if (lane == 0) l += V.part[o + D];
-      if (round == 1) {
-        const float4 y = *reinterpret_cast<const float4*>(V.part1 + o + 4 * lane);
-        a.x += y.x; a.y += y.y; a.z += y.z; a.w += y.w;
-        if (lane == 0) l += V.part1[o + D];
-      }
+      if (lane == 0) l += P[o + D];
     }
     *reinterpret_cast<float4*>(&acc_s[warp][4 * lane]) = a;
     if (lane == 0) l_s[warp] = l;
@@ -386,13 +383,17 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
     tail_p[tid] = lt;
   }
   lt = block_sum(lt, ws.red);   // synchronises acc_s, l_s and tail_p too
-  float L = lt;
+  float* red = V.red0 + hb * (D + 4);
+  float L0 = (round == 1) ? red[D] : 0.f;
 #pragma unroll
-  for (int w = 0; w < BS_WARPS; ++w) L += l_s[w];
+  for (int w = 0; w < BS_WARPS; ++w) L0 += l_s[w];
+  const float L = L0 + lt;
+  if (round == 0 && tid == 0) red[D] = L0;
   if (tid < D) {
-    float a = 0.f;
+    float a = (round == 1) ? red[tid] : 0.f;
 #pragma unroll
     for (int w = 0; w < BS_WARPS; ++w) a += acc_s[w][tid];
+    if (round == 0) red[tid] = a;
     for (int t = 0; t < V.n_tail; ++t)
       a += tail_p[t] * __half2float(V.tail_v[((size_t)hs * BLK + t) * D + tid]);
     V.out[hb * D + tid] = __float2half_rn(a / L);
