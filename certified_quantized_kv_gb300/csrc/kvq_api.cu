@@ -81,7 +81,6 @@ struct kvq_cache {
   char* scr = nullptr;
   float *shat = nullptr, *lse8 = nullptr, *delta = nullptr, *lse16 = nullptr;
   uint8_t *sel = nullptr, *kprom0 = nullptr, *kprom1 = nullptr, *vprom1 = nullptr;
-  uint32_t* mkey = nullptr;
   HeadState* hst = nullptr;
   GroupState* gst = nullptr;
   float *part = nullptr, *part1 = nullptr, *dpart = nullptr, *red0 = nullptr;
@@ -330,7 +329,6 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   const size_t s_delta = o; o = align_up(o + HQ * nbm * 4, 256);
   const size_t s_lse16 = o; o = align_up(o + HQ * nbm * 4, 256);
   const size_t s_sel = o;   o = align_up(o + HQ * nbm, 256);
-  const size_t s_mkey = o;  o = align_up(o + HQ * nbm * 4, 256);
   const size_t s_kp0 = o;   o = align_up(o + BG * nbm, 256);
   const size_t s_kp1 = o;   o = align_up(o + BG * nbm, 256);
   const size_t s_vp1 = o;   o = align_up(o + BG * nbm, 256);
@@ -356,7 +354,6 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   c->delta = reinterpret_cast<float*>(c->scr + s_delta);
   c->lse16 = reinterpret_cast<float*>(c->scr + s_lse16);
   c->sel = reinterpret_cast<uint8_t*>(c->scr + s_sel);
-  c->mkey = reinterpret_cast<uint32_t*>(c->scr + s_mkey);
   c->kprom0 = reinterpret_cast<uint8_t*>(c->scr + s_kp0);
   c->kprom1 = reinterpret_cast<uint8_t*>(c->scr + s_kp1);
   c->vprom1 = reinterpret_cast<uint8_t*>(c->scr + s_vp1);
@@ -533,7 +530,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   V.shat = c->shat; V.lse8 = c->lse8; V.delta = c->delta; V.lse16 = c->lse16; V.sel = c->sel;
   V.kprom0 = c->kprom0; V.kprom1 = c->kprom1; V.vprom1 = c->vprom1;
   V.hst = c->hst; V.gst = c->gst; V.part = c->part; V.dpart = c->dpart; V.counters = c->counters;
-  V.mkey = c->mkey; V.part1 = c->part1; V.red0 = c->red0;
+  V.part1 = c->part1; V.red0 = c->red0;
 
   const bool all_dense = certified && ((tau >= 1.f) || (c->debug & KVQ_DEBUG_FORCE_DENSE));
   if (!all_dense) {

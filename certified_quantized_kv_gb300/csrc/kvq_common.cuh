@@ -114,7 +114,6 @@ struct LayerView {
   float* part1;          // same shape: deltas of the second mixed pass
   float* red0;           // [B*Hq][D+4] the first pass's partials summed (channels, then l)
   float* dpart;          // [BG][nslot][MAXREP][D+4] partials of the dense pass
-  uint32_t* mkey;        // [B][Hq][nbmax] selection keys (normalised values, fp32 bits)
   unsigned int* counters;  // work queues and completion counters (self-resetting)
 };
 

@@ -519,8 +519,17 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
       // rung 1: INT8 blocks by descending mass_b (e^Delta_b - 1) until the removed share
       // of S reaches 1 - eps A / (2 R S)
       const double need = 1.0 - (double)eps * (double)A / (2.0 * (double)R * (double)S);
-      for (int i = tid; i < nb; i += BS_THREADS)
-        keys[i] = kfl[i] ? 0u : __float_as_uint(expf(lse8[i] - LSEp) * expm1f(dl[i]) / S);
+      for (int i4 = tid; i4 < (nb + 3) / 4; i4 += BS_THREADS) {   // four blocks per step
+        const uchar4 kf4 = reinterpret_cast<const uchar4*>(kfl)[i4];
+        const float4 l8 = reinterpret_cast<const float4*>(lse8)[i4];
+        const float4 d4 = reinterpret_cast<const float4*>(dl)[i4];
+        const unsigned char kf[4] = {kf4.x, kf4.y, kf4.z, kf4.w};
+        const float a8[4] = {l8.x, l8.y, l8.z, l8.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (4 * i4 + j < nb)
+            keys[4 * i4 + j] = kf[j] ? 0u : __float_as_uint(expf(a8[j] - LSEp) * expm1f(dd[j]) / S);
+      }
       __syncthreads();
       unsigned long long taken = 0;
       block_select_top(nb, keys, fixed62(need), [&](int i) { k1[i] = 1; }, ws, &taken);
@@ -537,8 +546,19 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
         // are FP16 yet)
         const double target = fmin((double)eps - (double)ekey_proj, (double)V.v_tol);
         const double need = 1.0 - target / (double)e_val;
-        for (int i = tid; i < nb; i += BS_THREADS)
-          keys[i] = __float_as_uint(expf((kfl[i] ? lse16[i] : lse8[i]) - LSEp) * eta[i] / e_val);
+        for (int i4 = tid; i4 < (nb + 3) / 4; i4 += BS_THREADS) {   // four blocks per step
+          const uchar4 kf4 = reinterpret_cast<const uchar4*>(kfl)[i4];
+          const float4 l8 = reinterpret_cast<const float4*>(lse8)[i4];
+          const float4 l16 = reinterpret_cast<const float4*>(lse16)[i4];
+          const float4 e4 = reinterpret_cast<const float4*>(eta)[i4];
+          const unsigned char kf[4] = {kf4.x, kf4.y, kf4.z, kf4.w};
+          const float a8[4] = {l8.x, l8.y, l8.z, l8.w}, a16[4] = {l16.x, l16.y, l16.z, l16.w};
+          const float ee[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            if (4 * i4 + j < nb)
+              keys[4 * i4 + j] = __float_as_uint(expf((kf[j] ? a16[j] : a8[j]) - LSEp) * ee[j] / e_val);
+        }
         __syncthreads();
         unsigned long long taken = 0;
         block_select_top(nb, keys, fixed62(need), [&](int i) { v1[i] = 1; }, ws, &taken);
