@@ -14,7 +14,9 @@
 // tokens are the MMA rows, channels the k dimension and the eight
 // MMA columns hold the four query heads twice, as the high and low fp16 halves of the
 // exact fp32 product q_c s_{b,c} (scaled by a power of two), so the f16 MMA reproduces
-// the fp32 product exactly.  The INT8 codes convert to f16 exactly in registers.
+// the fp32 product exactly.  The 512 products of a block are formed once per warp (16 per
+// lane) and exchanged through shared memory in B-fragment order.  The INT8 codes convert
+// to f16 exactly in registers.
 //
 // A second kernel (one CTA per sequence and query head) selects, per query head,
 // the fewest blocks covering tau_cov of exp(lse8_b - LSE) (descending mass, ties to the
@@ -44,16 +46,25 @@ __device__ __forceinline__ size_t head_row(const LayerView& V, int b, int g, int
 // is read once, so the copies carry an L2 evict-first hint.
 constexpr int SCORE_CTAS_PER_SM = 4;
 constexpr int SCORE_STAGES = 2;
+// B words of one block: [head][hi, lo][channel pair], a pair index j stored at
+// j + 4 (j / 16) and the lo row 80 words after the hi row, so that the eight lanes of a
+// quarter warp read disjoint banks.
+constexpr int BW_ROW = 80;
+constexpr int BW_HEAD = 2 * BW_ROW;
+constexpr int BW_WORDS = MAXREP * BW_HEAD;   // per warp
 
 struct __align__(16) ScoreHalf {   // row tiles 2h, 2h+1 of a block; the scales with h = 0
   uint4 codes[256];
   uint4 scales[16];
 };
 
-__device__ __forceinline__ void cp_async16_evict_first(void* dst_smem, const void* src) {
-  const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
+__device__ __forceinline__ unsigned long long evict_first_policy() {
   unsigned long long pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void cp_async16_hint(void* dst_smem, const void* src, unsigned long long pol) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
                :: "r"(d), "l"(src), "l"(pol) : "memory");
 }
@@ -61,15 +72,23 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
 __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView V) {
   extern __shared__ __align__(16) unsigned char score_dsm[];
-  ScoreHalf* ring = reinterpret_cast<ScoreHalf*>(score_dsm) + (threadIdx.x >> 5) * SCORE_STAGES;
+  const int warp = threadIdx.x >> 5;
+  ScoreHalf* ring = reinterpret_cast<ScoreHalf*>(score_dsm) + warp * SCORE_STAGES;
+  uint32_t* bw = reinterpret_cast<uint32_t*>(score_dsm + sizeof(ScoreHalf) * SCORE_STAGES * 4) + warp * BW_WORDS;
   pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
+  const int hp = lane >> 3, sub = lane & 7;   // product role: head hp, channels 16 sub + [0, 16)
+  const unsigned long long pol = evict_first_policy();
   const long long total = (long long)V.BG * V.nb;
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long wid = (long long)blockIdx.x * (blockDim.x >> 5) + warp;
   const long long per = (total + nwarps - 1) / nwarps;
   const long long g0 = wid * per;
   const int count = (int)max(0ll, min(total, g0 + per) - g0);
@@ -85,9 +104,9 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
       ScoreHalf& st = ring[u % SCORE_STAGES];
       const uint4* kp = reinterpret_cast<const uint4*>(V.kc + pbi * KC_BYTES) + 256 * h;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) cp_async16_evict_first(&st.codes[lane + 32 * j], kp + lane + 32 * j);
+      for (int j = 0; j < 8; ++j) cp_async16_hint(&st.codes[lane + 32 * j], kp + lane + 32 * j, pol);
       if (h == 0 && lane < 16)
-        cp_async16_evict_first(&st.scales[lane], reinterpret_cast<const uint4*>(V.ks + pbi * D) + lane);
+        cp_async16_hint(&st.scales[lane], reinterpret_cast<const uint4*>(V.ks + pbi * D) + lane, pol);
       if (h == 1) ++pblk;
     }
     cp_async_commit();
@@ -96,8 +115,8 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
   for (int u = 0; u < SCORE_STAGES - 1; ++u) issue(u);
 
   int cur_hs = -1;
-  __half2 qh2[16];                  // q of head gid>>1 at channels 32tig + [0, 32)
-  float pre = 1.f, inv_pre = 1.f;   // 2^e of head gid>>1 and its inverse
+  float2 qp2[8];                    // q 2^e of head hp at channels 16 sub + [0, 16) (exact)
+  float inv_pre = 1.f;              // 2^-e of head hp
   float sc_out = 0.f;               // output scale of head tig
   // the group's queries: max |q| per head, this lane's slice, the power-of-two prescale
   auto setup_q = [&](int hs_q) {
@@ -116,35 +135,31 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
       }
       qm[r] = warp_max(m);
     }
-    const int r = gid >> 1;
     float qmr = 0.f, qmt = 0.f;
 #pragma unroll
     for (int k = 0; k < MAXREP; ++k) {
-      qmr = (k == r) ? qm[k] : qmr;
+      qmr = (k == hp) ? qm[k] : qmr;
       qmt = (k == tig) ? qm[k] : qmt;
     }
-    if (r < V.n_rep) {
-      const uint4* qp = reinterpret_cast<const uint4*>(V.q + (size_t)(hrow + r) * D + 32 * tig);
+    if (hp < V.n_rep) {
+      const float pre = prescale_for(qmr * smax);
+      const uint4* qp = reinterpret_cast<const uint4*>(V.q + (size_t)(hrow + hp) * D + 16 * sub);
+      const uint4 u0 = qp[0], u1 = qp[1];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint4 u = qp[i];
-        qh2[4 * i] = u32_as_h2(u.x); qh2[4 * i + 1] = u32_as_h2(u.y);
-        qh2[4 * i + 2] = u32_as_h2(u.z); qh2[4 * i + 3] = u32_as_h2(u.w);
-      }
-      pre = prescale_for(qmr * smax);
+      for (int i = 0; i < 8; ++i)
+        qp2[i] = mul2(__half22float2(u32_as_h2(word_of(i < 4 ? u0 : u1, i & 3))), make_float2(pre, pre));
+      inv_pre = 1.f / pre;
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) qh2[i] = __float2half2_rn(0.f);
-      pre = 1.f;
+      for (int i = 0; i < 8; ++i) qp2[i] = make_float2(0.f, 0.f);
+      inv_pre = 1.f;
     }
-    inv_pre = 1.f / pre;
     sc_out = (tig < V.n_rep) ? INV_SQRT_D / prescale_for(qmt * smax) : 0.f;
   };
   if (units > 0) setup_q((int)(g0 / V.nb));   // overlaps the first copy
 
   int hs = (int)(g0 / V.nb), blk = (int)(g0 % V.nb) - 1;
   uint32_t bf[16];
-  float dp = 0.f;
   float x[8];
   for (int u = 0; u < units; ++u) {
     issue(u + SCORE_STAGES - 1);
@@ -155,44 +170,61 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
     if (h == 0) {
       if (++blk == V.nb) { blk = 0; ++hs; }
       if (hs != cur_hs) setup_q(hs);
-      // B fragments for k-steps 0..7: channels 32tig + 4kk + {0,1} (b0) and {2,3} (b1),
-      // column gid = (head gid>>1, hi or lo half of q_c s_c 2^e)
-      dp = 0.f;
-      const uint4 Sv[4] = {cur.scales[4 * tig], cur.scales[4 * tig + 1], cur.scales[4 * tig + 2],
-                           cur.scales[4 * tig + 3]};
+      // products q_c s_c 2^e of head hp at channels 16 sub + [0, 16), split hi + lo
+      const uint4 S0 = cur.scales[2 * sub], S1 = cur.scales[2 * sub + 1];
+      uint32_t hw[8], lw[8];
+      float dp = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const uint32_t sw = (i & 3) == 0 ? Sv[i >> 2].x : (i & 3) == 1 ? Sv[i >> 2].y : (i & 3) == 2 ? Sv[i >> 2].z : Sv[i >> 2].w;
-        const float2 s2 = __half22float2(u32_as_h2(sw));
-        const float2 q2 = __half22float2(qh2[i]);
-        const float2 w = mul2(mul2(q2, make_float2(pre, pre)), s2);   // exact products
+      for (int i = 0; i < 8; ++i) {
+        const float2 s2 = __half22float2(u32_as_h2(word_of(i < 4 ? S0 : S1, i & 3)));
+        const float2 w = mul2(qp2[i], s2);                            // exact products
         dp += fabsf(w.x) + fabsf(w.y);
         const __half2 hi = __floats2half2_rn(w.x, w.y);
         const float2 rem = sub2(w, __half22float2(hi));               // exact remainders
-        const __half2 lo = __floats2half2_rn(rem.x, rem.y);
-        bf[i] = (gid & 1) ? h2_as_u32(lo) : h2_as_u32(hi);
+        hw[i] = h2_as_u32(hi);
+        lw[i] = h2_as_u32(__floats2half2_rn(rem.x, rem.y));
+      }
+      {   // pairs 8 sub + [0, 8) at 8 sub + 4 (sub / 2) + [0, 8)
+        uint32_t* ph = bw + hp * BW_HEAD + 8 * sub + 4 * (sub >> 1);
+        *reinterpret_cast<uint4*>(ph) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(ph + 4) = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        *reinterpret_cast<uint4*>(ph + BW_ROW) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        *reinterpret_cast<uint4*>(ph + BW_ROW + 4) = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+      }
+      dp += __shfl_xor_sync(0xffffffffu, dp, 1);   // sum_c |q_c| s_c 2^e of head hp
+      dp += __shfl_xor_sync(0xffffffffu, dp, 2);
+      dp += __shfl_xor_sync(0xffffffffu, dp, 4);
+      if (sub == 0 && hp < V.n_rep)
+        V.delta[(size_t)(hs * V.n_rep + hp) * V.nbmax + blk] = KAPPA * INV_SQRT_D * (dp * inv_pre);
+      __syncwarp();
+      // B fragments of column gid = (head gid>>1, hi or lo): k-step kk takes pairs
+      // 16 tig + 2kk (channels 32tig + 4kk + {0,1}) and 16 tig + 2kk + 1 ({2,3})
+      const uint4* pb = reinterpret_cast<const uint4*>(bw + (gid >> 1) * BW_HEAD + (gid & 1) * BW_ROW + 20 * tig);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint4 v = pb[m];
+        bf[4 * m] = v.x; bf[4 * m + 1] = v.y; bf[4 * m + 2] = v.z; bf[4 * m + 3] = v.w;
       }
     }
 #pragma unroll
     for (int ww = 0; ww < 2; ++ww) {     // MMA row tile 2h + ww: tokens 16(2h + ww) + [0, 16)
       const uint4 R0 = cur.codes[lane + 128 * ww], R1 = cur.codes[lane + 128 * ww + 32];
       const uint4 R2 = cur.codes[lane + 128 * ww + 64], R3 = cur.codes[lane + 128 * ww + 96];
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // two chains: k-steps 0-3, 4-7
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         const uint4& ra = (kk < 4) ? R0 : R1;
         const uint4& rb = (kk < 4) ? R2 : R3;
-        const int wi = kk & 3;
-        const uint32_t wa = (wi == 0) ? ra.x : (wi == 1) ? ra.y : (wi == 2) ? ra.z : ra.w;
-        const uint32_t wb = (wi == 0) ? rb.x : (wi == 1) ? rb.y : (wi == 2) ? rb.z : rb.w;
+        const uint32_t wa = word_of(ra, kk & 3), wb = word_of(rb, kk & 3);
         uint32_t a0, a2, a1, a3;
         i8x4_to_f16(wa, a0, a2);
         i8x4_to_f16(wb, a1, a3);
-        mma16816(acc, a0, a1, a2, a3, bf[2 * kk], bf[2 * kk + 1]);
+        mma16816(acc[kk >> 2], a0, a1, a2, a3, bf[2 * kk], bf[2 * kk + 1]);
       }
       // head tig, tokens 16w + gid and 16w + gid + 8 (w = 2h + ww)
-      const float2 xs = mul2(add2(make_float2(acc[0], acc[2]), make_float2(acc[1], acc[3])),
-                             make_float2(sc_out, sc_out));
+      const float2 c0 = add2(make_float2(acc[0][0], acc[0][2]), make_float2(acc[0][1], acc[0][3]));
+      const float2 c1 = add2(make_float2(acc[1][0], acc[1][2]), make_float2(acc[1][1], acc[1][3]));
+      const float2 xs = mul2(add2(c0, c1), make_float2(sc_out, sc_out));
       if (h == 0) { x[2 * ww] = xs.x; x[2 * ww + 1] = xs.y; }
       else { x[4 + 2 * ww] = xs.x; x[5 + 2 * ww] = xs.y; }
     }
@@ -220,14 +252,9 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
       l += __shfl_xor_sync(0xffffffffu, l, 4);
       l += __shfl_xor_sync(0xffffffffu, l, 8);
       l += __shfl_xor_sync(0xffffffffu, l, 16);
-      float d2 = dp;
-      d2 += __shfl_xor_sync(0xffffffffu, d2, 1);
-      d2 += __shfl_xor_sync(0xffffffffu, d2, 2);
-      // lane tig (gid 0) holds lse of head tig; lane 8r (tig 0, gid 2r) holds Delta of head r
+      // lane tig (gid 0) holds lse of head tig
       if (gid == 0 && tig < V.n_rep)
         V.lse8[(size_t)(hrow + tig) * V.nbmax + blk] = m + logf(l);
-      if (tig == 0 && (gid & 1) == 0 && (gid >> 1) < V.n_rep)
-        V.delta[(size_t)(hrow + (gid >> 1)) * V.nbmax + blk] = KAPPA * INV_SQRT_D * (d2 * inv_pre);
     }
   }
   cp_async_wait<0>();
@@ -367,7 +394,7 @@ cudaError_t launch_score(const LayerView& V, int grid, cudaStream_t st) {
   const long long total = (long long)V.BG * V.nb;
   if (total == 0) return cudaSuccess;   // nothing to score (only a partial block)
   if ((long long)grid * 4 > total) grid = (int)((total + 3) / 4);
-  const size_t dyn = sizeof(ScoreHalf) * SCORE_STAGES * 4;   // 4 warps
+  const size_t dyn = (sizeof(ScoreHalf) * SCORE_STAGES + BW_WORDS * 4) * 4;   // 4 warps
   cudaError_t e = cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
   score_kernel<<<grid, 128, dyn, st>>>(V);
