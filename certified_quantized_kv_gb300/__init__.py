@@ -46,7 +46,7 @@ class kvq_config(ctypes.Structure):
         ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("block_tokens", ctypes.c_int),
         ("value_group", ctypes.c_int), ("max_ctx", ctypes.c_int), ("rank_positions", ctypes.c_int),
         ("l4_head_fraction", ctypes.c_float), ("value_bits", ctypes.c_int),
-        ("v_tol", ctypes.c_float),
+        ("v_tol", ctypes.c_float), ("resident_blocks", ctypes.c_int),
     ]
 
 
@@ -82,6 +82,8 @@ def load_library() -> ctypes.CDLL:
         "kvq_export_decode_state": [vp, vp, vp, vp, vp, vp, vp, vp],
         "kvq_profile_read": [vp, ctypes.POINTER(kvq_kernel_stat), i32, ctypes.POINTER(i32), i32],
         "kvq_dense_decode_noalloc": [vp, vp, vp, i32, i32, i32, i32, vp, vp],
+        "kvq_residency_stats": [vp, i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
+                                ctypes.POINTER(i32), i32],
     }
     for name, argt in sigs.items():
         fn = getattr(lib, name)
@@ -122,11 +124,11 @@ class Cache:
 
     def __init__(self, n_layers, batch, n_q_heads, n_kv_heads, max_ctx, rank_positions=1,
                  l4_head_fraction=0.5, head_dim=HEAD_DIM, block_tokens=BLOCK,
-                 value_group=VALUE_GROUP, value_bits=4, v_tol=0.0):
+                 value_group=VALUE_GROUP, value_bits=4, v_tol=0.0, resident_blocks=0):
         self.lib = load_library()
         self.cfg = kvq_config(n_layers, batch, n_q_heads, n_kv_heads, head_dim, block_tokens,
                               value_group, max_ctx, rank_positions, l4_head_fraction, value_bits,
-                              v_tol)
+                              v_tol, resident_blocks)
         self.value_bits = value_bits
         h = ctypes.c_void_p()
         _check(self.lib.kvq_cache_create(ctypes.byref(self.cfg), ctypes.byref(h)))
@@ -213,6 +215,14 @@ class Cache:
                                                 _ptr(o["kprom1"]), _ptr(o["vprom1"]), _ptr(o["lse8"]),
                                                 _ptr(o["delta"]), _stream(stream)))
         return o
+
+    def residency_stats(self, layer: int, reset: bool = False) -> dict:
+        """FP16 block bytes of `layer` served from resident HBM copies and read over the
+        host link since the last reset, and the slots in use (kvq_residency_stats)."""
+        hit, host, used = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int()
+        _check(self.lib.kvq_residency_stats(self.handle, layer, ctypes.byref(hit), ctypes.byref(host),
+                                            ctypes.byref(used), int(reset)))
+        return {"resident_bytes": hit.value, "host_bytes": host.value, "slots_in_use": used.value}
 
     def profile_read(self, reset: bool = True) -> dict:
         arr = (kvq_kernel_stat * 16)()

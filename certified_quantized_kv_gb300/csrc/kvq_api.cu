@@ -49,10 +49,10 @@ __global__ void fill_u32(uint32_t* p, uint32_t v, size_t n) {
 }
 
 enum KernelId { K_SCORE = 0, K_SELECT, K_MIX0, K_COMB0, K_MIX1, K_COMB1, K_DENSE, K_FINAL,
-                K_APPEND, K_TAIL, K_COUNT };
+                K_APPEND, K_TAIL, K_RESIDENT, K_COUNT };
 const char* kKernelNames[K_COUNT] = {"score", "select", "mixed_round0", "combine_round0",
                                      "mixed_round1", "combine_round1", "dense_fallback",
-                                     "finalize", "quantize_append", "int4_tail"};
+                                     "finalize", "quantize_append", "int4_tail", "residency"};
 
 }  // namespace
 
@@ -88,6 +88,12 @@ struct kvq_cache {
   __half *q_stage = nullptr, *out_stage = nullptr;
   kvq_certificate* cert_stage = nullptr;
   int32_t* level_stage = nullptr;
+  // cross-step residency of FP16 tier-2 blocks, all layers in one allocation
+  int nres = 0;
+  char* res = nullptr;
+  size_t res_layer = 0, off_rk = 0, off_rv = 0, off_rown = 0, off_rstamp = 0, off_rfree = 0,
+         off_rstate = 0, off_rbytes = 0, off_rpool = 0;
+  std::vector<unsigned int> call_id;   // certified decode calls per layer
   cudaStream_t side = nullptr;
   cudaEvent_t ev_in = nullptr, ev_mirror = nullptr;
   int debug = 0;
@@ -206,6 +212,7 @@ void free_all(kvq_cache* c) {
   for (auto e : c->ev_pool) cudaEventDestroy(e);
   if (c->t1) cudaFree(c->t1);
   if (c->scr) cudaFree(c->scr);
+  if (c->res) cudaFree(c->res);
   for (auto p : c->t2k_host) if (p) cudaFreeHost(p);
   for (auto p : c->t2v_host) if (p) cudaFreeHost(p);
   if (c->side) cudaStreamDestroy(c->side);
@@ -252,6 +259,7 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   if (k.value_bits != 0 && k.value_bits != 4 && k.value_bits != 16)
     return fail(KVQ_ERR_INVALID, "value_bits must be 4 (or 0) or 16");
   if (!(k.v_tol >= 0.f)) return fail(KVQ_ERR_INVALID, "v_tol must be >= 0 (0: no value budget)");
+  if (k.resident_blocks < 0) return fail(KVQ_ERR_INVALID, "resident_blocks must be >= 0");
 
   kvq_cache* c = new kvq_cache();
   c->cfg = k;
@@ -368,6 +376,40 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   c->out_stage = reinterpret_cast<__half*>(c->scr + s_out);
   c->cert_stage = reinterpret_cast<kvq_certificate*>(c->scr + s_cert);
   c->level_stage = reinterpret_cast<int32_t*>(c->scr + s_lvl);
+
+  // ---- cross-step residency (resident_blocks slots of 16 KiB per layer) ----
+  c->call_id.assign(c->L, 0u);
+  c->nres = k.resident_blocks;
+  if (c->nres > 0) {
+    if ((size_t)BG * nbm >= (1u << 30))
+      { free_all(c); return fail(KVQ_ERR_INVALID, "resident_blocks: cache too large for the slot table"); }
+    const size_t S = (size_t)c->nres;
+    o = 0;
+    c->off_rk = o;     o = align_up(o + BG * nbm * 4, 256);
+    c->off_rv = o;     o = align_up(o + BG * nbm * 4, 256);
+    c->off_rown = o;   o = align_up(o + S * 4, 256);
+    c->off_rstamp = o; o = align_up(o + S * 4, 256);
+    c->off_rfree = o;  o = align_up(o + S * 4, 256);
+    c->off_rstate = o; o = align_up(o + RS_WORDS * 4, 256);
+    c->off_rbytes = o; o = align_up(o + 2 * 8, 256);
+    c->off_rpool = o;  o = align_up(o + S * F16_BLOCK_BYTES, 256);
+    c->res_layer = o;
+    if (cudaMalloc(&c->res, c->res_layer * c->L) != cudaSuccess) {
+      cudaGetLastError();
+      free_all(c);
+      return fail(KVQ_ERR_OOM, "residency device allocation failed");
+    }
+    for (int l = 0; l < c->L; ++l) {
+      char* r = c->res + c->res_layer * l;
+      cudaMemset(r + c->off_rk, 0xff, BG * nbm * 4);   // -1: not resident
+      cudaMemset(r + c->off_rv, 0xff, BG * nbm * 4);
+      const unsigned int st0[RS_WORDS] = {(unsigned int)S, 0u, 0u, 0u};
+      cudaMemcpy(r + c->off_rstate, st0, sizeof st0, cudaMemcpyHostToDevice);
+      cudaMemset(r + c->off_rbytes, 0, 16);
+      launch_residency_init(reinterpret_cast<int*>(r + c->off_rfree), reinterpret_cast<int*>(r + c->off_rown),
+                            reinterpret_cast<unsigned int*>(r + c->off_rstamp), c->nres, 0);
+    }
+  }
 
   if (cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking) != cudaSuccess ||
       cudaEventCreateWithFlags(&c->ev_in, cudaEventDisableTiming) != cudaSuccess ||
@@ -531,6 +573,22 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   V.kprom0 = c->kprom0; V.kprom1 = c->kprom1; V.vprom1 = c->vprom1;
   V.hst = c->hst; V.gst = c->gst; V.part = c->part; V.dpart = c->dpart; V.counters = c->counters;
   V.part1 = c->part1; V.red0 = c->red0;
+  V.nres = 0; V.call_id = 0u;
+  V.rslot_k = V.rslot_v = nullptr; V.rpool = nullptr; V.rowner = nullptr; V.rstamp = nullptr;
+  V.rfree = nullptr; V.rstate = nullptr; V.rbytes = nullptr;
+  if (certified && c->nres > 0) {   // only certified calls page FP16 blocks in
+    char* r = c->res + c->res_layer * layer;
+    V.nres = c->nres;
+    V.call_id = ++c->call_id[layer];
+    V.rslot_k = reinterpret_cast<int*>(r + c->off_rk);
+    V.rslot_v = reinterpret_cast<int*>(r + c->off_rv);
+    V.rowner = reinterpret_cast<int*>(r + c->off_rown);
+    V.rstamp = reinterpret_cast<unsigned int*>(r + c->off_rstamp);
+    V.rfree = reinterpret_cast<int*>(r + c->off_rfree);
+    V.rstate = reinterpret_cast<unsigned int*>(r + c->off_rstate);
+    V.rbytes = reinterpret_cast<unsigned long long*>(r + c->off_rbytes);
+    V.rpool = reinterpret_cast<__half*>(r + c->off_rpool);
+  }
 
   const bool all_dense = certified && ((tau >= 1.f) || (c->debug & KVQ_DEBUG_FORCE_DENSE));
   if (!all_dense) {
@@ -557,6 +615,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
     KVQ_CUDA(s.done(launch_dense(V, all_dense ? 1 : 0, dense_grid(c->num_sms), st)), "dense_fallback");
   }
   { KernelScope s(c, K_FINAL, st); KVQ_CUDA(s.done(launch_finalize(V, cd, ld, st)), "finalize"); }
+  if (V.nres > 0) { KernelScope s(c, K_RESIDENT, st); KVQ_CUDA(s.done(launch_residency(V, st)), "residency"); }
 
   if (!out_dev) KVQ_CUDA(cudaMemcpyAsync(out, od, HQ * D * 2, cudaMemcpyDeviceToHost, st), "copy out");
   if (cert && !cert_dev) KVQ_CUDA(cudaMemcpyAsync(cert, cd, HQ * sizeof(kvq_certificate), cudaMemcpyDeviceToHost, st), "copy cert");
@@ -629,6 +688,26 @@ kvq_status kvq_profile_read(kvq_cache* c, kvq_kernel_stat* stats, int max, int* 
   if (reset) {
     for (int i = 0; i < K_COUNT; ++i) { c->prof_ms[i] = 0; c->prof_n[i] = 0; }
   }
+  return KVQ_OK;
+}
+
+kvq_status kvq_residency_stats(kvq_cache* c, int layer, int64_t* resident_bytes,
+                               int64_t* host_bytes, int32_t* slots_in_use, int reset) {
+  if (!c) return fail(KVQ_ERR_INVALID, "kvq_residency_stats: NULL cache");
+  if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, "kvq_residency_stats: layer out of range");
+  DeviceGuard dg(c->device);
+  unsigned long long b[2] = {0ull, 0ull};
+  unsigned int stt[RS_WORDS] = {0u, 0u, 0u, 0u};
+  if (c->nres > 0) {
+    char* r = c->res + c->res_layer * layer;
+    KVQ_CUDA(cudaDeviceSynchronize(), "kvq_residency_stats: sync");
+    KVQ_CUDA(cudaMemcpy(b, r + c->off_rbytes, sizeof b, cudaMemcpyDeviceToHost), "kvq_residency_stats: read");
+    KVQ_CUDA(cudaMemcpy(stt, r + c->off_rstate, sizeof stt, cudaMemcpyDeviceToHost), "kvq_residency_stats: read");
+    if (reset) KVQ_CUDA(cudaMemset(r + c->off_rbytes, 0, sizeof b), "kvq_residency_stats: reset");
+  }
+  if (resident_bytes) *resident_bytes = (int64_t)b[0];
+  if (host_bytes) *host_bytes = (int64_t)b[1];
+  if (slots_in_use) *slots_in_use = (int32_t)stt[RS_USED];
   return KVQ_OK;
 }
 

@@ -115,7 +115,24 @@ struct LayerView {
   float* red0;           // [B*Hq][D+4] the first pass's partials summed (channels, then l)
   float* dpart;          // [BG][nslot][MAXREP][D+4] partials of the dense pass
   unsigned int* counters;  // work queues and completion counters (self-resetting)
+  // cross-step residency of FP16 tier-2 blocks in HBM (nres == 0: off)
+  int nres;              // slots of this layer
+  unsigned int call_id;  // certified decode calls of this layer so far (stamps slot use)
+  int* rslot_k;          // [BG][nbmax] slot holding the block's keys, or -1
+  int* rslot_v;          // [BG][nbmax] slot holding the block's values, or -1
+  __half* rpool;         // [nres][64][128]
+  int* rowner;           // [nres] (kv << 30) | (hs * nbmax + blk), or -1
+  unsigned int* rstamp;  // [nres] call_id of the last call that used the slot
+  int* rfree;            // [nres] free slots (the first rstate[RS_NFREE] entries)
+  unsigned int* rstate;  // RS_* below
+  unsigned long long* rbytes;  // [2] bytes served from slots, bytes read over the host link
 };
+
+// residency state words
+constexpr int RS_NFREE = 0;   // free slots at the start of the call
+constexpr int RS_TAKEN = 1;   // free-list entries claimed during the call
+constexpr int RS_USED = 2;    // slots holding a block after the last eviction pass
+constexpr int RS_WORDS = 4;
 
 // counters layout
 constexpr int CNT_MIX_Q = 2;

@@ -18,6 +18,7 @@
 // reused and only the values cross the link.
 #include "kvq_common.cuh"
 #include "kvq_launch.h"
+#include "kvq_resident.cuh"
 #include "kvq.h"
 
 namespace kvq {
@@ -33,6 +34,7 @@ struct __align__(16) DenseSmem {
   int item;
   int mask;
   int is_last;
+  int res[4];   // residency picks: keys [0..1], values [2..3]
 };
 
 __device__ __forceinline__ size_t head_row(const LayerView& V, int b, int g, int r) {
@@ -172,10 +174,16 @@ __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) 
       // FP16 keys this call already paged in: their exact scores are in the score scratch
       const bool have_s = !all_dense && V.kprom1[(size_t)hs * V.nbmax + blk];
       {
-        // all sixteen 16-byte loads of a thread in flight before the first store
-        const uint4* ks = reinterpret_cast<const uint4*>(V.t2k + src);
+        // tier 2 or the blocks' resident copies; all sixteen 16-byte loads of a thread in
+        // flight before the first store
+        const size_t bi = (size_t)hs * V.nbmax + blk;
+        const ResPick pk = have_s ? ResPick{-1, -1} : res_pick(V, 0, bi, sm.res);
+        const ResPick pv = V.v16 ? ResPick{-1, -1} : res_pick(V, 1, bi, sm.res + 2);
+        const uint4* ks = reinterpret_cast<const uint4*>(res_src(V, pk, V.t2k + src));
         const uint4* vs = reinterpret_cast<const uint4*>(
-            V.v16 ? V.v16 + ((size_t)hs * V.nbmax + blk) * (BLK * D) : V.t2v + src);   // FP16 values
+            V.v16 ? V.v16 + bi * (BLK * D) : res_src(V, pv, V.t2v + src));   // FP16 values
+        uint4* kcopy = reinterpret_cast<uint4*>(res_dst(V, pk));
+        uint4* vcopy = reinterpret_cast<uint4*>(res_dst(V, pv));
         uint4 rk[8], rv[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -188,6 +196,16 @@ __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) 
           if (!have_s) *reinterpret_cast<uint4*>(&sm.kbuf[row][col]) = rk[j];
           *reinterpret_cast<uint4*>(&sm.vbuf[row][col]) = rv[j];
         }
+        if (kcopy) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) kcopy[tid + 128 * j] = rk[j];
+        }
+        if (vcopy) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) vcopy[tid + 128 * j] = rv[j];
+        }
+        res_commit(V, 0, bi, pk);
+        res_commit(V, 1, bi, pv);
       }
       __syncthreads();
       if (have_s) {

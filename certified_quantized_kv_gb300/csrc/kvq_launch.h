@@ -58,4 +58,8 @@ cudaError_t launch_dense(const LayerView& V, int all_dense, int grid, cudaStream
 cudaError_t launch_finalize(const LayerView& V, kvq_certificate* cert, int32_t* level,
                             cudaStream_t st);
 
+// Cross-step residency of FP16 tier-2 blocks (kvq_resident.cu).
+cudaError_t launch_residency(const LayerView& V, cudaStream_t st);
+cudaError_t launch_residency_init(int* rfree, int* rowner, unsigned int* rstamp, int n, cudaStream_t st);
+
 }  // namespace kvq

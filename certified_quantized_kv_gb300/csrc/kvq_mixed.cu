@@ -31,6 +31,7 @@
 #include "kvq_common.cuh"
 #include "kvq_blocksel.cuh"
 #include "kvq_launch.h"
+#include "kvq_resident.cuh"
 
 namespace kvq {
 
@@ -49,6 +50,7 @@ struct __align__(16) MixSmem {
   } st;
   int item;
   int skip;
+  int res[4];                 // residency picks: keys [0..1], values [2..3]
 };
 
 
@@ -63,11 +65,12 @@ __device__ __forceinline__ unsigned long long fixed62(double x) {
   return (unsigned long long)(x * 4611686018427387904.0);
 }
 
-// Copy one FP16 block (64 x 128, 16 KiB) from tier 2 into shared memory rows of `stride`
-// halves (128 threads).  A thread issues all eight of its 16-byte loads before the first
-// store, so the block costs one host-link round trip instead of eight.
+// Copy one FP16 block (64 x 128, 16 KiB) from tier 2 (or its resident copy) into shared
+// memory rows of `stride` halves (128 threads), and into `copy` (a free resident slot)
+// when given.  A thread issues all eight of its 16-byte loads before the first store, so
+// the block costs one host-link round trip instead of eight.
 template <int STRIDE>
-__device__ __forceinline__ void load_f16_block(__half* dst, const __half* src) {
+__device__ __forceinline__ void load_f16_block(__half* dst, const __half* src, __half* copy) {
   const uint4* s = reinterpret_cast<const uint4*>(src);
   uint4 r[8];
 #pragma unroll
@@ -76,6 +79,10 @@ __device__ __forceinline__ void load_f16_block(__half* dst, const __half* src) {
   for (int j = 0; j < 8; ++j) {
     const int i = threadIdx.x + 128 * j, row = i >> 4, col = (i & 15) * 8;
     *reinterpret_cast<uint4*>(dst + row * STRIDE + col) = r[j];
+  }
+  if (copy) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) reinterpret_cast<uint4*>(copy)[threadIdx.x + 128 * j] = r[j];
   }
 }
 
@@ -160,7 +167,11 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
       }
       float sn0 = so0, sn1 = so1;
       if (need_k16) {
-        load_f16_block<KROW>(&sm.st.kbuf[0][0], V.t2k + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
+        const ResPick pk = res_pick(V, 0, bi, sm.res);
+        load_f16_block<KROW>(&sm.st.kbuf[0][0],
+                             res_src(V, pk, V.t2k + ((size_t)hs * V.cap + (size_t)blk * BLK) * D),
+                             res_dst(V, pk));
+        res_commit(V, 0, bi, pk);
         __syncthreads();
         {
           const int t = tid & 63, rp = (tid >> 6) * 2;  // heads rp, rp+1
@@ -259,8 +270,12 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
         }
       }
       if (use16) {
-        load_f16_block<D>(&sm.st.vbuf[0][0], v16 ? V.v16 + bi * (BLK * D)
-                                                 : V.t2v + ((size_t)hs * V.cap + (size_t)blk * BLK) * D);
+        const ResPick pv = v16 ? ResPick{-1, -1} : res_pick(V, 1, bi, sm.res + 2);
+        load_f16_block<D>(&sm.st.vbuf[0][0],
+                          v16 ? V.v16 + bi * (BLK * D)
+                              : res_src(V, pv, V.t2v + ((size_t)hs * V.cap + (size_t)blk * BLK) * D),
+                          res_dst(V, pv));
+        res_commit(V, 1, bi, pv);
         __syncthreads();
         const int c0 = 32 * warp + gid;
         const float* pr = sm.pn[par][tig];

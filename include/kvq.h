@@ -77,6 +77,16 @@ typedef struct kvq_config {
                               v_tol, and rung 2 pages in values until it holds (the paper's
                               v_tol, Results: structured reasoning).  0 (or +inf): no budget
                               beyond eps.  Must not be negative or NaN. */
+  int resident_blocks;     /* cross-step residency (not part of the paper: an option of
+                              this library).  Each layer may keep up to this many FP16
+                              tier-2 blocks (keys or values, 16 KiB each) in device memory
+                              across decode calls, so that a block paged in again by a
+                              later call is read from HBM instead of over the host link.
+                              A block read from tier 2 takes a free slot if one is left;
+                              after each certified call the slots its layer did not use in
+                              that call are freed.  Outputs and certificates are unchanged
+                              (the copies are bit-identical).  Costs resident_blocks x
+                              16 KiB of device memory per layer.  0 (the default): none. */
 } kvq_config;
 
 /* Per-head certificate of one decode call (Method §2, §3). */
@@ -88,8 +98,10 @@ typedef struct kvq_certificate {
                               2 values promoted, 3 per-head dense, 4 per-layer dense */
   int32_t k_star;          /* blocks selected for this head by the top-K* pass */
   int32_t n_val_promoted;  /* value blocks paged in for the head's certified result */
-  int64_t promoted_bytes;  /* tier-2 bytes read over the host link for this head's KV
-                              group during the call (same for all heads of the group) */
+  int64_t promoted_bytes;  /* FP16 tier-2 bytes paged in for this head's KV group during
+                              the call (same for all heads of the group).  With
+                              resident_blocks > 0 part of them may come from the resident
+                              copies in HBM (kvq_residency_stats) */
 } kvq_certificate;
 
 typedef struct kvq_cache kvq_cache;
@@ -201,6 +213,15 @@ typedef struct kvq_kernel_stat {
  * them afterwards.  Errors: KVQ_ERR_INVALID, KVQ_ERR_CUDA. */
 kvq_status kvq_profile_read(kvq_cache* cache, kvq_kernel_stat* stats, int max, int* n,
                             int reset);
+
+/* kvq_residency_stats -- FP16 block traffic of `layer`'s certified decode calls since the
+ * last reset (cross-step residency, see kvq_config.resident_blocks): bytes of tier-2
+ * blocks served from resident copies in device memory, bytes read over the host link,
+ * and the slots currently holding a block.  Any output pointer may be NULL; reset != 0
+ * clears the two byte counters.  Synchronises the device.
+ * Errors: KVQ_ERR_INVALID (NULL cache, layer out of range), KVQ_ERR_CUDA. */
+kvq_status kvq_residency_stats(kvq_cache* cache, int layer, int64_t* resident_bytes,
+                               int64_t* host_bytes, int32_t* slots_in_use, int reset);
 
 /* kvq_dense_decode_noalloc -- exact dense FP16 decode attention that allocates no memory.
  * The paper has no counterpart to this call.  It is for callers that cannot allocate

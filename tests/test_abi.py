@@ -54,3 +54,12 @@ def test_certificate_layout_matches_header():
     body = body[: body.index("} kvq_certificate;")]
     fields = [ln.split(";")[0].split()[-1] for ln in body.splitlines()[1:] if ";" in ln]
     assert fields == list(kvq.CERT_DTYPE.names)
+
+
+def test_resident_blocks_validated_without_gpu():
+    lib = _lib()
+    cfg = kvq.kvq_config(1, 1, 32, 8, 128, 64, 32, 1024, 1, 0.5, 4, 0.0, -1)   # resident_blocks < 0
+    h = ctypes.c_void_p()
+    assert lib.kvq_cache_create(ctypes.byref(cfg), ctypes.byref(h)) == kvq.KVQ_ERR_INVALID
+    assert b"resident_blocks" in lib.kvq_last_error()
+    assert lib.kvq_residency_stats(None, 0, None, None, None, 0) == kvq.KVQ_ERR_INVALID
