@@ -327,6 +327,77 @@ def measure_fp16_values(args, wl):
             "what": "value_bits 16: INT8 keys, FP16 values in VRAM, keys-only tier 2"}
 
 
+def measure_residency(args, wl, frac=0.25, layers=4):
+    """Cross-step residency of paged-in FP16 blocks (kvq_config.resident_blocks: an option
+    of this library, not of the paper), same timing protocol as the headline.
+    (1) The headline caches, `layers` layers, each allowed to keep `frac` of its FP16
+    tier-2 blocks (keys and values) in HBM.  (2) The concentrated 32K x 4 workload, with
+    and without room for its whole working set.  Warm-up calls fill the slots; the timed
+    calls report tokens/s/layer and the FP16 bytes read over the host link and from HBM."""
+    import torch
+    import certified_quantized_kv_gb300 as kvq
+    import workloads as W
+    B, N = wl["batch"], wl["ctx"]
+    Hq, Hkv, D = wl["q_heads"], wl["kv_heads"], wl["head_dim"]
+    tau, eps = wl["tau_cov"], wl["eps"]
+
+    def run(cache, qs, n_layers, batch):
+        out = torch.empty(batch, Hq, D, dtype=torch.float16, device="cuda")
+
+        def step():
+            for layer in range(n_layers):
+                cache.decode(layer, qs[layer], tau, eps, out)
+
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        for layer in range(n_layers):
+            cache.residency_stats(layer, reset=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            step()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        st = [cache.residency_stats(layer) for layer in range(n_layers)]
+        per = args.steps * n_layers
+        return {"value": batch * n_layers / (ms / 1e3), "unit": UNIT, "us_per_layer": 1e3 * ms / n_layers,
+                "host_bytes_per_layer": sum(x["host_bytes"] for x in st) / per,
+                "resident_bytes_per_layer": sum(x["resident_bytes"] for x in st) / per,
+                "slots_in_use_per_layer": sum(x["slots_in_use"] for x in st) / n_layers}
+
+    res = {}
+    nblk = B * Hkv * (N // 64) * 2
+    slots = int(frac * nblk)
+    cache = kvq.Cache(layers, B, Hq, Hkv, max_ctx=N, resident_blocks=slots)
+    qs = []
+    for layer in range(layers):
+        q, K, V = W.c3_layer(layer, device="cuda", seed=wl["seed"], batch=B, ctx=N, Hq=Hq, Hkv=Hkv)
+        cache.append(layer, K.contiguous(), V.contiguous())
+        qs.append(q.contiguous())
+        del K, V
+    r = run(cache, qs, layers, B)
+    cache.close()
+    r.update({"workload": f"{wl['name']} (first {layers} layers)", "resident_blocks": slots,
+              "resident_fraction_of_tier2": frac, "extra_vram_bytes_per_layer": slots * F16_BLOCK})
+    res["headline_shape"] = r
+    q, K, V = W.c2(device="cuda", batch=4, ctx=32768)
+    q = q.contiguous()
+    for slots in (0, 4 * Hkv * 512 * 2):
+        cache = kvq.Cache(1, 4, Hq, Hkv, max_ctx=32768, resident_blocks=slots)
+        cache.append(0, K.contiguous(), V.contiguous())
+        r = run(cache, [q], 1, 4)
+        cache.close()
+        r.update({"resident_blocks": slots, "extra_vram_bytes_per_layer": slots * F16_BLOCK})
+        res[f"c2_ctx32k_b4_slots{slots}"] = r
+    del K, V
+    res["what"] = ("FP16 blocks paged in by one call kept in HBM for the next (not part of the paper); "
+                   "outputs and certificates are bit-identical to the cache without residency")
+    return res
+
+
+
 def our_arm(args, wl):
     import torch
     import torch.distributed as dist
@@ -528,6 +599,7 @@ def our_arm(args, wl):
                                     "sample": f"failed: {e}"[:200]}
     cache.close()
     line["fp16_values"] = measure_fp16_values(args, wl)
+    line["residency"] = measure_residency(args, wl)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

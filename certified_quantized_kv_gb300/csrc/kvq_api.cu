@@ -403,7 +403,7 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
       char* r = c->res + c->res_layer * l;
       cudaMemset(r + c->off_rk, 0xff, BG * nbm * 4);   // -1: not resident
       cudaMemset(r + c->off_rv, 0xff, BG * nbm * 4);
-      const unsigned int st0[RS_WORDS] = {(unsigned int)S, 0u, 0u, 0u};
+      const unsigned int st0[RS_WORDS] = {(unsigned int)S, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
       cudaMemcpy(r + c->off_rstate, st0, sizeof st0, cudaMemcpyHostToDevice);
       cudaMemset(r + c->off_rbytes, 0, 16);
       launch_residency_init(reinterpret_cast<int*>(r + c->off_rfree), reinterpret_cast<int*>(r + c->off_rown),
@@ -697,7 +697,7 @@ kvq_status kvq_residency_stats(kvq_cache* c, int layer, int64_t* resident_bytes,
   if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, "kvq_residency_stats: layer out of range");
   DeviceGuard dg(c->device);
   unsigned long long b[2] = {0ull, 0ull};
-  unsigned int stt[RS_WORDS] = {0u, 0u, 0u, 0u};
+  unsigned int stt[RS_WORDS] = {};
   if (c->nres > 0) {
     char* r = c->res + c->res_layer * layer;
     KVQ_CUDA(cudaDeviceSynchronize(), "kvq_residency_stats: sync");

@@ -129,10 +129,12 @@ struct LayerView {
 };
 
 // residency state words
-constexpr int RS_NFREE = 0;   // free slots at the start of the call
-constexpr int RS_TAKEN = 1;   // free-list entries claimed during the call
+constexpr int RS_NFREE = 0;   // free slots at the start of the call (rfree[0, NFREE))
+constexpr int RS_TAKEN = 1;   // claims during the call (from the top of the free stack)
 constexpr int RS_USED = 2;    // slots holding a block after the last eviction pass
-constexpr int RS_WORDS = 4;
+constexpr int RS_PUSHED = 3;  // slots freed by the running eviction pass
+constexpr int RS_DONE = 4;    // CTAs of the running eviction pass that have finished
+constexpr int RS_WORDS = 8;
 
 // counters layout
 constexpr int CNT_MIX_Q = 2;

@@ -7,9 +7,11 @@
 //
 // Per FP16 block a CTA (128 threads) is about to read, thread 0 looks the block up in
 // the layer's slot table; on a hit the CTA reads the slot, on a miss it reads tier 2 and,
-// while a free slot is left, copies the block into it as it goes.  Slot use is stamped
-// with the layer's call number; after each certified call an eviction pass frees the
-// slots that call did not use and rebuilds the free list in slot order.
+// while a free slot is left, copies the block into it as it goes (claims pop the free
+// stack from the top).  Slot use is stamped with the layer's call number; after each
+// certified call an eviction pass frees the slots that call did not use and pushes them
+// back onto the stack.  Which slot a block lands in depends on timing; which blocks are
+// resident, and every output, does not.
 #pragma once
 
 #include "kvq_common.cuh"
@@ -35,7 +37,8 @@ __device__ __forceinline__ ResPick res_pick(const LayerView& V, int kv, size_t b
       atomicAdd(&V.rbytes[0], (unsigned long long)F16_BLOCK_BYTES);
     } else {
       const unsigned int t = atomicAdd(&V.rstate[RS_TAKEN], 1u);
-      if (t < V.rstate[RS_NFREE]) adm = V.rfree[t];
+      const unsigned int nfree = V.rstate[RS_NFREE];   // constant during the call
+      if (t < nfree) adm = V.rfree[nfree - 1u - t];
       atomicAdd(&V.rbytes[1], (unsigned long long)F16_BLOCK_BYTES);
     }
     sh[0] = s;
