@@ -23,6 +23,10 @@ namespace {
 
 constexpr int TAIL_CTAS_PER_SM = 4;
 constexpr int TAIL_STAGES = 2;
+// B words of one value group: [head][hi, lo][token pair], rows of 32 pairs padded to 36
+// words so that the eight lanes of a quarter warp read disjoint banks.
+constexpr int TW_ROW = 36;
+constexpr int TW_WORDS = MAXREP * 2 * TW_ROW;   // per warp
 
 // One block's tail data in shared memory: INT4 codes (this lane's chunks at lane + 32 j),
 // (scale, offset) per value group and token, and the INT8 scores of the group's heads.
@@ -32,35 +36,41 @@ struct __align__(16) TailStage {
   float4 s[MAXREP * BLK / 4];          // [head][token]
 };
 
-__device__ __forceinline__ void cp16(void* dst_smem, const void* src) {
+__device__ __forceinline__ void cp16(void* dst_smem, const void* src, unsigned long long pol) {
   const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
-  unsigned long long pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
                :: "r"(d), "l"(src), "l"(pol) : "memory");
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
 }  // namespace
 
 __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V, int runs) {
   extern __shared__ __align__(16) unsigned char tail_dsm[];
-  TailStage* ring = reinterpret_cast<TailStage*>(tail_dsm) + (threadIdx.x >> 5) * TAIL_STAGES;
+  const int warp = threadIdx.x >> 5;
+  TailStage* ring = reinterpret_cast<TailStage*>(tail_dsm) + warp * TAIL_STAGES;
+  uint32_t* tw = reinterpret_cast<uint32_t*>(tail_dsm + sizeof(TailStage) * TAIL_STAGES * 4) + warp * TW_WORDS;
   pdl_trigger();
   pdl_wait();   // scores of the scoring pass, reference maxima of the selection
   const int lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
-  const int r = gid >> 1;   // head of this lane's B column (hi half for even gid)
+  const int hp = lane >> 3, sub = lane & 7;   // product role: head hp, tokens 8 sub + [0, 8)
   const int nwarps = gridDim.x * (blockDim.x >> 5);
-  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int wid = blockIdx.x * (blockDim.x >> 5) + warp;
   const int NCH = V.nslot;
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
 
   for (int unit = wid; unit < V.BG * runs; unit += nwarps) {
     const int hs = unit / runs, run = unit % runs;
     const int b0 = (int)((long long)run * V.nb / runs);
     const int b1 = (int)((long long)(run + 1) * V.nb / runs);
     const int hrow = hs * V.n_rep;
-    const bool act = r < V.n_rep;
-    const float M = act ? V.hst[hrow + r].M : 0.f;
+    const bool act = hp < V.n_rep;
+    const float M = act ? V.hst[hrow + hp].M : 0.f;
     const float pre_v = prescale_for(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
     const uint8_t* kp0 = V.kprom0 + (size_t)hs * V.nbmax;
     // the run's blocks that keep INT8 scores (FP16-key blocks are the mixed pass's)
@@ -75,15 +85,15 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
         TailStage& T = ring[st];
         const uint4* vc = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cp16(&T.codes[lane + 32 * j], vc + lane + 32 * j);
+        for (int j = 0; j < 8; ++j) cp16(&T.codes[lane + 32 * j], vc + lane + 32 * j, pol);
         const uint4* so = reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS);
-        cp16(&T.so[lane], so + lane);
-        cp16(&T.so[lane + 32], so + lane + 32);
+        cp16(&T.so[lane], so + lane, pol);
+        cp16(&T.so[lane + 32], so + lane + 32, pol);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {   // 64 float4 of scores: head j * 2 + lane / 16
           const int idx = lane + 32 * j, h = idx >> 4;
           if (h < V.n_rep)
-            cp16(&T.s[idx], V.shat + (size_t)(hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)pb * BLK + 4 * (idx & 15));
+            cp16(&T.s[idx], V.shat + (size_t)(hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)pb * BLK + 4 * (idx & 15), pol);
         }
         pb = next_block(pb + 1);
       }
@@ -97,8 +107,8 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[g][mt][j] = 0.f;
-    float off[NG] = {0.f, 0.f, 0.f, 0.f};   // sum p o per value group, head r
-    float lsum = 0.f;                        // sum p, head r
+    float off[NG] = {0.f, 0.f, 0.f, 0.f};   // sum p o per value group, head hp, tokens of this lane
+    float lsum = 0.f;                        // sum p, head hp, tokens of this lane
 
     issue(0);
     int it = 0;
@@ -107,69 +117,73 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
       asm volatile("cp.async.wait_group 1;" ::: "memory");
       __syncwarp();
       const TailStage& T = ring[it % TAIL_STAGES];
-      // weights of head r at tokens 16 tig + [0, 16) (k-step kk: tokens 16 tig + 4 kk + i)
-      float p[16];
+      // weights of head hp at tokens 8 sub + [0, 8), prescaled by 2^e (exact)
+      float pp[8];
+      {
+        const float4 sa = T.s[hp * (BLK / 4) + 2 * sub], sb = T.s[hp * (BLK / 4) + 2 * sub + 1];
+        const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const float4 s4 = T.s[(act ? r : 0) * (BLK / 4) + 4 * tig + kk];
-        p[4 * kk] = act ? __expf(s4.x - M) : 0.f;
-        p[4 * kk + 1] = act ? __expf(s4.y - M) : 0.f;
-        p[4 * kk + 2] = act ? __expf(s4.z - M) : 0.f;
-        p[4 * kk + 3] = act ? __expf(s4.w - M) : 0.f;
+        for (int i = 0; i < 8; ++i) {
+          const float p = act ? __expf(sv[i] - M) : 0.f;
+          lsum += p;
+          pp[i] = p;
+        }
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) lsum += p[i];
-#pragma unroll
       for (int g = 0; g < NG; ++g) {
-        uint32_t bb0[4], bb1[4];
+        // products p_t s_{t,g} 2^e of head hp, tokens 8 sub + [0, 8), as hi + lo halves
+        const uint4 S0 = T.so[g * (BLK / 4) + 2 * sub], S1 = T.so[g * (BLK / 4) + 2 * sub + 1];
+        uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint4 so = T.so[g * (BLK / 4) + 4 * tig + kk];   // (scale, offset) of 4 tokens
-          const __half2* so2 = reinterpret_cast<const __half2*>(&so);
-          uint32_t bw[2];
-#pragma unroll
-          for (int i = 0; i < 4; i += 2) {   // tokens 4kk + i, 4kk + i + 1
-            const float2 a = __half22float2(so2[i]), c = __half22float2(so2[i + 1]);
-            const float2 pv = make_float2(p[4 * kk + i], p[4 * kk + i + 1]);
-            const float2 o2 = mul2(pv, make_float2(a.y, c.y));
-            off[g] += o2.x + o2.y;
-            // p s 2^e as hi + lo, both f16 (the fp32 remainder is exact)
-            const float2 w = mul2(mul2(pv, make_float2(a.x, c.x)), make_float2(pre_v, pre_v));
-            const __half2 hi = __floats2half2_rn(w.x, w.y);
-            const float2 rem = sub2(w, __half22float2(hi));
-            const __half2 lo = __floats2half2_rn(rem.x, rem.y);
-            bw[i >> 1] = (gid & 1) ? h2_as_u32(lo) : h2_as_u32(hi);
-          }
-          bb0[kk] = bw[0];
-          bb1[kk] = bw[1];
+        for (int i = 0; i < 4; ++i) {   // token pair 4 sub + i: tokens 8 sub + 2i, +1
+          const uint4& S = (i < 2) ? S0 : S1;
+          const float2 a = __half22float2(u32_as_h2(word_of(S, 2 * (i & 1))));       // (scale, offset)
+          const float2 c = __half22float2(u32_as_h2(word_of(S, 2 * (i & 1) + 1)));
+          const float2 pv = make_float2(pp[2 * i], pp[2 * i + 1]);
+          const float2 o2 = mul2(pv, make_float2(a.y, c.y));
+          off[g] += o2.x + o2.y;
+          const float2 w = mul2(mul2(pv, make_float2(pre_v, pre_v)), make_float2(a.x, c.x));
+          const __half2 hi = __floats2half2_rn(w.x, w.y);
+          const float2 rem = sub2(w, __half22float2(hi));   // exact remainders
+          hw[i] = h2_as_u32(hi);
+          lw[i] = h2_as_u32(__floats2half2_rn(rem.x, rem.y));
         }
+        uint32_t* wr = tw + hp * (2 * TW_ROW) + 4 * sub;
+        *reinterpret_cast<uint4*>(wr) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(wr + TW_ROW) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        __syncwarp();
+        // B fragments of column gid = (head gid>>1, hi or lo): k-step kk takes token pairs
+        // 8 tig + 2kk (tokens 16 tig + 4kk + {0,1}) and 8 tig + 2kk + 1 ({2,3})
+        const uint32_t* rd = tw + (gid >> 1) * (2 * TW_ROW) + (gid & 1) * TW_ROW + 8 * tig;
+        const uint4 B0 = *reinterpret_cast<const uint4*>(rd), B1 = *reinterpret_cast<const uint4*>(rd + 4);
+        const uint32_t bb[8] = {B0.x, B0.y, B0.z, B0.w, B1.x, B1.y, B1.z, B1.w};
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           const uint4 Cw = T.codes[lane + 32 * (2 * g + mt)];
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t w = (kk == 0) ? Cw.x : (kk == 1) ? Cw.y : (kk == 2) ? Cw.z : Cw.w;
             uint32_t a0, a1, a2, a3;
-            nib8_to_f16x4(w, a0, a1, a2, a3);
-            mma16816(acc[g][mt], a0, a1, a2, a3, bb0[kk], bb1[kk]);
+            nib8_to_f16x4(word_of(Cw, kk), a0, a1, a2, a3);
+            mma16816(acc[g][mt], a0, a1, a2, a3, bb[2 * kk], bb[2 * kk + 1]);
           }
         }
+        __syncwarp();   // every lane has read the B words before the next group's
       }
-      __syncwarp();   // every lane is done with this slot before it is refilled
     }
     asm volatile("cp.async.wait_group 0;" ::: "memory");
     __syncwarp();
 
-    // head r's sums are spread over the four tig lanes of lane pair (2r, 2r+1): the hi
-    // lane (even gid) carries them once
+    // head hp's sums are spread over its eight product lanes
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
       off[g] += __shfl_xor_sync(0xffffffffu, off[g], 1);
       off[g] += __shfl_xor_sync(0xffffffffu, off[g], 2);
+      off[g] += __shfl_xor_sync(0xffffffffu, off[g], 4);
     }
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-    // this lane writes head tig: its offsets sit in lane 8 tig (gid 2 tig, tig 0)
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
+    // this lane writes head tig: its offsets sit in lane 8 tig
     float offh[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) offh[g] = __shfl_sync(0xffffffffu, off[g], 8 * tig);
@@ -186,7 +200,7 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
           pr[c0 + 8] = (acc[g][mt][2] + acc[g][mt][3]) * inv + offh[g];
         }
     }
-    if (tig == 0 && (gid & 1) == 0 && act) pp[r * (D + 4) + D] = lsum;
+    if (sub == 0 && act) pp[hp * (D + 4) + D] = lsum;
   }
 }
 
@@ -199,7 +213,7 @@ cudaError_t launch_tail(const LayerView& V, int runs, int num_sms, cudaStream_t 
   int grid = num_sms * TAIL_CTAS_PER_SM;
   const int units = V.BG * runs;
   if (grid * 4 > units) grid = (units + 3) / 4;
-  const size_t dyn = sizeof(TailStage) * TAIL_STAGES * 4;   // 4 warps
+  const size_t dyn = (sizeof(TailStage) * TAIL_STAGES + TW_WORDS * 4) * 4;   // 4 warps
   cudaError_t e = cudaFuncSetAttribute(tail_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
   return launch_dependent(tail_kernel, dim3(grid), dim3(128), dyn, st, V, runs);
