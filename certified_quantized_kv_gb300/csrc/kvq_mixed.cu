@@ -38,12 +38,17 @@ namespace kvq {
 namespace {
 
 constexpr int KROW = D + 8;   // padded FP16 row (272 bytes): conflict-free 16-byte reads
+// B words of one value group: [head][hi, lo][token pair], rows of 32 pairs padded to 36
+// words so that the eight lanes of a quarter warp read disjoint banks.
+constexpr int MW_ROW = 36;
+constexpr int MW_WORDS = MAXREP * 2 * MW_ROW;   // per warp
 
 struct __align__(16) MixSmem {
   float p[2][MAXREP][BLK];    // INT4-path weights
   float pn[2][MAXREP][BLK];   // FP16-value weights / FP16 scores
   float qf[MAXREP][D];
   float M[MAXREP];
+  uint32_t bw[4][MW_WORDS];   // per warp: the INT4-path B words of its value group
   struct {
     __half kbuf[BLK][KROW];
     __half vbuf[BLK][D];
@@ -135,7 +140,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
     float acc16[4] = {0.f, 0.f, 0.f, 0.f};
-    float off = 0.f;     // sum p * offset for head gid>>1, group = warp
+    float off = 0.f;     // sum p * offset for head lane/8 (this lane's tokens), group = warp
     float lsum = 0.f;    // sum p for head = warp
 
     const int blk_end = min(V.nb, (ch + 1) * V.chunk);
@@ -235,27 +240,42 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
       if (!v16) {
         const uint4* vcp = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES) + (warp * 2) * 32 + lane;
         const uint4 C0 = __ldcs(vcp), C1 = __ldcs(vcp + 32);
-        const uint4* svp = reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS + warp * BLK + 16 * tig);
-        const int rr = gid >> 1;
-        const float* pr = &sm.p[par][rr][16 * tig];
-        uint32_t bb0[4], bb1[4];
+        // products p_t s_{t,g} 2^e of head hp = lane / 8 at tokens 8 (lane % 8) + [0, 8), as
+        // hi + lo halves, formed once per warp and exchanged as B fragments
+        {
+          const int hp = lane >> 3, sub = lane & 7;
+          const uint4* svp = reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS + warp * BLK + 8 * sub);
+          const uint4 S0 = __ldcs(svp), S1 = __ldcs(svp + 1);        // (scale, offset), 8 tokens
+          const float4 pa = *reinterpret_cast<const float4*>(&sm.p[par][hp][8 * sub]);
+          const float4 pb = *reinterpret_cast<const float4*>(&sm.p[par][hp][8 * sub + 4]);
+          const float pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+          const uint32_t sw[8] = {S0.x, S0.y, S0.z, S0.w, S1.x, S1.y, S1.z, S1.w};
+          uint32_t hw[4], lw[4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint4 so = __ldcs(svp + kk);                       // tokens 4kk .. 4kk+3
-          const float4 pp = *reinterpret_cast<const float4*>(pr + 4 * kk);
-          const __half2* so2 = reinterpret_cast<const __half2*>(&so);
-          const float pv[4] = {pp.x, pp.y, pp.z, pp.w};
-          __half sel[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 sof = __half22float2(so2[i]);
-            off = fmaf(pv[i], sof.y, off);
-            __half hi, lo;
-            split_hl(pv[i] * sof.x * pre_v, hi, lo);
-            sel[i] = (gid & 1) ? lo : hi;
+          for (int i = 0; i < 4; ++i) {   // token pair 4 sub + i
+            const float2 a = __half22float2(u32_as_h2(sw[2 * i])), c = __half22float2(u32_as_h2(sw[2 * i + 1]));
+            const float2 p2 = make_float2(pv[2 * i], pv[2 * i + 1]);
+            off = fmaf(p2.x, a.y, off);
+            off = fmaf(p2.y, c.y, off);
+            const float2 w = mul2(mul2(p2, make_float2(a.x, c.x)), make_float2(pre_v, pre_v));
+            const __half2 hi = __floats2half2_rn(w.x, w.y);
+            const float2 rem = sub2(w, __half22float2(hi));   // exact remainders
+            hw[i] = h2_as_u32(hi);
+            lw[i] = h2_as_u32(__floats2half2_rn(rem.x, rem.y));
           }
-          bb0[kk] = h2_as_u32(__halves2half2(sel[0], sel[1]));
-          bb1[kk] = h2_as_u32(__halves2half2(sel[2], sel[3]));
+          uint32_t* wr = sm.bw[warp] + hp * (2 * MW_ROW) + 4 * sub;
+          *reinterpret_cast<uint4*>(wr) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(wr + MW_ROW) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        __syncwarp();
+        // column gid = (head gid>>1, hi or lo): k-step kk takes token pairs 8 tig + 2kk and
+        // 8 tig + 2kk + 1 (tokens 16 tig + 4kk + {0,1} and {2,3})
+        uint32_t bb0[4], bb1[4];
+        {
+          const uint32_t* rd = sm.bw[warp] + (gid >> 1) * (2 * MW_ROW) + (gid & 1) * MW_ROW + 8 * tig;
+          const uint4 B0 = *reinterpret_cast<const uint4*>(rd), B1 = *reinterpret_cast<const uint4*>(rd + 4);
+          bb0[0] = B0.x; bb1[0] = B0.y; bb0[1] = B0.z; bb1[1] = B0.w;
+          bb0[2] = B1.x; bb1[2] = B1.y; bb0[3] = B1.z; bb1[3] = B1.w;
         }
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
@@ -290,9 +310,10 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
     }
 
     // ---- write this chunk's partial: l and acc[D] per head ----
-    off += __shfl_xor_sync(0xffffffffu, off, 1);
+    off += __shfl_xor_sync(0xffffffffu, off, 1);   // head lane/8: its eight product lanes
     off += __shfl_xor_sync(0xffffffffu, off, 2);
-    const float offh = __shfl_sync(0xffffffffu, off, 8 * tig);  // head tig, hi lane
+    off += __shfl_xor_sync(0xffffffffu, off, 4);
+    const float offh = __shfl_sync(0xffffffffu, off, 8 * tig);  // head tig
     const float inv = 1.f / pre_v;
     float* pp = (round == 0 ? V.part : V.part1) + (((size_t)hs * NCH + ch) * MAXREP) * (D + 4);
     if (tig < V.n_rep) {
