@@ -346,7 +346,7 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   const size_t s_part1 = o; o = align_up(o + BG * NCH * MAXREP * (D + 4) * 4, 256);
   const size_t s_red0 = o;  o = align_up(o + HQ * (D + 4) * 4, 256);
   const size_t s_dpart = o; o = align_up(o + BG * NCH * MAXREP * (D + 4) * 4, 256);
-  const size_t s_cnt = o;   o = align_up(o + (CNT_GROUP_BASE + 4 * BG) * 4, 256);
+  const size_t s_cnt = o;   o = align_up(o + (CNT_GROUP_BASE + 4 * BG + c->B) * 4, 256);
   const size_t s_q = o;     o = align_up(o + HQ * D * 2, 256);
   const size_t s_out = o;   o = align_up(o + HQ * D * 2, 256);
   const size_t s_cert = o;  o = align_up(o + HQ * sizeof(kvq_certificate), 256);

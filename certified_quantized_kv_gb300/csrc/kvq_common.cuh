@@ -145,6 +145,9 @@ constexpr int CNT_ANY_DENSE = 6;    // set when a head reaches rung 3 (reset by 
 constexpr int CNT_NEED_R1 = 7;      // set when a head plans rung 1 or 2 (reset by the finaliser)
 constexpr int CNT_GROUP_BASE = 16;  // + stage*BG + hs: per-group completion counters
 constexpr int N_STAGE_COUNTERS = 3;
+// + b after the four per-group stages: heads of sequence b at rung 3 after the ladder
+// plan (kept by the combine kernels, read by the dense pass, cleared by the finaliser)
+__host__ __device__ constexpr int cnt_rung3(int BG, int b) { return CNT_GROUP_BASE + 4 * BG + b; }
 
 // ---------------------------------------------------------------------------------
 // small helpers

@@ -46,8 +46,8 @@ __device__ int dense_mask(const LayerView& V, int hs, int all_dense) {
   const int b = hs / V.Hkv, g = hs % V.Hkv;
   const int full = (1 << V.n_rep) - 1;
   if (all_dense) return full;
-  int n3 = 0;
-  for (int h = 0; h < V.Hq; ++h) n3 += (V.hst[(size_t)b * V.Hq + h].level1 == 3);
+  const unsigned int n3 = V.counters[cnt_rung3(V.BG, b)];   // heads of sequence b at rung 3
+  if (n3 == 0u) return 0;
   if ((float)n3 >= V.l4_frac * (float)V.Hq) return full;
   int m = 0;
   for (int r = 0; r < V.n_rep; ++r)
@@ -103,9 +103,7 @@ __device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dens
   }
   __syncthreads();
   if (tid == 0) {
-    int n3 = 0;
-    if (!all_dense)
-      for (int h = 0; h < V.Hq; ++h) n3 += (V.hst[(size_t)b * V.Hq + h].level1 == 3);
+    const unsigned int n3 = all_dense ? 0u : V.counters[cnt_rung3(V.BG, b)];
     const bool l4 = all_dense || ((float)n3 >= V.l4_frac * (float)V.Hq);
     for (int r = 0; r < V.n_rep; ++r) {
       HeadState& h = V.hst[head_row(V, b, g, r)];
@@ -310,6 +308,7 @@ __global__ void finalize_kernel(LayerView V, kvq_certificate* cert, int32_t* lev
   }
   __syncthreads();
   if (threadIdx.x == 0 && level) level[b] = mx;
+  if (threadIdx.x == 0) V.counters[cnt_rung3(V.BG, b)] = 0u;   // consumed by the dense pass
   if (b == 0 && threadIdx.x == 0) {   // the flags of this call have been consumed
     V.counters[CNT_ANY_DENSE] = 0u;
     V.counters[CNT_NEED_R1] = 0u;

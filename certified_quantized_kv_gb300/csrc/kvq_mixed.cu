@@ -480,7 +480,10 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
     hsd.level1 = (e_key + e_val <= V.eps && e_val <= V.v_tol) ? hsd.planned : 3;
     if (tid == 0) {
       V.hst[hb] = hsd;
-      if (hsd.level1 == 3) V.counters[CNT_ANY_DENSE] = 1u;
+      if (hsd.level1 == 3) {
+        V.counters[CNT_ANY_DENSE] = 1u;
+        atomicAdd(&V.counters[cnt_rung3(V.BG, b)], 1u);
+      }
     }
     return;
   }
@@ -609,7 +612,10 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   hsd.level1 = planned;   // rungs 1/2 are confirmed, or raised to 3, by the second pass
   if (tid == 0) {
     V.hst[hb] = hsd;
-    if (planned == 3) V.counters[CNT_ANY_DENSE] = 1u;
+    if (planned == 3) {
+      V.counters[CNT_ANY_DENSE] = 1u;
+      atomicAdd(&V.counters[cnt_rung3(V.BG, b)], 1u);
+    }
   }
 }
 
