@@ -146,3 +146,45 @@ def test_fp16_values_configuration():
         _same(a, b)
     assert res[1]["stats"]["host_bytes"] == 0
     _oracle_check(q, K, V, 0.995, 0.25, res[1], value_bits=16)
+
+
+def test_serving_loop_with_appends():
+    """Decode steps interleaved with appends (some completing a block, some not): blocks
+    completed after a slot table was filled must be paged in from tier 2, and every step
+    must equal the cache without residency bit for bit."""
+    q0, K, V = W.c1(ctx=64 * 20 + 50, Hq=8, Hkv=2, batch=2)
+    gen = torch.Generator().manual_seed(31)
+    steps = [(int(n), torch.randn(q0.shape, generator=gen).half()) for n in (1, 13, 64, 2, 70)]
+    B, Hkv, N0, D = K.shape
+    extra = sum(n for n, _ in steps)
+    Kx = torch.randn(B, Hkv, extra, D, generator=gen).half()
+    Vx = torch.randn(B, Hkv, extra, D, generator=gen).half()
+
+    def run(slots):
+        cache = kvq.Cache(1, B, q0.shape[1], Hkv, max_ctx=N0 + extra, resident_blocks=slots)
+        outs, pos = [], 0
+        try:
+            cache.append(0, K.cuda().contiguous(), V.cuda().contiguous())
+            for n, q in steps:
+                cache.append(0, Kx[:, :, pos:pos + n].cuda().contiguous(), Vx[:, :, pos:pos + n].cuda().contiguous())
+                pos += n
+                out = torch.empty(B, q.shape[1], D, dtype=torch.float16, device="cuda")
+                cert = torch.empty(B * q.shape[1] * 32, dtype=torch.uint8, device="cuda")
+                cache.decode(0, q.cuda().contiguous(), 0.995, 0.25, out, cert)
+                torch.cuda.synchronize()
+                outs.append((out.cpu(), kvq.certificates(cert).tobytes(), cache.residency_stats(0, reset=True)))
+        finally:
+            cache.close()
+        return outs
+
+    base, res = run(0), run(4096)
+    for (ob, cb, _), (orr, cr, st) in zip(base, res):
+        assert torch.equal(ob, orr) and cb == cr
+    assert res[-1][2]["resident_bytes"] > 0
+    # the final state against the oracle
+    pos = extra
+    Kf = torch.cat([K, Kx], dim=2)
+    Vf = torch.cat([V, Vx], dim=2)
+    c = kvq.certificates(res[-1][1]).reshape(B, q0.shape[1])
+    _oracle_check(steps[-1][1], Kf, Vf, 0.995, 0.25,
+                  dict(out=res[-1][0], cert=c, level=c["level"].max(axis=1)))
