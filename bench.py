@@ -470,6 +470,19 @@ def our_arm(args, wl):
     uncertified = {"value": world * B * L / (unc_ms / 1e3), "unit": UNIT, "ms_per_step": unc_ms,
                    "what": "INT8 scores and INT4 values on every block: no page-in, no ladder"}
 
+    # the tier-1 kernels alone: uncertified calls on one layer in a loop, CUDA events
+    # around every kernel (the scoring pass and the INT4 value pass)
+    cache.set_debug(kvq.DEBUG_PROFILE)
+    for _ in range(3):
+        cache.decode_uncertified(0, qs[0], outs[0])
+    torch.cuda.synchronize()
+    cache.profile_read(reset=True)
+    for _ in range(20):
+        cache.decode_uncertified(0, qs[0], outs[0])
+    torch.cuda.synchronize()
+    prof_alone = cache.profile_read(reset=True)
+    cache.set_debug(0)
+
     # certificates of the last step: ladder histogram, promoted bytes
     hist = [0] * 5
     prom = 0
@@ -567,6 +580,18 @@ def our_arm(args, wl):
     elif dom in hbm_algo:
         roofline = hbm_roofline(dom)
     roofline_hbm = hbm_roofline("score") if "score" in kern else None
+    # the same kernels timed alone (one layer, uncertified calls back to back)
+    tier1_alone = {}
+    for k, per_unit in (("score", SCORE_BYTES_PER_TOKEN_HEAD), ("int4_tail", MIX_BYTES_PER_TOKEN_HEAD + 4 * (Hq // Hkv))):
+        if k in prof_alone:
+            n, tot = prof_alone[k]
+            us = 1e3 * tot / max(1, n)
+            b = per_unit * units
+            t = traffic.get(k, {}).get("dram_bytes")
+            tier1_alone[k] = {"bound": "hbm", "kernel": k, "avg_us": us, "achieved": b / (us * 1e-6) / 1e9,
+                              "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                              "frac": b / (us * 1e-6) / 1e9 / hbm_peak, "traffic": t,
+                              "algorithmic_bytes_per_launch": b}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -578,6 +603,7 @@ def our_arm(args, wl):
         "gpu_launches": int(sum(v["launches"] for v in kern.values())) // max(1, args.steps) * args.steps,
         "roofline": roofline,
         "roofline_hbm": roofline_hbm,
+        "roofline_tier1_alone": tier1_alone,
         "kernels": kern,
         "ladder_histogram": hist,
         "promoted_bytes_per_step": prom,
