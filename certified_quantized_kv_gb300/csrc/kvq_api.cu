@@ -2,10 +2,11 @@
 // exports for tests, per-kernel timing.
 //
 // Orchestration of one decode call ("Runtime-Certified Bounded-Error Quantized
-// Attention", gist.science technical summary, Method §1-§3): the INT8 scoring pass with
-// top-K* selection, the mixed-precision pass with certificate and ladder plan, a second
-// mixed pass for groups that asked for rungs 1-2, the dense rungs 3-4, and the
-// certificate write-out -- five stream-ordered launches with no host round trip; every
+// Attention", gist.science technical summary, Method §1-§3): the INT8 scoring pass, the
+// top-K* selection, the mixed-precision pass and its combine (certificate and ladder
+// plan), a second mixed pass and combine for groups that asked for rungs 1-2, the dense
+// rungs 3-4 and the certificate write-out -- eight stream-ordered launches (a ninth, the
+// eviction pass, with cross-step residency) with no host round trip; every
 // data-dependent decision is taken on the device.
 #include <cuda_runtime.h>
 #include <nvtx3/nvToolsExt.h>

@@ -200,12 +200,6 @@ __device__ __forceinline__ void nib8_to_f16x4(uint32_t w, uint32_t& a0, uint32_t
   a3 = h2_as_u32(__hfma2(u32_as_h2((x & 0x00F000F0u) | 0x64006400u), k16th, km64));
 }
 
-// x = hi + lo with hi = rn16(x), lo = rn16(x - hi); exact unless lo is subnormal.
-__device__ __forceinline__ void split_hl(float x, __half& hi, __half& lo) {
-  hi = __float2half_rn(x);
-  lo = __float2half_rn(x - __half2float(hi));
-}
-
 // Packed fp32 pairs (two lanes of one 64-bit register pair per instruction).
 __device__ __forceinline__ unsigned long long f2_bits(float2 v) {
   return ((unsigned long long)__float_as_uint(v.y) << 32) | __float_as_uint(v.x);
