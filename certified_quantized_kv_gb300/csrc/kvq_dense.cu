@@ -80,26 +80,36 @@ __device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dens
     }
   }
   __syncthreads();
-  for (int r = 0; r < V.n_rep; ++r) {
-    if (!(mask >> r & 1)) continue;
-    // global max over chunk maxima and the partial block
+  // warp r combines head slot r's chunk partials (lane = four channels): the global max
+  // over the chunk maxima and the partial block, then the rescaled sums in chunk order
+  const int r = warp;
+  if (r < V.n_rep && (mask >> r & 1)) {
+    const int nchv = V.nb > 0 ? nch : 0;
+    const float* P = V.dpart + ((size_t)hs * NCH * MAXREP + r) * (D + 4);   // chunk c at + c MAXREP (D + 4)
     float M = -INFINITY;
-    for (int c = 0; c < nch && V.nb > 0; ++c)
-      M = fmaxf(M, V.dpart[(((size_t)hs * NCH + c) * MAXREP + r) * (D + 4) + D]);
-    for (int t = 0; t < V.n_tail; ++t) M = fmaxf(M, sm.s[r][t]);
-    float L = 0.f, a = 0.f;
-    for (int c = 0; c < nch && V.nb > 0; ++c) {
-      const float* pp = V.dpart + (((size_t)hs * NCH + c) * MAXREP + r) * (D + 4);
+    for (int c = lane; c < nchv; c += 32) M = fmaxf(M, P[(size_t)c * MAXREP * (D + 4) + D]);
+    for (int t = lane; t < V.n_tail; t += 32) M = fmaxf(M, sm.s[r][t]);
+    M = warp_max(M);
+    float L = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int c = 0; c < nchv; ++c) {
+      const float* pp = P + (size_t)c * MAXREP * (D + 4);
       const float w = expf(pp[D] - M);
+      const float4 x = *reinterpret_cast<const float4*>(pp + 4 * lane);
       L += pp[D + 1] * w;
-      a += pp[tid] * w;
+      a.x += x.x * w; a.y += x.y * w; a.z += x.z * w; a.w += x.w * w;
     }
     for (int t = 0; t < V.n_tail; ++t) {
       const float p = expf(sm.s[r][t] - M);
+      const uint2 vv = *reinterpret_cast<const uint2*>(V.tail_v + ((size_t)hs * BLK + t) * D + 4 * lane);
+      const float2 v01 = __half22float2(u32_as_h2(vv.x)), v23 = __half22float2(u32_as_h2(vv.y));
       L += p;
-      a += p * __half2float(V.tail_v[((size_t)hs * BLK + t) * D + tid]);
+      a.x += p * v01.x; a.y += p * v01.y; a.z += p * v23.x; a.w += p * v23.y;
     }
-    V.out[head_row(V, b, g, r) * D + tid] = __float2half_rn(a / L);
+    __half2* o = reinterpret_cast<__half2*>(V.out + head_row(V, b, g, r) * D + 4 * lane);
+    o[0] = __floats2half2_rn(a.x / L, a.y / L);
+    o[1] = __floats2half2_rn(a.z / L, a.w / L);
   }
   __syncthreads();
   if (tid == 0) {
