@@ -188,3 +188,16 @@ def test_serving_loop_with_appends():
     c = kvq.certificates(res[-1][1]).reshape(B, q0.shape[1])
     _oracle_check(steps[-1][1], Kf, Vf, 0.995, 0.25,
                   dict(out=res[-1][0], cert=c, level=c["level"].max(axis=1)))
+
+
+@pytest.mark.parametrize("ctx", [37, 64, 64 * 3 + 5])
+def test_short_layers(ctx):
+    """Layers with no or few full blocks: the eviction pass and the slot table must cope
+    with nothing (or almost nothing) to page in."""
+    q, K, V = W.tiny(seed=40 + ctx, ctx=ctx, Hq=8, Hkv=2, batch=2, kscale=3.0)
+    base = _calls(K, V, [q, q], 0.995, 0.25, 0)
+    res = _calls(K, V, [q, q], 0.995, 0.25, 16, uncertified_between=True)
+    for a, b in zip(res, base):
+        _same(a, b)
+        assert a["stats"]["resident_bytes"] + a["stats"]["host_bytes"] == a["paged"]
+    _oracle_check(q, K, V, 0.995, 0.25, res[1])
