@@ -703,7 +703,8 @@ def decode_loop(args):
     Hq, Hkv, D, tau, eps = wl["q_heads"], wl["kv_heads"], wl["head_dim"], wl["tau_cov"], wl["eps"]
     T, Wm = args.steps, args.warmup
     n0 = N - T - Wm
-    cache = kvq.Cache(L, B, Hq, Hkv, max_ctx=N)
+    slots = int(args.resident * B * Hkv * (N // 64) * 2)   # a fraction of each layer's FP16 blocks
+    cache = kvq.Cache(L, B, Hq, Hkv, max_ctx=N, resident_blocks=slots)
     for layer in range(L):
         _, K, V = W.c3_layer(layer, device="cuda", seed=wl["seed"], batch=B, ctx=n0, Hq=Hq, Hkv=Hkv)
         cache.append(layer, K.contiguous(), V.contiguous())
@@ -725,6 +726,8 @@ def decode_loop(args):
     for t in range(Wm):
         step(t)
     torch.cuda.synchronize()
+    for layer in range(L):
+        cache.residency_stats(layer, reset=True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for t in range(Wm, steps):
@@ -732,9 +735,14 @@ def decode_loop(args):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / T
+    rs = [cache.residency_stats(layer) for layer in range(L)]
     print(json.dumps({"mode": "decode_loop", "metric": "tokens/s/layer (append + certified decode per token)",
                       "value": B / (ms / L / 1e3), "ms_per_step": ms, "steps": T, "warmup": Wm,
-                      "layers": L, "batch": B, "ctx_end": N, "tau_cov": tau, "eps": eps}), flush=True)
+                      "layers": L, "batch": B, "ctx_end": N, "tau_cov": tau, "eps": eps,
+                      "resident_fraction": args.resident, "resident_blocks_per_layer": slots,
+                      "host_bytes_per_step": sum(x["host_bytes"] for x in rs) / T if slots else None,
+                      "resident_bytes_per_step": sum(x["resident_bytes"] for x in rs) / T if slots else None}),
+          flush=True)
     cache.close()
 
 
@@ -792,6 +800,8 @@ def main():
     ap.add_argument("--ctx", type=int, default=None, help="override the context (not the headline)")
     ap.add_argument("--batch", type=int, default=None, help="override the batch (not the headline)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--resident", type=float, default=0.0,
+                    help="with --loop: fraction of each layer's FP16 blocks kept resident in HBM")
     ap.add_argument("--loop", action="store_true",
                     help="token-by-token decode loop (append + decode per layer and step)")
     ap.add_argument("--sweep", choices=["c5", "vtol"], default=None,
