@@ -91,6 +91,29 @@ __device__ __forceinline__ void load_f16_block(__half* dst, const __half* src, _
   }
 }
 
+// FP16 scores of one block for the group's heads, s = (q . k) / sqrt(D) in fp32 in channel
+// order: thread t (of 128) takes token t % 64 and heads 2 (t / 64) and 2 (t / 64) + 1.
+__device__ __forceinline__ void score_f16_block(const __half (*kbuf)[KROW], const float (*qf)[D],
+                                                float (*out)[BLK]) {
+  const int t = threadIdx.x & 63, rp = (threadIdx.x >> 6) * 2;
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < D; c += 8) {
+    const uint4 kv = *reinterpret_cast<const uint4*>(&kbuf[t][c]);
+    const __half2* k2 = reinterpret_cast<const __half2*>(&kv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 kf = __half22float2(k2[j]);
+      s0 = fmaf(qf[rp][c + 2 * j], kf.x, s0);
+      s0 = fmaf(qf[rp][c + 2 * j + 1], kf.y, s0);
+      s1 = fmaf(qf[rp + 1][c + 2 * j], kf.x, s1);
+      s1 = fmaf(qf[rp + 1][c + 2 * j + 1], kf.y, s1);
+    }
+  }
+  out[rp][t] = s0 * INV_SQRT_D;
+  out[rp + 1][t] = s1 * INV_SQRT_D;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
@@ -178,25 +201,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
                              res_dst(V, pk));
         res_commit(V, 0, bi, pk);
         __syncthreads();
-        {
-          const int t = tid & 63, rp = (tid >> 6) * 2;  // heads rp, rp+1
-          float s0 = 0.f, s1 = 0.f;
-#pragma unroll 4
-          for (int c = 0; c < D; c += 8) {
-            const uint4 kv = *reinterpret_cast<const uint4*>(&sm.st.kbuf[t][c]);
-            const __half2* k2 = reinterpret_cast<const __half2*>(&kv);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 kf = __half22float2(k2[j]);
-              s0 = fmaf(sm.qf[rp][c + 2 * j], kf.x, s0);
-              s0 = fmaf(sm.qf[rp][c + 2 * j + 1], kf.y, s0);
-              s1 = fmaf(sm.qf[rp + 1][c + 2 * j], kf.x, s1);
-              s1 = fmaf(sm.qf[rp + 1][c + 2 * j + 1], kf.y, s1);
-            }
-          }
-          sm.pn[par][rp][t] = s0 * INV_SQRT_D;
-          sm.pn[par][rp + 1][t] = s1 * INV_SQRT_D;
-        }
+        score_f16_block(sm.st.kbuf, sm.qf, sm.pn[par]);
         __syncthreads();
         sn0 = sm.pn[par][r][lane];
         sn1 = sm.pn[par][r][lane + 32];
@@ -619,9 +624,235 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   }
 }
 
+namespace {
+
+// Round 0 with INT4 values in VRAM.  Every block needs the INT4 codes and scale/offset of
+// its values, and a block that keeps its INT8 scores needs nothing else, so each warp
+// (one value group) forms the weights of all the group's heads for itself from the
+// stored scores: such blocks run without a CTA barrier, fed by a two-stage cp.async ring
+// per warp that holds the next block while the current one is multiplied.  Blocks with
+// FP16 keys are scored by the whole CTA (tier-2 read, then the dot products between two
+// barriers) and their weights handed to the warps through shared memory.
+constexpr int R0_STAGES = 2;
+
+struct __align__(16) R0Stage {   // one block, one value group
+  float4 s[MAXREP * BLK / 4];    // INT8 scores [head][token]
+  uint4 codes[64];               // the group's INT4 code chunks (this lane's: lane, lane + 32)
+  uint4 so[BLK / 4];             // the group's (scale, offset) half2 per token
+};
+
+struct __align__(16) R0Smem {
+  float p[MAXREP][BLK];          // weights of an FP16-key block
+  float s16[MAXREP][BLK];        // its FP16 scores
+  float qf[MAXREP][D];
+  float M[MAXREP];
+  uint32_t bw[4][MW_WORDS];      // per warp: the B words of its value group
+  __half kbuf[BLK][KROW];
+  R0Stage ring[4][R0_STAGES];
+  int item;
+  int res[2];
+};
+
+}  // namespace
+
+__global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
+  pdl_trigger();
+  pdl_wait();   // selection: FP16-key flags, reference maxima; scores of the scoring pass
+  __shared__ R0Smem sm;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int hp = lane >> 3, sub = lane & 7;   // weight role: head hp, tokens 8 sub + [0, 8)
+  const int nch = max(1, (V.nb + V.chunk - 1) / V.chunk);
+  const int NCH = V.nslot;
+  const int total = V.BG * nch;
+  const bool act = hp < V.n_rep;              // head hp exists
+  const bool wact = warp < V.n_rep;           // head `warp` exists (FP16-key role)
+  const unsigned long long pol = evict_first_policy();
+  R0Stage* ring = sm.ring[warp];
+  int cur_hs = -1;
+  float pre_v = 1.f, Mh = 0.f;
+
+  for (;;) {
+    if (tid == 0) sm.item = (int)atomicAdd(&V.counters[CNT_MIX_Q], 1u);
+    __syncthreads();
+    const int item = sm.item;
+    if (item >= total) break;
+    const int hs = item / nch, ch = item % nch;
+    const int b = hs / V.Hkv, g = hs % V.Hkv;
+    const size_t hrow = head_row(V, b, g, 0);
+    if (hs != cur_hs) {
+      cur_hs = hs;
+      for (int i = tid; i < MAXREP * D; i += blockDim.x) {
+        const int r = i / D, c = i % D;
+        sm.qf[r][c] = (r < V.n_rep) ? __half2float(V.q[(hrow + r) * D + c]) : 0.f;
+      }
+      if (tid < MAXREP) sm.M[tid] = (tid < V.n_rep) ? V.hst[hrow + tid].M : 0.f;
+      pre_v = prescale_for(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
+      __syncthreads();
+      Mh = sm.M[hp];
+    }
+
+    const int blk0 = ch * V.chunk, blk_end = min(V.nb, blk0 + V.chunk);
+    int pb = blk0;                 // producer: next block to copy
+    unsigned char kp_next = 0;     // FP16-key flag of the block copied last
+    auto issue = [&](int st) {
+      if (pb < blk_end) {
+        const size_t bi = (size_t)hs * V.nbmax + pb;
+        R0Stage& T = ring[st];
+        kp_next = V.kprom0[bi];
+        const uint4* vc = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES) + warp * 64;
+        cp_async16_hint(&T.codes[lane], vc + lane, pol);
+        cp_async16_hint(&T.codes[lane + 32], vc + lane + 32, pol);
+        if (lane < BLK / 4)
+          cp_async16_hint(&T.so[lane], reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS + warp * BLK) + lane, pol);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {   // 64 float4 of scores: head (lane + 32 j) / 16
+          const int idx = lane + 32 * j, h = idx >> 4;
+          if (h < V.n_rep)
+            cp_async16_hint(&T.s[idx], V.shat + (hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)pb * BLK + 4 * (idx & 15), pol);
+        }
+        ++pb;
+      }
+      cp_async_commit();
+    };
+
+    float acc[2][4];
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    float off = 0.f;    // sum p * offset: head hp, this lane's tokens, group = warp
+    float lsum = 0.f;   // sum p: head hp, this lane's tokens
+
+    issue(0);
+    for (int blk = blk0, it = 0; blk < blk_end; ++blk, ++it) {
+      const bool kp0 = kp_next != 0;
+      issue((it + 1) % R0_STAGES);
+      cp_async_wait<1>();
+      __syncwarp();
+      const R0Stage& T = ring[it % R0_STAGES];
+      // weights p = exp(s' - M) of head hp at tokens 8 sub + [0, 8)
+      float pv[8];
+      if (kp0) {
+        // FP16 keys from tier 2 (or their resident copy); the FP16 scores replace the
+        // INT8 ones in the score scratch for the second pass
+        const size_t bi = (size_t)hs * V.nbmax + blk;
+        const ResPick pk = res_pick(V, 0, bi, sm.res);
+        load_f16_block<KROW>(&sm.kbuf[0][0],
+                             res_src(V, pk, V.t2k + ((size_t)hs * V.cap + (size_t)blk * BLK) * D),
+                             res_dst(V, pk));
+        res_commit(V, 0, bi, pk);
+        __syncthreads();
+        score_f16_block(sm.kbuf, sm.qf, sm.s16);
+        __syncthreads();
+        float p0 = 0.f, p1 = 0.f;
+        if (wact) {
+          const float sn0 = sm.s16[warp][lane], sn1 = sm.s16[warp][lane + 32];
+          const float m = warp_max(fmaxf(sn0, sn1));
+          const float l = warp_sum(expf(sn0 - m) + expf(sn1 - m));
+          if (lane == 0) V.lse16[(hrow + warp) * V.nbmax + blk] = m + logf(l);
+          float* shat_r = V.shat + (hrow + warp) * ((size_t)V.nbmax * BLK) + (size_t)blk * BLK;
+          shat_r[lane] = sn0;
+          shat_r[lane + 32] = sn1;
+          p0 = expf(sn0 - sm.M[warp]);
+          p1 = expf(sn1 - sm.M[warp]);
+        }
+        sm.p[warp][lane] = p0;
+        sm.p[warp][lane + 32] = p1;
+        __syncthreads();
+        const float4 pa = *reinterpret_cast<const float4*>(&sm.p[hp][8 * sub]);
+        const float4 pc = *reinterpret_cast<const float4*>(&sm.p[hp][8 * sub + 4]);
+        pv[0] = pa.x; pv[1] = pa.y; pv[2] = pa.z; pv[3] = pa.w;
+        pv[4] = pc.x; pv[5] = pc.y; pv[6] = pc.z; pv[7] = pc.w;
+      } else {
+        const float4 sa = T.s[hp * (BLK / 4) + 2 * sub], sb = T.s[hp * (BLK / 4) + 2 * sub + 1];
+        const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pv[i] = act ? __expf(sv[i] - Mh) : 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) lsum += pv[i];
+      // products p_t s_{t,g} 2^e of head hp at tokens 8 sub + [0, 8) as hi + lo halves,
+      // exchanged through shared memory as B fragments
+      {
+        const uint4 S0 = T.so[2 * sub], S1 = T.so[2 * sub + 1];   // (scale, offset), 8 tokens
+        const uint32_t sw[8] = {S0.x, S0.y, S0.z, S0.w, S1.x, S1.y, S1.z, S1.w};
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {   // token pair 4 sub + i
+          const float2 a = __half22float2(u32_as_h2(sw[2 * i])), c = __half22float2(u32_as_h2(sw[2 * i + 1]));
+          const float2 p2 = make_float2(pv[2 * i], pv[2 * i + 1]);
+          off = fmaf(p2.x, a.y, off);
+          off = fmaf(p2.y, c.y, off);
+          const float2 w = mul2(mul2(p2, make_float2(a.x, c.x)), make_float2(pre_v, pre_v));
+          const __half2 hi = __floats2half2_rn(w.x, w.y);
+          const float2 rem = sub2(w, __half22float2(hi));   // exact remainders
+          hw[i] = h2_as_u32(hi);
+          lw[i] = h2_as_u32(__floats2half2_rn(rem.x, rem.y));
+        }
+        uint32_t* wr = sm.bw[warp] + hp * (2 * MW_ROW) + 4 * sub;
+        *reinterpret_cast<uint4*>(wr) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(wr + MW_ROW) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      __syncwarp();
+      // column gid = (head gid>>1, hi or lo): k-step kk takes token pairs 8 tig + 2kk and
+      // 8 tig + 2kk + 1 (tokens 16 tig + 4kk + {0,1} and {2,3})
+      uint32_t bb0[4], bb1[4];
+      {
+        const uint32_t* rd = sm.bw[warp] + (gid >> 1) * (2 * MW_ROW) + (gid & 1) * MW_ROW + 8 * tig;
+        const uint4 B0 = *reinterpret_cast<const uint4*>(rd), B1 = *reinterpret_cast<const uint4*>(rd + 4);
+        bb0[0] = B0.x; bb1[0] = B0.y; bb0[1] = B0.z; bb1[1] = B0.w;
+        bb0[2] = B1.x; bb1[2] = B1.y; bb0[3] = B1.z; bb1[3] = B1.w;
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const uint4 C = T.codes[lane + 32 * mt];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          nib8_to_f16x4(word_of(C, kk), a0, a1, a2, a3);
+          mma16816(acc[mt], a0, a1, a2, a3, bb0[kk], bb1[kk]);
+        }
+      }
+      __syncwarp();   // every lane is done with the B words and this ring stage
+    }
+    cp_async_wait<0>();
+    __syncwarp();
+
+    // ---- this chunk's partial: l and acc[D] per head ----
+    off += __shfl_xor_sync(0xffffffffu, off, 1);   // head hp: its eight product lanes
+    off += __shfl_xor_sync(0xffffffffu, off, 2);
+    off += __shfl_xor_sync(0xffffffffu, off, 4);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
+    const float offh = __shfl_sync(0xffffffffu, off, 8 * tig);   // head tig
+    const float inv = 1.f / pre_v;
+    float* pp = V.part + (((size_t)hs * NCH + ch) * MAXREP) * (D + 4);
+    if (tig < V.n_rep) {
+      float* pr = pp + tig * (D + 4);
+      const int c0 = 32 * warp + gid;
+      pr[c0] = (acc[0][0] + acc[0][1]) * inv + offh;
+      pr[c0 + 8] = (acc[0][2] + acc[0][3]) * inv + offh;
+      pr[c0 + 16] = (acc[1][0] + acc[1][1]) * inv + offh;
+      pr[c0 + 24] = (acc[1][2] + acc[1][3]) * inv + offh;
+    }
+    if (warp == 0 && sub == 0 && act) pp[hp * (D + 4) + D] = lsum;   // every warp has the sums
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const unsigned int old = atomicAdd(&V.counters[CNT_MIX_EXIT], 1u);
+    if (old == gridDim.x - 1) {
+      V.counters[CNT_MIX_Q] = 0u;
+      V.counters[CNT_MIX_EXIT] = 0u;
+    }
+  }
+}
+
 int mixed_grid(int num_sms) { return num_sms * 4; }
 
 cudaError_t launch_mixed(const LayerView& V, int round, int grid, cudaStream_t st) {
+  if (round == 0 && V.v16 == nullptr) return launch_dependent(mixed_kernel_r0, dim3(grid), dim3(128), 0, st, V);
   return launch_dependent(mixed_kernel, dim3(grid), dim3(128), 0, st, V, round);
 }
 

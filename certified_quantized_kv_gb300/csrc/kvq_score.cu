@@ -58,24 +58,6 @@ struct __align__(16) ScoreHalf {   // row tiles 2h, 2h+1 of a block; the scales 
   uint4 scales[16];
 };
 
-__device__ __forceinline__ unsigned long long evict_first_policy() {
-  unsigned long long pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ void cp_async16_hint(void* dst_smem, const void* src, unsigned long long pol) {
-  const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
-               :: "r"(d), "l"(src), "l"(pol) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
 __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView V) {
   extern __shared__ __align__(16) unsigned char score_dsm[];
   const int warp = threadIdx.x >> 5;

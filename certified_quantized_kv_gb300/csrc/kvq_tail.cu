@@ -36,16 +36,6 @@ struct __align__(16) TailStage {
   float4 s[MAXREP * BLK / 4];          // [head][token]
 };
 
-__device__ __forceinline__ void cp16(void* dst_smem, const void* src, unsigned long long pol) {
-  const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
-               :: "r"(d), "l"(src), "l"(pol) : "memory");
-}
-
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
-  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
-}
-
 }  // namespace
 
 __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V, int runs) {
@@ -61,8 +51,7 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
   const int nwarps = gridDim.x * (blockDim.x >> 5);
   const int wid = blockIdx.x * (blockDim.x >> 5) + warp;
   const int NCH = V.nslot;
-  unsigned long long pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  const unsigned long long pol = evict_first_policy();
 
   for (int unit = wid; unit < V.BG * runs; unit += nwarps) {
     const int hs = unit / runs, run = unit % runs;
@@ -85,19 +74,19 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
         TailStage& T = ring[st];
         const uint4* vc = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) cp16(&T.codes[lane + 32 * j], vc + lane + 32 * j, pol);
+        for (int j = 0; j < 8; ++j) cp_async16_hint(&T.codes[lane + 32 * j], vc + lane + 32 * j, pol);
         const uint4* so = reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS);
-        cp16(&T.so[lane], so + lane, pol);
-        cp16(&T.so[lane + 32], so + lane + 32, pol);
+        cp_async16_hint(&T.so[lane], so + lane, pol);
+        cp_async16_hint(&T.so[lane + 32], so + lane + 32, pol);
 #pragma unroll
         for (int j = 0; j < 2; ++j) {   // 64 float4 of scores: head j * 2 + lane / 16
           const int idx = lane + 32 * j, h = idx >> 4;
           if (h < V.n_rep)
-            cp16(&T.s[idx], V.shat + (size_t)(hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)pb * BLK + 4 * (idx & 15), pol);
+            cp_async16_hint(&T.s[idx], V.shat + (size_t)(hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)pb * BLK + 4 * (idx & 15), pol);
         }
         pb = next_block(pb + 1);
       }
-      asm volatile("cp.async.commit_group;" ::: "memory");
+      cp_async_commit();
     };
 
     float acc[NG][2][4];
@@ -114,7 +103,7 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
     int it = 0;
     for (int blk = next_block(b0); blk < b1; blk = next_block(blk + 1), ++it) {
       issue((it + 1) % TAIL_STAGES);
-      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      cp_async_wait<1>();
       __syncwarp();
       const TailStage& T = ring[it % TAIL_STAGES];
       // weights of head hp at tokens 8 sub + [0, 8), prescaled by 2^e (exact)
@@ -170,7 +159,7 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
         __syncwarp();   // every lane has read the B words before the next group's
       }
     }
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    cp_async_wait<0>();
     __syncwarp();
 
     // head hp's sums are spread over its eight product lanes
