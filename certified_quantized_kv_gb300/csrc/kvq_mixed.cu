@@ -634,6 +634,7 @@ namespace {
 // FP16 keys are scored by the whole CTA (tier-2 read, then the dot products between two
 // barriers) and their weights handed to the warps through shared memory.
 constexpr int R0_STAGES = 2;
+static_assert(CHUNK <= 32, "one FP16-key flag per lane of a warp");
 
 struct __align__(16) R0Stage {   // one block, one value group
   float4 s[MAXREP * BLK / 4];    // INT8 scores [head][token]
@@ -693,28 +694,49 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
     }
 
     const int blk0 = ch * V.chunk, blk_end = min(V.nb, blk0 + V.chunk);
-    int pb = blk0;                 // producer: next block to copy
-    unsigned char kp_next = 0;     // FP16-key flag of the block copied last
+    const size_t bi0 = (size_t)hs * V.nbmax + blk0;
+    int pb = blk0;          // producer: next block to copy
+    unsigned kmask = 0;     // bit j: block blk0 + j has FP16 keys
+    auto issue_vals = [&](int st) {   // the group's INT4 codes and (scale, offset) of block pb
+      const size_t bi = bi0 + (pb - blk0);
+      R0Stage& T = ring[st];
+      const uint4* vc = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES) + warp * 64;
+      cp_async16_hint(&T.codes[lane], vc + lane, pol);
+      cp_async16_hint(&T.codes[lane + 32], vc + lane + 32, pol);
+      if (lane < BLK / 4)
+        cp_async16_hint(&T.so[lane], reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS + warp * BLK) + lane, pol);
+    };
+    auto issue_scores = [&](int st) {   // INT8 scores of block pb, unless its keys are FP16
+      if ((kmask >> (pb - blk0)) & 1u) return;
+      R0Stage& T = ring[st];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {   // 64 float4 of scores: head (lane + 32 j) / 16
+        const int idx = lane + 32 * j, h = idx >> 4;
+        if (h < V.n_rep)
+          cp_async16_hint(&T.s[idx], V.shat + (hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)pb * BLK + 4 * (idx & 15), pol);
+      }
+    };
     auto issue = [&](int st) {
       if (pb < blk_end) {
-        const size_t bi = (size_t)hs * V.nbmax + pb;
-        R0Stage& T = ring[st];
-        kp_next = V.kprom0[bi];
-        const uint4* vc = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES) + warp * 64;
-        cp_async16_hint(&T.codes[lane], vc + lane, pol);
-        cp_async16_hint(&T.codes[lane + 32], vc + lane + 32, pol);
-        if (lane < BLK / 4)
-          cp_async16_hint(&T.so[lane], reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS + warp * BLK) + lane, pol);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {   // 64 float4 of scores: head (lane + 32 j) / 16
-          const int idx = lane + 32 * j, h = idx >> 4;
-          if (h < V.n_rep)
-            cp_async16_hint(&T.s[idx], V.shat + (hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)pb * BLK + 4 * (idx & 15), pol);
-        }
+        issue_vals(st);
+        issue_scores(st);
         ++pb;
       }
       cp_async_commit();
     };
+    // the item's FP16-key flags (one block per lane), fetched while the first block is in
+    // flight; that block's scores are copied whatever its flag, so that no copy waits on it
+    {
+      const int nblk = blk_end - blk0;
+      const unsigned char f = (lane < nblk) ? V.kprom0[bi0 + lane] : 0;
+      if (nblk > 0) {
+        issue_vals(0);
+        issue_scores(0);   // kmask is still 0
+        ++pb;
+      }
+      cp_async_commit();
+      kmask = __ballot_sync(0xffffffffu, f != 0);
+    }
 
     float acc[2][4];
 #pragma unroll
@@ -724,9 +746,8 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
     float off = 0.f;    // sum p * offset: head hp, this lane's tokens, group = warp
     float lsum = 0.f;   // sum p: head hp, this lane's tokens
 
-    issue(0);
     for (int blk = blk0, it = 0; blk < blk_end; ++blk, ++it) {
-      const bool kp0 = kp_next != 0;
+      const bool kp0 = (kmask >> (blk - blk0)) & 1u;
       issue((it + 1) % R0_STAGES);
       cp_async_wait<1>();
       __syncwarp();
