@@ -19,15 +19,18 @@
 //   values in descending mass_b eta_b until the projected E_key + E_val <= eps.
 //
 // Work split: a persistent grid takes (KV group, run of up to 16 blocks) items from a
-// queue; short layers use shorter runs so that every CTA gets several items.
-// For each block the CTA first produces p_t = exp(s'_t - M) for the four query heads in
-// shared memory -- from the stored INT8 scores, or from FP16 keys read from tier 2 -- and
-// then each warp (one 32-channel value group) multiplies them into V: INT4 codes on the
-// tensor cores (channels as MMA rows, tokens as k, the eight MMA columns = four heads x
-// hi/lo halves of p * scale), FP16 values of promoted blocks on the CUDA cores.  M >= every
-// score, so no online rescaling is needed.  A second kernel combines the
-// chunk partials in a fixed order and writes the output, certificate and ladder plan.
-// (That combine runs as its own kernel, one CTA per sequence and query head.)
+// queue; short layers use shorter runs so that every CTA gets several items.  Each warp
+// owns one 32-channel value group and multiplies the weights p_t = exp(s'_t - M) of the
+// group's query heads into V: INT4 codes on the tensor cores (channels as MMA rows, tokens
+// as k, the eight MMA columns = four heads x hi/lo halves of p * scale), FP16 values on the
+// CUDA cores.  M >= every score, so no online rescaling is needed.
+//   mixed_kernel_r0 (first pass, INT4 values): a block that keeps its INT8 scores is
+//     handled by each warp alone, from its own cp.async ring; a block with FP16 keys is
+//     read from tier 2 and scored by the whole CTA.
+//   mixed_kernel (second pass; first pass with FP16 values in VRAM): the CTA forms each
+//     block's weights in shared memory, with a barrier per block.
+// combine_kernel (one CTA per sequence and query head) adds the item partials in a fixed
+// order and writes the output, the certificate and the ladder plan.
 #include "kvq_common.cuh"
 #include "kvq_blocksel.cuh"
 #include "kvq_launch.h"
