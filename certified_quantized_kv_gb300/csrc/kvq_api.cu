@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <cstdint>
 #include <string>
 #include <vector>
 
@@ -44,6 +45,7 @@ kvq_status cuda_fail(cudaError_t e, const char* where) {
   } while (0)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
 __global__ void fill_u32(uint32_t* p, uint32_t v, size_t n) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) p[i] = v;
@@ -457,6 +459,8 @@ kvq_status kvq_append(kvq_cache* c, int layer, const void* k, const void* v, int
   if (!k || !v) return fail(KVQ_ERR_INVALID, "kvq_append: NULL k or v");
   if (!is_device_ptr(k) || !is_device_ptr(v))
     return fail(KVQ_ERR_INVALID, "kvq_append: k and v must be device memory");
+  if (!aligned(k, 16) || !aligned(v, 16))   // read with 16-byte loads
+    return fail(KVQ_ERR_INVALID, "kvq_append: k and v must be 16-byte aligned");
   const int pos = c->n_tokens[layer];
   if ((long long)pos + n > c->cfg.max_ctx)
     return fail(KVQ_ERR_CAPACITY, "kvq_append: cache capacity (max_ctx) exceeded");
@@ -546,6 +550,12 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   const bool cert_dev = cert && is_device_ptr(cert);
   const bool lvl_dev = ladder_level && is_device_ptr(ladder_level);
   bool host_any = !q_dev || !out_dev || (cert && !cert_dev) || (ladder_level && !lvl_dev);
+  // device buffers are read and written in place with vector accesses (host buffers are
+  // staged through the cache's own)
+  if ((q_dev && !aligned(q, 16)) || (out_dev && !aligned(out, 16)))
+    return fail(KVQ_ERR_INVALID, f + ": device q and out must be 16-byte aligned");
+  if ((cert_dev && !aligned(cert, alignof(kvq_certificate))) || (lvl_dev && !aligned(ladder_level, 4)))
+    return fail(KVQ_ERR_INVALID, f + ": device cert must be 8-byte and ladder_level 4-byte aligned");
   const __half* qd = static_cast<const __half*>(q);
   if (!q_dev) {
     KVQ_CUDA(cudaMemcpyAsync(c->q_stage, q, HQ * D * 2, cudaMemcpyHostToDevice, st), "stage q");

@@ -174,6 +174,26 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
+// q . k over the D channels of one FP16 row in fp32, fused multiply-adds in channel order
+// (16-byte loads; both rows 16-byte aligned).
+__device__ __forceinline__ float dot_f16_row(const __half* q, const __half* k) {
+  const uint4* q4 = reinterpret_cast<const uint4*>(q);
+  const uint4* k4 = reinterpret_cast<const uint4*>(k);
+  float s = 0.f;
+#pragma unroll 4
+  for (int i = 0; i < D / 8; ++i) {
+    const uint4 qv = q4[i], kv = k4[i];
+    const uint32_t qw[4] = {qv.x, qv.y, qv.z, qv.w}, kw[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 qq = __half22float2(u32_as_h2(qw[j])), kk = __half22float2(u32_as_h2(kw[j]));
+      s = fmaf(qq.x, kk.x, s);
+      s = fmaf(qq.y, kk.y, s);
+    }
+  }
+  return s;
+}
+
 // Four INT8 codes stored offset binary (byte = code + 128; one 32-bit word) -> two
 // f16x2 registers, exactly: placed under the exponent pattern 0x64 a byte reads as the
 // half 1024 + byte, and subtracting 1152 leaves the code.  Every step is exact in binary16.

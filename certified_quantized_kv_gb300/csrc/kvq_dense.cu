@@ -65,17 +65,7 @@ __device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dens
     const __half* q = V.q + head_row(V, b, g, warp) * D;
     for (int t = lane; t < BLK; t += 32) {
       float s = -INFINITY;
-      if (t < V.n_tail) {
-        const __half* k = V.tail_k + ((size_t)hs * BLK + t) * D;
-        s = 0.f;
-        for (int c = 0; c < D; c += 2) {
-          const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(k + c));
-          const float2 qq = __half22float2(*reinterpret_cast<const __half2*>(q + c));
-          s = fmaf(qq.x, kk.x, s);
-          s = fmaf(qq.y, kk.y, s);
-        }
-        s *= INV_SQRT_D;
-      }
+      if (t < V.n_tail) s = dot_f16_row(q, V.tail_k + ((size_t)hs * BLK + t) * D) * INV_SQRT_D;
       sm.s[warp][t] = s;
     }
   }
@@ -92,8 +82,8 @@ __device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dens
     M = warp_max(M);
     float L = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int c = 0; c < nchv; ++c) {
+#pragma unroll 16
+    for (int c = 0; c < nchv; ++c) {   // sixteen partials' loads in flight per lane
       const float* pp = P + (size_t)c * MAXREP * (D + 4);
       const float w = expf(pp[D] - M);
       const float4 x = *reinterpret_cast<const float4*>(pp + 4 * lane);

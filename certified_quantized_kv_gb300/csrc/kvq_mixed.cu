@@ -414,15 +414,7 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   // (2) the partial FP16 block with exact scores
   float lt = 0.f;
   if (tid < V.n_tail) {
-    const __half* q = V.q + hb * D;
-    const __half* k = V.tail_k + ((size_t)hs * BLK + tid) * D;
-    float sc = 0.f;
-    for (int c = 0; c < D; c += 2) {
-      const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(k + c));
-      const float2 qq = __half22float2(*reinterpret_cast<const __half2*>(q + c));
-      sc = fmaf(qq.x, kk.x, sc);
-      sc = fmaf(qq.y, kk.y, sc);
-    }
+    const float sc = dot_f16_row(V.q + hb * D, V.tail_k + ((size_t)hs * BLK + tid) * D);
     lt = expf(sc * INV_SQRT_D - hsd.M);
     tail_p[tid] = lt;
   }

@@ -13,6 +13,8 @@
 // contents; each call clears the counters it needs before its kernel runs.  Calls
 // whose kernels overlap on the GPU (two streams, or two host threads) race on the
 // array and must be serialised by the caller.
+#include <cstdint>
+#include <initializer_list>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -218,6 +220,12 @@ extern "C" kvq_status kvq_dense_decode_noalloc(const void* q, const void* k, con
   if (!is_device(q) || !is_device(k) || !is_device(v) || !is_device(out)) {
     kvq::set_last_error("kvq_dense_decode_noalloc: q, k, v and out must be device memory");
     return KVQ_ERR_INVALID;
+  }
+  for (const void* p : {q, k, v, static_cast<const void*>(out)}) {
+    if (reinterpret_cast<uintptr_t>(p) % 16 != 0) {   // 16-byte vector accesses
+      kvq::set_last_error("kvq_dense_decode_noalloc: q, k, v and out must be 16-byte aligned");
+      return KVQ_ERR_INVALID;
+    }
   }
   const int BG = batch * n_kv_heads;
   const int nch = (n_tokens + NA_CHUNK * BLK - 1) / (NA_CHUNK * BLK);

@@ -262,15 +262,7 @@ __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
   // exact scores of the partial FP16 block (counts as covered)
   float tmax = -INFINITY;
   if (tid < V.n_tail) {
-    const __half* q = V.q + hb * D;
-    const __half* k = V.tail_k + ((size_t)hs * BLK + tid) * D;
-    float sc = 0.f;
-    for (int c = 0; c < D; c += 2) {
-      const float2 kk = __half22float2(*reinterpret_cast<const __half2*>(k + c));
-      const float2 qq = __half22float2(*reinterpret_cast<const __half2*>(q + c));
-      sc = fmaf(qq.x, kk.x, sc);
-      sc = fmaf(qq.y, kk.y, sc);
-    }
+    float sc = dot_f16_row(V.q + hb * D, V.tail_k + ((size_t)hs * BLK + tid) * D);
     sc *= INV_SQRT_D;
     tail_s[tid] = sc;
     tmax = sc;

@@ -122,15 +122,16 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out);
 kvq_status kvq_cache_destroy(kvq_cache* cache);
 
 /* kvq_append -- quantise-and-append `n_tokens` new tokens to every sequence of `layer`
- * (Method §1).  k and v are caller-owned device buffers [B, Hkv, n_tokens, D] of FP16.
+ * (Method §1).  k and v are caller-owned device buffers [B, Hkv, n_tokens, D] of FP16,
+ * 16-byte aligned.
  * Full 64-token blocks are quantised into tier 1 (INT8 keys with one fp16 scale per
  * block and channel; INT4 values with fp16 scale and offset per token and 32-channel
  * group; eta_b = max |v - v_hat| over the block); the partial last block stays FP16 in
  * VRAM until it fills.  Every token is also mirrored to tier 2 by a copy on an internal
  * side stream that `stream` waits for before any later work, so k and v may be reused
  * by later work on `stream`.  n_tokens = 0 is a no-op.
- * Errors: KVQ_ERR_INVALID (layer out of range, NULL buffers, n_tokens < 0),
- * KVQ_ERR_CAPACITY (length would exceed max_ctx), KVQ_ERR_CUDA. */
+ * Errors: KVQ_ERR_INVALID (layer out of range, NULL, host or unaligned buffers,
+ * n_tokens < 0), KVQ_ERR_CAPACITY (length would exceed max_ctx), KVQ_ERR_CUDA. */
 kvq_status kvq_append(kvq_cache* cache, int layer, const void* k, const void* v,
                       int n_tokens, void* stream);
 
@@ -144,11 +145,12 @@ kvq_status kvq_append(kvq_cache* cache, int layer, const void* k, const void* v,
  *   cert         [B * Hq] certificates (may be NULL), device or host memory
  *   ladder_level [B] highest rung reached per sequence (may be NULL), device or host
  * If any of q, out, cert or ladder_level is host memory, the call stages it through
- * device buffers and synchronises `stream` before returning.  Tier-2 blocks are read
+ * device buffers and synchronises `stream` before returning.  Device buffers are used in
+ * place and must be aligned: q and out to 16 bytes, cert to 8, ladder_level to 4.  Tier-2 blocks are read
  * directly by the kernels through the host link (NVLink-C2C); no host round trip
  * happens inside the call.
  * Errors: KVQ_ERR_INVALID (layer out of range, empty layer, tau_cov outside (0, 1],
- * eps < 0 or NaN, NULL q/out), KVQ_ERR_CUDA. */
+ * eps < 0 or NaN, NULL q/out, unaligned device buffers), KVQ_ERR_CUDA. */
 kvq_status kvq_decode_attention(kvq_cache* cache, int layer, const void* q, float tau_cov,
                                 float eps, void* out, kvq_certificate* cert,
                                 int32_t* ladder_level, void* stream);
@@ -164,7 +166,8 @@ kvq_status kvq_decode_attention(kvq_cache* cache, int layer, const void* q, floa
  *                   level 0, k_star 0, n_val_promoted 0, promoted_bytes 0.
  * Debug flags that force rungs are ignored.  The selection state it leaves (nothing
  * selected) is what kvq_export_decode_state reports afterwards.
- * Errors: KVQ_ERR_INVALID (layer out of range, empty layer, NULL q/out), KVQ_ERR_CUDA. */
+ * Errors: KVQ_ERR_INVALID (layer out of range, empty layer, NULL q/out, unaligned
+ * device buffers), KVQ_ERR_CUDA. */
 kvq_status kvq_decode_attention_uncertified(kvq_cache* cache, int layer, const void* q,
                                             void* out, kvq_certificate* cert, void* stream);
 
@@ -233,6 +236,7 @@ kvq_status kvq_residency_stats(kvq_cache* cache, int layer, int64_t* resident_by
  * cudaMalloc, cudaFree or any allocating routine.
  *   q   [B, Hq, D] FP16, device;  k, v [B, Hkv, n_tokens, D] FP16, device
  *   out [B, Hq, D] FP16, device (caller-owned);  Hq / Hkv in 1..4, n_tokens >= 1
+ *   q, k, v and out 16-byte aligned
  * Size limit: B * Hkv * ceil(n_tokens / 1024) * 2112 bytes of partials (plus a few
  * counters) must fit in the 8 MiB array, e.g. B * Hkv = 8 with up to 507904 tokens.
  * The array exists once per device that loads the library and is held until the
@@ -240,7 +244,7 @@ kvq_status kvq_residency_stats(kvq_cache* cache, int layer, int64_t* resident_by
  * array's device address; make that first call before any stream capture.  Every call
  * shares the array and clears the counters it needs itself; calls whose work overlaps
  * on the GPU (other streams, other host threads) race on it and must be serialised.
- * Stream-ordered.  Errors: KVQ_ERR_INVALID (NULL or host pointers, bad shape),
+ * Stream-ordered.  Errors: KVQ_ERR_INVALID (NULL, host or unaligned pointers, bad shape),
  * KVQ_ERR_CAPACITY (beyond the size limit), KVQ_ERR_CUDA. */
 kvq_status kvq_dense_decode_noalloc(const void* q, const void* k, const void* v, int batch,
                                     int n_q_heads, int n_kv_heads, int n_tokens, void* out,

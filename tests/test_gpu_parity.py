@@ -185,6 +185,66 @@ def test_errors():
     assert e.value.status == kvq.KVQ_ERR_INVALID
 
 
+def _offset_view(shape, dtype, byte_offset):
+    """A contiguous CUDA tensor of `shape` that starts `byte_offset` bytes into an
+    allocation (torch's CUDA allocations start 256-byte aligned)."""
+    es = torch.empty(0, dtype=dtype).element_size()
+    assert byte_offset % es == 0
+    n = math.prod(shape)
+    raw = torch.zeros(n * es + 256, dtype=torch.uint8, device="cuda")
+    return raw[byte_offset:byte_offset + n * es].view(dtype).view(shape)
+
+
+def test_unaligned_device_buffers_are_rejected():
+    """The kernels read and write device buffers in place with vector accesses; buffers
+    that are not aligned for them are refused before anything is enqueued, and the cache
+    stays usable."""
+    cache = kvq.Cache(1, 1, 4, 1, max_ctx=256)
+    try:
+        k = torch.randn(1, 1, 100, 128, device="cuda").half()
+        kb = _offset_view((1, 1, 100, 128), torch.float16, 2)
+        kb.copy_(k)
+        assert kb.data_ptr() % 16 == 2
+        with pytest.raises(kvq.KvqError) as e:
+            cache.append(0, kb, k)
+        assert e.value.status == kvq.KVQ_ERR_INVALID and "aligned" in str(e.value)
+        assert cache.length(0) == 0
+        cache.append(0, k, k)
+        q = torch.randn(1, 4, 128, device="cuda").half()
+        out = torch.empty_like(q)
+        qb = _offset_view((1, 4, 128), torch.float16, 8)
+        qb.copy_(q)
+        ob = _offset_view((1, 4, 128), torch.float16, 6)
+        for qq, oo in [(qb, out), (q, ob)]:
+            with pytest.raises(kvq.KvqError) as e:
+                cache.decode(0, qq, 0.9, 0.25, oo)
+            assert e.value.status == kvq.KVQ_ERR_INVALID
+            with pytest.raises(kvq.KvqError) as e:
+                cache.decode_uncertified(0, qq, oo)
+            assert e.value.status == kvq.KVQ_ERR_INVALID
+        cert_bad = _offset_view((4 * 32,), torch.uint8, 4)
+        lvl_bad = _offset_view((8,), torch.uint8, 2)
+        for cb, lb in [(cert_bad, None), (None, lvl_bad)]:
+            with pytest.raises(kvq.KvqError) as e:
+                cache.decode(0, q, 0.9, 0.25, out, cert=cb, ladder_level=lb)
+            assert e.value.status == kvq.KVQ_ERR_INVALID
+        torch.cuda.synchronize()
+        cache.decode(0, q, 0.9, 0.25, out)           # still usable
+        ref = torch.empty_like(q)
+        cache.decode(0, qb.clone(), 0.9, 0.25, ref)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    finally:
+        cache.close()
+    q = torch.randn(1, 4, 128, device="cuda").half()
+    k = torch.randn(1, 1, 64, 128, device="cuda").half()
+    out = torch.empty_like(q)
+    qb = _offset_view((1, 4, 128), torch.float16, 2)
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.dense_decode_noalloc(qb, k, k, out)
+    assert e.value.status == kvq.KVQ_ERR_INVALID
+
+
 # ---------------------------------------------------------------------------------
 # value tolerance v_tol (Results: structured reasoning)
 # ---------------------------------------------------------------------------------
