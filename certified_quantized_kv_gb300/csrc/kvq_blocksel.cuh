@@ -145,7 +145,15 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
   uint32_t prefix = 0;
   unsigned long long above = 0;
   int level = 0, ncand = 0;
-  for (; level < 3; ++level) {
+  if (n <= SEL_CAND) {
+    // every key fits the exact ranking: no histogram level (keys are below 2^30, so
+    // with the 30-bit shift below, prefix 0 makes every nonzero key a candidate)
+    level = -1;
+    int cnt = 0;
+    for (int i = i0; i < i1; ++i) cnt += keys[i] != 0u;
+    ncand = block_sum_int(cnt, ws.red);
+  }
+  for (; level >= 0 && level < 3; ++level) {
     const int sh = 20 - 10 * level;
     for (int d = lane; d < 1024; d += 32) ws.hist[warp][d] = 0ull;
     __syncwarp();
