@@ -264,10 +264,18 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
   if (!(k.v_tol >= 0.f)) return fail(KVQ_ERR_INVALID, "v_tol must be >= 0 (0: no value budget)");
   if (k.resident_blocks < 0) return fail(KVQ_ERR_INVALID, "resident_blocks must be >= 0");
 
+  int dev = 0, sms = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de == cudaSuccess) de = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (de != cudaSuccess || sms < 1) {
+    cudaGetLastError();
+    return fail(KVQ_ERR_CUDA, std::string("kvq_cache_create: no usable CUDA device: ") +
+                                  (de != cudaSuccess ? cudaGetErrorString(de) : "no multiprocessors"));
+  }
   kvq_cache* c = new kvq_cache();
   c->cfg = k;
-  cudaGetDevice(&c->device);
-  cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  c->device = dev;
+  c->num_sms = sms;
   c->B = k.batch; c->Hq = k.n_q_heads; c->Hkv = k.n_kv_heads; c->n_rep = k.n_q_heads / k.n_kv_heads;
   c->BG = c->B * c->Hkv; c->L = k.n_layers;
   c->nbmax_used = k.max_ctx / BLK;
@@ -298,10 +306,15 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
     free_all(c);
     return fail(KVQ_ERR_OOM, "tier-1 device allocation failed");
   }
-  cudaMemset(c->t1, 0, c->t1_layer * c->L);
-  for (int l = 0; l < c->L; ++l) {
+  cudaError_t ie = cudaMemset(c->t1, 0, c->t1_layer * c->L);
+  for (int l = 0; l < c->L && ie == cudaSuccess; ++l) {
     fill_u32<<<64, 256>>>(layer_vmin(c, l), 0xFF800000u, BG * D);  // encoding of +inf
     fill_u32<<<64, 256>>>(layer_vmax(c, l), 0x007FFFFFu, BG * D);  // encoding of -inf
+    ie = cudaGetLastError();
+  }
+  if (ie != cudaSuccess) {
+    free_all(c);
+    return fail(KVQ_ERR_CUDA, std::string("kvq_cache_create: tier-1 initialisation: ") + cudaGetErrorString(ie));
   }
 
   // ---- tier 2: pinned, mapped host memory ----

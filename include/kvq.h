@@ -115,7 +115,8 @@ typedef struct kvq_cache kvq_cache;
 /* kvq_cache_create -- allocate tier 1 (device), tier 2 (pinned, mapped host memory) and
  * scratch for `n_layers` layers of `batch` sequences of up to `max_ctx` tokens (Method §1).
  * The library owns all of it until kvq_cache_destroy.  Uses the current CUDA device.
- * Errors: KVQ_ERR_INVALID (cfg NULL or unsupported), KVQ_ERR_OOM, KVQ_ERR_HOST_OOM. */
+ * Errors: KVQ_ERR_INVALID (cfg NULL or unsupported), KVQ_ERR_OOM, KVQ_ERR_HOST_OOM,
+ * KVQ_ERR_CUDA (no usable CUDA device, or initialising tier 1 failed). */
 kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out);
 
 /* kvq_cache_destroy -- synchronise the device and free everything.  NULL is a no-op. */

@@ -63,3 +63,18 @@ def test_resident_blocks_validated_without_gpu():
     assert lib.kvq_cache_create(ctypes.byref(cfg), ctypes.byref(h)) == kvq.KVQ_ERR_INVALID
     assert b"resident_blocks" in lib.kvq_last_error()
     assert lib.kvq_residency_stats(None, 0, None, None, None, 0) == kvq.KVQ_ERR_INVALID
+
+
+def test_create_without_device_reports_cuda_error():
+    """A valid configuration on a machine without a usable GPU fails with KVQ_ERR_CUDA and
+    says why (rather than reporting an out-of-memory)."""
+    lib = _lib()
+    cfg = kvq.kvq_config(1, 1, 4, 1, 128, 64, 32, 1024, 1, 0.5)
+    h = ctypes.c_void_p()
+    st = lib.kvq_cache_create(ctypes.byref(cfg), ctypes.byref(h))
+    if st == kvq.KVQ_OK:   # a GPU is present: nothing to check here
+        lib.kvq_cache_destroy(h)
+        import pytest
+        pytest.skip("a CUDA device is present")
+    assert st == kvq.KVQ_ERR_CUDA, (st, lib.kvq_last_error())
+    assert b"no usable CUDA device" in lib.kvq_last_error()
