@@ -104,6 +104,22 @@ def _ptr(t) -> int | None:
     return None if t is None else t.data_ptr()
 
 
+def _need(t, name, dtype, shape=None, nbytes=None):
+    """Check a tensor argument before its pointer crosses the C ABI (which sees only the
+    address): contiguous, of `dtype`, and of `shape` or `nbytes` when given."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if nbytes is not None and t.numel() * t.element_size() < nbytes:
+        raise ValueError(f"{name} must hold at least {nbytes} bytes")
+
+
 def _stream(stream) -> int | None:
     import torch
     if stream is None:
@@ -156,14 +172,22 @@ class Cache:
 
     def append(self, layer: int, k, v, stream=None):
         """k, v: contiguous fp16 CUDA tensors [B, Hkv, n, 128]."""
-        assert k.is_contiguous() and v.is_contiguous() and k.shape == v.shape
+        import torch
+        if k.dim() != 4:
+            raise ValueError("k must be [batch, n_kv_heads, n_tokens, 128]")
+        shape = (self.batch, self.n_kv_heads, k.shape[2], HEAD_DIM)
+        _need(k, "k", torch.float16, shape)
+        _need(v, "v", torch.float16, shape)
         _check(self.lib.kvq_append(self.handle, layer, _ptr(k), _ptr(v), k.shape[2], _stream(stream)))
 
     def decode(self, layer: int, q, tau_cov: float, eps: float, out, cert=None, ladder_level=None,
                stream=None):
         """q, out: contiguous fp16 tensors [B, Hq, 128] (device or host); cert: uint8 tensor
         of B*Hq*32 bytes or None; ladder_level: int32 tensor [B] or None."""
-        assert q.is_contiguous() and out.is_contiguous()
+        self._check_decode_args(q, out, cert)
+        if ladder_level is not None:
+            import torch
+            _need(ladder_level, "ladder_level", torch.int32, (self.batch,))
         st = _stream(stream) if (q.is_cuda or out.is_cuda) else None
         _check(self.lib.kvq_decode_attention(self.handle, layer, _ptr(q), float(tau_cov), float(eps),
                                              _ptr(out), _ptr(cert), _ptr(ladder_level), st))
@@ -171,10 +195,18 @@ class Cache:
     def decode_uncertified(self, layer: int, q, out, cert=None, stream=None):
         """Plain INT8/INT4 decode attention, nothing paged in and no ladder
         (kvq_decode_attention_uncertified); cert receives the unenforced bounds."""
-        assert q.is_contiguous() and out.is_contiguous()
+        self._check_decode_args(q, out, cert)
         st = _stream(stream) if (q.is_cuda or out.is_cuda) else None
         _check(self.lib.kvq_decode_attention_uncertified(self.handle, layer, _ptr(q), _ptr(out),
                                                          _ptr(cert), st))
+
+    def _check_decode_args(self, q, out, cert):
+        import torch
+        shape = (self.batch, self.n_q_heads, HEAD_DIM)
+        _need(q, "q", torch.float16, shape)
+        _need(out, "out", torch.float16, shape)
+        if cert is not None:
+            _need(cert, "cert", torch.uint8, nbytes=self.batch * self.n_q_heads * CERT_DTYPE.itemsize)
 
     def export_tier1(self, layer: int, stream=None) -> dict:
         """Tier-1 contents of `layer` in canonical layout, as CUDA tensors."""
@@ -238,9 +270,15 @@ def dense_decode_noalloc(q, k, v, out, stream=None):
     [B, Hq, 128]; k, v: device fp16 [B, Hkv, n_tokens, 128].  Its scratch is a fixed
     8 MiB device array shared by every call, so overlapping calls must be serialised.
     """
-    assert q.is_contiguous() and k.is_contiguous() and v.is_contiguous() and out.is_contiguous()
+    import torch
+    if q.dim() != 3 or k.dim() != 4:
+        raise ValueError("q must be [batch, n_q_heads, 128] and k, v [batch, n_kv_heads, n_tokens, 128]")
     B, Hq, _ = q.shape
     Hkv, N = k.shape[1], k.shape[2]
+    _need(q, "q", torch.float16, (B, Hq, HEAD_DIM))
+    _need(k, "k", torch.float16, (B, Hkv, N, HEAD_DIM))
+    _need(v, "v", torch.float16, (B, Hkv, N, HEAD_DIM))
+    _need(out, "out", torch.float16, (B, Hq, HEAD_DIM))
     _check(load_library().kvq_dense_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N,
                                                    _ptr(out), _stream(stream)))
 

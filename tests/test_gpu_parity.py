@@ -226,11 +226,22 @@ def test_unaligned_device_buffers_are_rejected():
                 cache.decode_uncertified(0, qq, oo)
             assert e.value.status == kvq.KVQ_ERR_INVALID
         cert_bad = _offset_view((4 * 32,), torch.uint8, 4)
+        with pytest.raises(kvq.KvqError) as e:
+            cache.decode(0, q, 0.9, 0.25, out, cert=cert_bad)
+        assert e.value.status == kvq.KVQ_ERR_INVALID
+        # an int32 tensor is always 4-byte aligned, so the misaligned ladder-level buffer
+        # goes to the C entry point directly
         lvl_bad = _offset_view((8,), torch.uint8, 2)
-        for cb, lb in [(cert_bad, None), (None, lvl_bad)]:
-            with pytest.raises(kvq.KvqError) as e:
-                cache.decode(0, q, 0.9, 0.25, out, cert=cb, ladder_level=lb)
-            assert e.value.status == kvq.KVQ_ERR_INVALID
+        st = cache.lib.kvq_decode_attention(cache.handle, 0, q.data_ptr(), 0.9, 0.25, out.data_ptr(),
+                                            None, lvl_bad.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert st == kvq.KVQ_ERR_INVALID
+        # the binding refuses wrong dtypes and shapes before the C call
+        with pytest.raises(ValueError):
+            cache.decode(0, q.float(), 0.9, 0.25, out)
+        with pytest.raises(ValueError):
+            cache.decode(0, q[:, :2].contiguous(), 0.9, 0.25, out)
+        with pytest.raises(ValueError):
+            cache.append(0, k.float(), k.float())
         torch.cuda.synchronize()
         cache.decode(0, q, 0.9, 0.25, out)           # still usable
         ref = torch.empty_like(q)
