@@ -109,6 +109,38 @@ def test_c3_layer_128k_uncertified_sampled_groups():
             assert np.all(np.abs(gv - ov) <= BOUND_RTOL * np.abs(ov) + BOUND_ATOL), name
 
 
+def test_c4_planted_needle_64k_b8_rung4():
+    """The planted-needle workload at full size (B = 8, 64K tokens, 32 query / 8 KV heads):
+    INT8 rounding reverses the top block of every KV group, so every ranking check fails,
+    every sequence takes rung 4 and every head returns dense attention over the FP16
+    originals with E_key = E_val = 0.  Sampled heads are compared with the oracle's dense
+    attention in float64."""
+    from _parity import OUT_ATOL, OUT_RTOL
+    q, K, V, info = W.c4(device="cuda")
+    B, Hq, D = q.shape
+    Hkv, N = K.shape[1], K.shape[2]
+    cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=N)
+    try:
+        cache.append(0, K.half().contiguous(), V.half().contiguous())
+        qh = q.half().contiguous()
+        out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+        cert = torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda")
+        lvl = torch.empty(B, dtype=torch.int32, device="cuda")
+        cache.decode(0, qh, 0.995, 0.25, out, cert, lvl)
+        torch.cuda.synchronize()
+    finally:
+        cache.close()
+    c = kvq.certificates(cert).reshape(B, Hq)
+    assert np.all(lvl.cpu().numpy() == 4)
+    assert np.all(c["level"] == 4) and np.all(c["e_key"] == 0) and np.all(c["e_val"] == 0)
+    n_rep = Hq // Hkv
+    for b, h in [(0, 0), (3, 13), (7, 31)]:
+        g = h // n_rep
+        o = O.dense_attention(qh[b, h].cpu().numpy(), K[b, g].half().cpu().numpy(), V[b, g].half().cpu().numpy())
+        err = np.abs(out[b, h].cpu().float().numpy() - o)
+        assert np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(o)), (b, h, float(err.max()))
+
+
 def test_max_context_2m_tokens():
     """The largest cache a sequence may hold (max_ctx = 2,097,152 tokens: 32,768 blocks,
     the selection keeps one key per block in shared memory), one KV group of four query
