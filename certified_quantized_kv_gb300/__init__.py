@@ -82,6 +82,7 @@ def load_library() -> ctypes.CDLL:
         "kvq_export_decode_state": [vp, vp, vp, vp, vp, vp, vp, vp],
         "kvq_profile_read": [vp, ctypes.POINTER(kvq_kernel_stat), i32, ctypes.POINTER(i32), i32],
         "kvq_dense_decode_noalloc": [vp, vp, vp, i32, i32, i32, i32, vp, vp],
+        "kvq_debug_fill_tier2": [vp, i32, ctypes.c_uint16],
         "kvq_residency_stats": [vp, i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
                                 ctypes.POINTER(i32), i32],
     }
@@ -255,6 +256,11 @@ class Cache:
         _check(self.lib.kvq_residency_stats(self.handle, layer, ctypes.byref(hit), ctypes.byref(host),
                                             ctypes.byref(used), int(reset)))
         return {"resident_bytes": hit.value, "host_bytes": host.value, "slots_in_use": used.value}
+
+    def debug_fill_tier2(self, layer: int, bits: int):
+        """Test aid (kvq_debug_fill_tier2): overwrite `layer`'s tier-2 FP16 originals with
+        the binary16 bit pattern `bits`, after the device has finished queued work."""
+        _check(self.lib.kvq_debug_fill_tier2(self.handle, layer, int(bits) & 0xFFFF))
 
     def profile_read(self, reset: bool = True) -> dict:
         arr = (kvq_kernel_stat * 16)()

@@ -735,4 +735,19 @@ kvq_status kvq_residency_stats(kvq_cache* c, int layer, int64_t* resident_bytes,
   return KVQ_OK;
 }
 
+kvq_status kvq_debug_fill_tier2(kvq_cache* c, int layer, uint16_t bits) {
+  if (!c) return fail(KVQ_ERR_INVALID, "kvq_debug_fill_tier2: NULL cache");
+  if (layer < 0 || layer >= c->L) return fail(KVQ_ERR_INVALID, "kvq_debug_fill_tier2: layer out of range");
+  DeviceGuard dg(c->device);
+  KVQ_CUDA(cudaDeviceSynchronize(), "kvq_debug_fill_tier2: sync");   // no copy or kernel in flight
+  const size_t n = (size_t)c->BG * c->cap * D;
+  uint16_t* k = reinterpret_cast<uint16_t*>(c->t2k_host[layer]);
+  std::fill(k, k + n, bits);
+  if (!c->v16) {
+    uint16_t* v = reinterpret_cast<uint16_t*>(c->t2v_host[layer]);
+    std::fill(v, v + n, bits);
+  }
+  return KVQ_OK;
+}
+
 }  // extern "C"

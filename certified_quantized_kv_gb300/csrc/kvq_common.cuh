@@ -281,12 +281,6 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-
 // Power-of-two prescale so that |x| * 2^e <= 2^14 for |x| <= xmax (keeps split halves
 // normal and far from overflow).  Returns 2^e as a float.
 __device__ __forceinline__ float prescale_for(float xmax) {

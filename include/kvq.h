@@ -227,6 +227,13 @@ kvq_status kvq_profile_read(kvq_cache* cache, kvq_kernel_stat* stats, int max, i
 kvq_status kvq_residency_stats(kvq_cache* cache, int layer, int64_t* resident_bytes,
                                int64_t* host_bytes, int32_t* slots_in_use, int reset);
 
+/* kvq_debug_fill_tier2 -- a test aid, not part of the paper: waits for the device, then
+ * overwrites every FP16 element of `layer`'s tier 2 (the keys, and the values when they
+ * live there) with the binary16 bit pattern `bits`.  Calls that page blocks in from
+ * tier 2 afterwards see the pattern, so a test can show which passes never read it.
+ * Errors: KVQ_ERR_INVALID (NULL cache, layer out of range), KVQ_ERR_CUDA. */
+kvq_status kvq_debug_fill_tier2(kvq_cache* cache, int layer, uint16_t bits);
+
 /* kvq_dense_decode_noalloc -- exact dense FP16 decode attention that allocates no memory.
  * The paper has no counterpart to this call.  It is for callers that cannot allocate
  * device memory when they call: a process whose device memory is fully held by another

@@ -46,6 +46,7 @@ def test_null_and_invalid_arguments_without_gpu():
     assert lib.kvq_decode_attention(None, 0, None, 0.9, 0.25, None, None, None, None) == kvq.KVQ_ERR_INVALID
     assert lib.kvq_decode_attention_uncertified(None, 0, None, None, None, None) == kvq.KVQ_ERR_INVALID
     assert b"kvq_decode_attention_uncertified" in lib.kvq_last_error()
+    assert lib.kvq_debug_fill_tier2(None, 0, 0) == kvq.KVQ_ERR_INVALID
 
 
 def test_certificate_layout_matches_header():

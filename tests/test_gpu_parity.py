@@ -273,6 +273,35 @@ def test_value_tolerance(v_tol):
     assert np.any(c["level"] == 2)
 
 
+def test_tier1_passes_never_read_tier2():
+    """The scoring pass, the selection, the INT8/INT4 pass and its combine use tier 1 only
+    (the bounds' inputs come without FP16 data, Method §2): the uncertified call gives
+    bit-identical outputs and bounds after tier 2 is overwritten with NaN, while a dense
+    call (tau_cov = 1, every block read from tier 2) then returns NaN."""
+    q, K, V = W.tiny(seed=80, ctx=64 * 40 + 5, Hq=8, Hkv=2, batch=2, kscale=3.0)
+    cache = kvq.Cache(1, 2, 8, 2, max_ctx=64 * 41)
+    try:
+        cache.append(0, K.cuda().contiguous(), V.cuda().contiguous())
+        qd = q.cuda().contiguous()
+        runs = []
+        for poison in (False, True):
+            if poison:
+                cache.debug_fill_tier2(0, 0x7E00)   # binary16 NaN
+            out = torch.empty(2, 8, 128, dtype=torch.float16, device="cuda")
+            cert = torch.empty(2 * 8 * 32, dtype=torch.uint8, device="cuda")
+            cache.decode_uncertified(0, qd, out, cert)
+            torch.cuda.synchronize()
+            runs.append((out.cpu(), cert.cpu()))
+        assert torch.equal(runs[0][0], runs[1][0]) and torch.equal(runs[0][1], runs[1][1])
+        assert torch.isfinite(runs[1][0].float()).all()
+        out = torch.empty(2, 8, 128, dtype=torch.float16, device="cuda")
+        cache.decode(0, qd, 1.0, 0.25, out)
+        torch.cuda.synchronize()
+        assert torch.isnan(out.float()).all()
+    finally:
+        cache.close()
+
+
 def test_token_by_token_appends_feed_tier2():
     """One token per append (the serving loop): tokens that stay in the partial block are
     mirrored to tier 2 from the partial-block buffer without a join; blocks they later
