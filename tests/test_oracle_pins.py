@@ -675,3 +675,40 @@ def test_v_tol_budget_holds_and_tightening_pages_in_more_values():
     b = O.decode_layer(q, K, V, t1, 0.99, 0.5, O.OracleConfig(n_rep=4, v_tol=math.inf))
     assert np.array_equal(a.level, b.level) and np.array_equal(a.out64, b.out64)
 
+
+
+# ---------------------------------------------------------------------------------
+# A4 value ranges: every cached token counts, the partial FP16 block included
+# ---------------------------------------------------------------------------------
+
+def test_value_range_includes_partial_block():
+    """Method §2 computes E_key from the range of the exact values; the range is taken
+    over every cached token, so an extreme value in the partial (not yet quantised)
+    block sets it, and E_key scales with it."""
+    rng = np.random.default_rng(41)
+    ctx = 64 * 3 + 10
+    V = rng.standard_normal((1, 1, ctx, 128)).astype(np.float16)
+    V[0, 0, 64 * 3 + 4, 7] = 50.0          # in the partial block
+    V[0, 0, 64 * 3 + 9, 9] = -40.0
+    K = rng.standard_normal((1, 1, ctx, 128)).astype(np.float16)
+    t1 = O.quantize_layer(K, V)
+    full = V[0, 0].astype(np.float32)
+    assert np.array_equal(t1.vmax[0, 0], full.max(axis=0)) and np.array_equal(t1.vmin[0, 0], full.min(axis=0))
+    assert t1.vmax[0, 0, 7] == 50.0 and t1.vmin[0, 0, 9] == -40.0
+    # a single token: the range is zero and so is E_key, whatever the key error
+    t_one = O.quantize_layer(K[:, :, :1], V[:, :, :1])
+    assert np.all(t_one.vmax == t_one.vmin)
+    # E_key is linear in R: the same head with the outliers removed from the partial block
+    V2 = V.copy()
+    V2[0, 0, 64 * 3 + 4, 7] = 0.0
+    V2[0, 0, 64 * 3 + 9, 9] = 0.0
+    q = rng.standard_normal((1, 1, 128)).astype(np.float16)   # one head: one selection
+    r1 = O.decode_layer(q, K, V, t1, 0.3, math.inf, O.OracleConfig(n_rep=1))
+    t2 = O.quantize_layer(K, V2)
+    r2 = O.decode_layer(q, K, V2, t2, 0.3, math.inf, O.OracleConfig(n_rep=1))
+    R1 = float(np.max(t1.vmax[0, 0].astype(np.float64) - t1.vmin[0, 0]))
+    R2 = float(np.max(t2.vmax[0, 0].astype(np.float64) - t2.vmin[0, 0]))
+    assert R1 >= 50.0 and R2 < 15.0
+    assert not r1.kprom0.all()              # INT8 blocks remain: E_key > 0
+    assert r2.e_key0[0, 0] > 0                # (round-0 bounds, before any rung)
+    assert abs(r1.e_key0[0, 0] / r2.e_key0[0, 0] - R1 / R2) <= 1e-12 * R1 / R2
