@@ -136,6 +136,111 @@ def oracle_sample(wl: dict, groups: int = 1) -> dict:
     return {"t_layer_s": t_layer, "sample_s": total, "groups": groups}
 
 
+# ---------------------------------------------------------------------------------
+# the oracle on every host core: one process per (sequence, KV head) group
+# ---------------------------------------------------------------------------------
+
+def _oracle_group_worker(idx, q, K, V, tau, eps, n_rep, barrier, out_q, rounds):
+    """Spawned worker: derive tier 1 of its group once (untimed), then decode it once per
+    round, every round starting on a barrier shared by all workers."""
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    sys.path.insert(0, ROOT)
+    import oracle as O
+    t1 = O.quantize_layer(K, V)
+    cfg = O.OracleConfig(n_rep=n_rep)
+    for _ in range(rounds):
+        barrier.wait(timeout=900)
+        t0 = time.time()
+        O.decode_layer(q, K, V, t1, tau, eps, cfg)
+        out_q.put((idx, t0, time.time()))
+
+
+def oracle_parallel(groups: list, tau: float, eps: float, n_rep: int, rounds: int) -> list:
+    """Decode the given (q, K, V) groups concurrently, one spawned process per group
+    (each single-threaded), `rounds` times.  Returns the makespan of every round in
+    seconds (first start to last finish)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")   # never fork a process that has touched the GPU
+    barrier = ctx.Barrier(len(groups))
+    out_q = ctx.Queue()
+    saved = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                                            "CUDA_VISIBLE_DEVICES")}
+    for v in saved:
+        os.environ[v] = "" if v == "CUDA_VISIBLE_DEVICES" else "1"
+    try:
+        procs = [ctx.Process(target=_oracle_group_worker,
+                             args=(i, q, K, V, tau, eps, n_rep, barrier, out_q, rounds), daemon=True)
+                 for i, (q, K, V) in enumerate(groups)]
+        for pr in procs:
+            pr.start()
+    finally:
+        for v, val in saved.items():
+            if val is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = val
+    spans = []
+    try:
+        for _ in range(rounds):
+            got = [out_q.get(timeout=1200) for _ in groups]
+            spans.append(max(e for _, _, e in got) - min(s for _, s, _ in got))
+    finally:
+        for pr in procs:
+            pr.join(timeout=60)
+            if pr.is_alive():
+                pr.terminate()
+    return spans
+
+
+def _split_groups(q, K, V, limit):
+    """(q, K, V) numpy slices of the first `limit` (sequence, KV head) groups."""
+    B, Hq = q.shape[0], q.shape[1]
+    Hkv = K.shape[1]
+    n_rep = Hq // Hkv
+    out = []
+    for b in range(B):
+        for g in range(Hkv):
+            if len(out) == limit:
+                return out
+            out.append((q[b:b + 1, g * n_rep:(g + 1) * n_rep].numpy().copy(),
+                        K[b:b + 1, g:g + 1].numpy().copy(), V[b:b + 1, g:g + 1].numpy().copy()))
+    return out
+
+
+def oracle_config_baselines(rounds: int = 1) -> dict:
+    """The oracle on the four workloads' shapes, on all host cores (one process per group,
+    up to the core count) and on one core (one group), in tokens/s/layer.  Each figure is
+    a bounded sample: the groups run, scaled to the layer (B sequences x Hkv groups)."""
+    import workloads as W
+    ncores = os.cpu_count() or 1
+    shapes = {
+        "c1_ctx4k": lambda: W.c1(),
+        "c2_lowrank_ctx32k_b4": lambda: W.c2(),
+        "c3_llama8b_ctx128k_32l": lambda: W.c3_layer(0, seed=WORKLOAD["seed"]),
+        "c4_planted_ctx64k_b8": lambda: W.c4()[:3],
+    }
+    res = {}
+    for name, make in shapes.items():
+        cfg = W.WORKLOADS[name]
+        q, K, V = make()
+        B, Hkv = q.shape[0], K.shape[1]
+        n_groups = B * Hkv
+        n_rep = q.shape[1] // Hkv
+        par = _split_groups(q, K, V, min(ncores, n_groups))
+        span = min(oracle_parallel(par, cfg.tau_cov, cfg.eps, n_rep, rounds))
+        one = oracle_parallel(par[:1], cfg.tau_cov, cfg.eps, n_rep, 1)[0]
+        del q, K, V
+        res[name] = {
+            "all_cores": {"value": (len(par) / n_groups) * B / span, "unit": UNIT, "cores": len(par),
+                          "sample": f"{len(par)} of {n_groups} groups concurrently, {span:.2f} s"},
+            "one_core": {"value": B / (one * n_groups), "unit": UNIT, "cores": 1,
+                         "sample": f"1 of {n_groups} groups, {one:.2f} s, scaled to the layer"},
+        }
+    res["nproc"] = ncores
+    return res
+
+
 def run_oracle_subprocess(wl: dict, groups: int = 1) -> dict:
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
@@ -148,24 +253,44 @@ def run_oracle_subprocess(wl: dict, groups: int = 1) -> dict:
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
+def _c3_groups(wl: dict, limit: int) -> list:
+    """(q, K, V) of up to `limit` (sequence, KV head) groups of the headline workload,
+    layer after layer, drawn on the CPU."""
+    import workloads as W
+    out = []
+    layer = 0
+    while len(out) < limit and layer < wl["layers"]:
+        q, K, V = W.c3_layer(layer, device="cpu", seed=wl["seed"], batch=wl["batch"], ctx=wl["ctx"],
+                             Hq=wl["q_heads"], Hkv=wl["kv_heads"])
+        out += _split_groups(q, K, V, limit - len(out))
+        layer += 1
+    return out
+
+
 def reference_arm(args, wl):
+    """The oracle, as it stands, on the host's cores: one single-threaded process per
+    (sequence, KV head) group of the headline workload, as many groups as there are
+    cores (drawn from consecutive layers), all decoding at once.  A step is one such
+    round; its time is scaled to one layer of the workload."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    times = []
-    for i in range(args.warmup + args.steps):
-        s = run_oracle_subprocess(wl, 1)
-        if i >= args.warmup:
-            times.append(s["t_layer_s"])
-    t_layer = float(np.mean(times))
+    ncores = os.cpu_count() or 1
+    n_groups = wl["batch"] * wl["kv_heads"]
+    n_rep = wl["q_heads"] // wl["kv_heads"]
+    groups = _c3_groups(wl, ncores)
+    spans = oracle_parallel(groups, wl["tau_cov"], wl["eps"], n_rep, args.warmup + args.steps)[args.warmup:]
+    t_layer = float(np.mean(spans)) * n_groups / len(groups)
     value = wl["batch"] / t_layer
-    sample = (f"oracle decode of 1 of {wl['batch'] * wl['kv_heads']} (sequence, KV head) groups "
-              f"(4 query heads) of one {wl['ctx']}-token layer per step, scaled to the layer")
+    sample = (f"oracle decode of {len(groups)} (sequence, KV head) groups of {wl['ctx']}-token layers "
+              f"({len(groups) / n_groups:g} layers) per step, one single-threaded process per group "
+              f"on {len(groups)} of {ncores} host cores, scaled to one layer")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_layer * wl["layers"] * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": _config(wl),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": len(groups), "kind": "oracle",
+                             "sample": sample, "nproc": ncores},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -423,6 +548,51 @@ def measure_residency(args, wl, frac=0.25, layers=4):
 
 
 
+def measure_configs(args, with_oracle: bool) -> dict:
+    """The other workloads' shapes (4K x 1, concentrated 32K x 4, planted-needle 64K x 8):
+    the median of 20 certified decode calls after 5 warm-up calls on the GPU, next to
+    the oracle on all host cores and on one core (bounded samples, scaled to the layer)."""
+    import torch
+    import certified_quantized_kv_gb300 as kvq
+    import workloads as W
+    res = {}
+    for name, make in (("c1_ctx4k", lambda: W.c1(device="cuda")),
+                       ("c2_lowrank_ctx32k_b4", lambda: W.c2(device="cuda")),
+                       ("c4_planted_ctx64k_b8", lambda: W.c4(device="cuda")[:3])):
+        cfg = W.WORKLOADS[name]
+        q, K, V = make()
+        B, Hq, Hkv, N = q.shape[0], q.shape[1], K.shape[1], K.shape[2]
+        cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=N)
+        cache.append(0, K.contiguous(), V.contiguous())
+        del K, V
+        q = q.contiguous()
+        out = torch.empty(B, Hq, 128, dtype=torch.float16, device="cuda")
+        cert = torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda")
+        for _ in range(5):
+            cache.decode(0, q, cfg.tau_cov, cfg.eps, out, cert)
+        times = []
+        for _ in range(20):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            cache.decode(0, q, cfg.tau_cov, cfg.eps, out, cert)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        c = kvq.certificates(cert).reshape(B, Hq)
+        res[name] = {"gpu": {"value": B / (ms / 1e3), "unit": UNIT, "us_per_call": 1e3 * ms,
+                             "ladder_histogram": [int(x) for x in np.bincount(c["level"].ravel(), minlength=5)],
+                             "promoted_bytes": int(c["promoted_bytes"][:, :: Hq // Hkv].sum())}}
+        cache.close()
+        torch.cuda.empty_cache()
+    if with_oracle:
+        orc = oracle_config_baselines()
+        for name in res:
+            res[name]["oracle"] = orc[name]
+        res["oracle_nproc"] = orc["nproc"]
+    return res
+
+
 def our_arm(args, wl):
     import torch
     import torch.distributed as dist
@@ -466,25 +636,29 @@ def our_arm(args, wl):
     st = torch.cuda.current_stream()
 
     def timed_region():
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # one event per step boundary on the launching stream: the K steps are timed as a
+        # whole, and the per-step times give the median
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
         with ClockSampler(local) as clk:
             torch.cuda.synchronize()
-            e0.record(st)
-            for _ in range(args.steps):
+            ev[0].record(st)
+            for i in range(args.steps):
                 step()
-            e1.record(st)
+                ev[i + 1].record(st)
             torch.cuda.synchronize()
-        return e0.elapsed_time(e1), clk.summary()
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+        return ev[0].elapsed_time(ev[-1]), per, clk.summary()
 
-    ms, clocks = timed_region()
+    ms, per_step, clocks = timed_region()
     if any_rank(clocks_rejected(clocks), "cuda" if world > 1 else None):
         # slowed down or clock-locked: measured once more, and the second run is reported
         if world > 1:
             dist.barrier()
-        ms, clocks = timed_region()
+        ms, per_step, clocks = timed_region()
         clocks["remeasured"] = True
     ms, units = aggregate_ranks(ms, B * L * args.steps, "cuda" if world > 1 else None)
     ms_per_step = ms / args.steps
+    ms_median = statistics.median(per_step)
     value = units / (ms / 1e3)
 
     # the uncertified INT8/INT4 baseline on the same caches: the speed ceiling of tier 1
@@ -590,9 +764,9 @@ def our_arm(args, wl):
         v["share"] = v["total_ms"] / tot_all
     units = B * Hkv * N      # token x KV-head units per layer
     traffic = _ncu_traffic()
+    t_layer_us = 1e3 * ms_per_step / L
     # HBM-bound tier-1 kernels: algorithmic bytes per launch (tier-1 bytes they must read)
     hbm_algo = {"score": SCORE_BYTES_PER_TOKEN_HEAD * units}
-    dom = max(kern.items(), key=lambda kv: kv[1]["total_ms"])[0] if kern else None
 
     def host_roofline(k):
         b = host_bytes.get(k, 0.0)
@@ -600,7 +774,9 @@ def our_arm(args, wl):
         t = traffic.get(k, {}).get("sysmem_bytes")
         return {"bound": "host_link", "kernel": k, "achieved": achieved, "peak": h2d_gbs,
                 "peak_kind": "measured in this run (pinned H2D copy, 256 MiB)", "unit": "GB/s",
-                "frac": achieved / h2d_gbs, "traffic": t, "algorithmic_bytes_per_launch": b}
+                "frac": achieved / h2d_gbs, "traffic": t, "algorithmic_bytes_per_launch": b,
+                "timing": "CUDA events around this kernel in a separate pass that brackets every kernel "
+                          "(that pass runs about 10% slower than the timed region)"}
 
     def hbm_roofline(k):
         achieved = hbm_algo[k] / (kern[k]["avg_us"] * 1e-6) / 1e9
@@ -609,11 +785,24 @@ def our_arm(args, wl):
                 "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": t,
                 "algorithmic_bytes_per_launch": hbm_algo[k]}
 
-    roofline = None
-    if dom in host_bytes and host_bytes[dom] > 0:
-        roofline = host_roofline(dom)
-    elif dom in hbm_algo:
-        roofline = hbm_roofline(dom)
+    # the decode step is bound by the FP16 blocks it pages in over the host link: the
+    # roofline is that link, from the timed region (every tier-2 read of the step: the
+    # first and second mixed passes and the dense rung, per layer call)
+    prom_layer = prom / L
+    link_traffic = [traffic.get(k, {}).get("sysmem_bytes") for k in ("mixed_round0", "mixed_round1", "dense_fallback")]
+    roofline = {"bound": "host_link",
+                "kernel": "decode call (tier-2 reads of mixed_round0, mixed_round1 and dense_fallback)",
+                "achieved": prom_layer / (t_layer_us * 1e-6) / 1e9, "peak": h2d_gbs,
+                "peak_kind": "measured in this run (pinned H2D copy, 256 MiB)", "unit": "GB/s",
+                "frac": prom_layer / (t_layer_us * 1e-6) / 1e9 / h2d_gbs,
+                "traffic": (sum(link_traffic) if all(x is not None for x in link_traffic) else None),
+                "algorithmic_bytes_per_launch": prom_layer,
+                "timing": "the timed region: ms_per_step / layers per decode call"}
+    tier1_layer = TIER1_BYTES_PER_TOKEN_HEAD * units
+    floor_us = 1e6 * (tier1_layer / (hbm_peak * 1e9) + prom_layer / (h2d_gbs * 1e9))
+    two_link = {"tier1_bytes_per_layer": tier1_layer, "promoted_bytes_per_layer": prom_layer,
+                "floor_us_per_layer": floor_us, "t_layer_us": t_layer_us, "frac": floor_us / t_layer_us,
+                "what": "(tier-1 bytes / measured HBM + promoted bytes / measured H2D) / time per layer"}
     roofline_hbm = hbm_roofline("score") if "score" in kern else None
     # the same kernels timed alone (one layer, uncertified calls back to back)
     tier1_alone = {}
@@ -627,40 +816,60 @@ def our_arm(args, wl):
                               "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
                               "frac": b / (us * 1e-6) / 1e9 / hbm_peak, "traffic": t,
                               "algorithmic_bytes_per_launch": b}
+    if "score" in tier1_alone and "int4_tail" in tier1_alone:
+        b = tier1_alone["score"]["algorithmic_bytes_per_launch"] + tier1_alone["int4_tail"]["algorithmic_bytes_per_launch"]
+        us = tier1_alone["score"]["avg_us"] + tier1_alone["int4_tail"]["avg_us"]
+        tier1_alone["pair"] = {"bound": "hbm", "kernel": "score + int4_tail", "avg_us": us,
+                               "achieved": b / (us * 1e-6) / 1e9, "peak": hbm_peak, "peak_kind": peak_kind,
+                               "unit": "GB/s", "frac": b / (us * 1e-6) / 1e9 / hbm_peak,
+                               "algorithmic_bytes_per_launch": b}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32 accumulate (int8/int4/f16 MMA operands)",
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_median": ms_median,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 accumulate (int8/int4/f16 MMA operands)",
         "data": "synthetic (seeded Gaussian caches shaped like Llama-3.1-8B attention)",
         "config": _config(wl),
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": int(sum(v["launches"] for v in kern.values())) // max(1, args.steps) * args.steps,
         "roofline": roofline,
+        "roofline_two_link": two_link,
         "roofline_hbm": roofline_hbm,
         "roofline_tier1_alone": tier1_alone,
-        "kernels": kern,
+    }
+    if args.cpu_baseline:
+        try:
+            ncores = os.cpu_count() or 1
+            n_groups = B * Hkv
+            groups = _c3_groups(wl, ncores)
+            span = min(oracle_parallel(groups, tau, eps, Hq // Hkv, 2))
+            t_all = span * n_groups / len(groups)
+            one = oracle_parallel(groups[:1], tau, eps, Hq // Hkv, 1)[0]
+            line["cpu_baseline"] = {
+                "value": B / t_all, "unit": UNIT, "cores": len(groups), "kind": "oracle", "nproc": ncores,
+                "sample": (f"oracle decode of {len(groups)} (sequence, KV head) groups of {N}-token layers at "
+                           f"once, one single-threaded process per group ({span:.2f} s), scaled to one layer"),
+                "one_core": {"value": B / (one * n_groups), "unit": UNIT, "cores": 1,
+                             "sample": f"1 of {n_groups} groups of one layer ({one:.2f} s), scaled to the layer"}}
+        except Exception as e:  # pragma: no cover
+            line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                    "sample": f"failed: {e}"[:200]}
+    line.update({
+        "roofline_kernel_mixed_round0": host_roofline("mixed_round0") if "mixed_round0" in kern else None,
         "ladder_histogram": hist,
         "promoted_bytes_per_step": prom,
         "host_link": {"h2d_gbs_measured": h2d_gbs, "bytes_per_layer": host_bytes,
                       "floor_us_per_layer": prom / L / (h2d_gbs * 1e3) if h2d_gbs else None},
+        "uncertified_baseline": uncertified,
+        "kernels": kern,
         "fill_s": t_fill,
         "append": append,
-        "uncertified_baseline": uncertified,
-    }
-    if args.cpu_baseline:
-        try:
-            s = run_oracle_subprocess(wl, 1)
-            line["cpu_baseline"] = {
-                "value": wl["batch"] / s["t_layer_s"], "unit": UNIT, "cores": 1, "kind": "oracle",
-                "sample": (f"oracle decode of 1 of {B * Hkv} (sequence, KV head) groups of one "
-                           f"{N}-token layer ({s['sample_s']:.1f} s of CPU), scaled to the layer")}
-        except Exception as e:  # pragma: no cover
-            line["cpu_baseline"] = {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                    "sample": f"failed: {e}"[:200]}
+    })
     cache.close()
     line["fp16_values"] = measure_fp16_values(args, wl)
     line["residency"] = measure_residency(args, wl)
+    line["configs"] = measure_configs(args, args.cpu_baseline)
     print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -828,8 +1037,8 @@ def sweep_vtol(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--layers", type=int, default=None, help="override the layer count (not the headline)")
     ap.add_argument("--ctx", type=int, default=None, help="override the context (not the headline)")

@@ -285,6 +285,14 @@ def dense_decode_noalloc(q, k, v, out, stream=None):
     _need(k, "k", torch.float16, (B, Hkv, N, HEAD_DIM))
     _need(v, "v", torch.float16, (B, Hkv, N, HEAD_DIM))
     _need(out, "out", torch.float16, (B, Hq, HEAD_DIM))
+    dev = q.device
+    if any(t.device != dev for t in (k, v, out)):
+        raise ValueError("q, k, v and out must be on one CUDA device")
+    if dev.type == "cuda":
+        with torch.cuda.device(dev):   # the call runs on the tensors' device and its stream
+            _check(load_library().kvq_dense_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N,
+                                                           _ptr(out), _stream(stream)))
+        return
     _check(load_library().kvq_dense_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N,
                                                    _ptr(out), _stream(stream)))
 

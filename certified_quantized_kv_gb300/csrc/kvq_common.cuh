@@ -42,7 +42,10 @@ constexpr float INV_SQRT_D = 0.088388347648318440550f;  // 1/sqrt(128), rounded 
 
 // Per (sequence, query head) state of one decode call.
 struct HeadState {
-  float M;          // reference >= every score of the head (exp(s - M) <= 1)
+  float M;          // softmax reference of the head: after the selection the largest INT8
+                    // block log-mass or partial-block score (>= every INT8 score); after a
+                    // combine the largest reference of that pass's work items (>= every
+                    // score the pass used)
   float lse_int8;   // log-sum-exp over all tokens with INT8 scores for full blocks
   float tail_lse;   // log-sum-exp of the partial block's exact scores (-inf if none)
   int k_star;       // |S_h|
@@ -110,7 +113,9 @@ struct LayerView {
   uint8_t* vprom1;
   HeadState* hst;        // [B*Hq]
   GroupState* gst;       // [BG]
-  float* part;           // [BG][nslot][MAXREP][D+4] partials of the mixed pass
+  float* part;           // [BG][nslot][MAXREP][D+4] partials of the mixed pass: D
+                         // channel sums, then the weight sum l and the item's reference M
+                         // (weights are exp(s - M))
   float* part1;          // same shape: deltas of the second mixed pass
   float* red0;           // [B*Hq][D+4] the first pass's partials summed (channels, then l)
   float* dpart;          // [BG][nslot][MAXREP][D+4] partials of the dense pass
@@ -206,18 +211,40 @@ __device__ __forceinline__ void i8x4_to_f16(uint32_t w, uint32_t& lo, uint32_t& 
 }
 
 // The four nibble pairs of a V-code word (pair i: bits 4i..4i+3 and 16+4i..16+4i+3) ->
-// f16x2 registers a0..a3, exactly, in nine instructions.  Pairs 0 and 2 sit at bits 0-3 and
-// 16-19 (of w, and of w with bytes 1 and 3 moved down by a byte permute): 0x6400 | n reads
-// 1024 + n.  Pairs 1 and 3 sit at bits 4-7 and 20-23: 0x6400 | 16 n reads 1024 + 16 n, and
-// (1024 + 16 n) / 16 - 64 = n; every step is exact in binary16.
-__device__ __forceinline__ void nib8_to_f16x4(uint32_t w, uint32_t& a0, uint32_t& a1, uint32_t& a2,
-                                              uint32_t& a3) {
+// f16x2 MMA operands a0..a3 in five instructions, read as binary16 subnormals: with a zero
+// exponent field the bits m of a half encode m * 2^-24 exactly.  Pairs 0 and 2 (of w, and
+// of w with bytes 1 and 3 moved down by a byte permute) sit at bits 0-3 and 16-19 and read
+// n * 2^-24; pairs 1 and 3 sit at bits 4-7 and 20-23 and read 16 n * 2^-24 = n * 2^-20.
+// The tensor cores take subnormal f16 operands as they are (checked on GB300 against an
+// fp64 sum: the accumulated error stays within 2.7e-6 of the sum of |products|, against
+// 7.6e-7 for the same products with normal operands), so an MMA over these operands
+// gives the code-weighted sum times 2^-24 in the rows of pairs 0/2 (A-fragment rows gid)
+// and times 2^-20 in the rows of pairs 1/3 (rows gid + 8); NIB_ROW_SCALE_* undo that.
+constexpr float NIB_ROW_SCALE_LO = 16777216.f;   // 2^24: accumulator rows gid
+constexpr float NIB_ROW_SCALE_HI = 1048576.f;    // 2^20: accumulator rows gid + 8
+__device__ __forceinline__ void nib8_to_sub_f16x4(uint32_t w, uint32_t& a0, uint32_t& a1, uint32_t& a2,
+                                                  uint32_t& a3) {
   const uint32_t x = __byte_perm(w, 0u, 0x4341);   // bytes 1 and 3 of w into bytes 0 and 2
-  const __half2 k1024 = u32_as_h2(0x64006400u), k16th = u32_as_h2(0x2C002C00u), km64 = u32_as_h2(0xD400D400u);
-  a0 = h2_as_u32(__hsub2(u32_as_h2((w & 0x000F000Fu) | 0x64006400u), k1024));
-  a1 = h2_as_u32(__hfma2(u32_as_h2((w & 0x00F000F0u) | 0x64006400u), k16th, km64));
-  a2 = h2_as_u32(__hsub2(u32_as_h2((x & 0x000F000Fu) | 0x64006400u), k1024));
-  a3 = h2_as_u32(__hfma2(u32_as_h2((x & 0x00F000F0u) | 0x64006400u), k16th, km64));
+  a0 = w & 0x000F000Fu;
+  a1 = w & 0x00F000F0u;
+  a2 = x & 0x000F000Fu;
+  a3 = x & 0x00F000F0u;
+}
+
+// 2^x by the hardware's base-2 exponential (ex2.approx: relative error about 2^-22;
+// results below 2^-126 flush to zero).  e^x is 2^(x log2 e).
+constexpr float LOG2E_F = 1.4426950408889634f;
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// Base-2 exponent e of the prescale 2^e chosen by prescale_for (0 when xmax <= 0).
+__device__ __forceinline__ int prescale_exp(float xmax) {
+  if (!(xmax > 0.f)) return 0;
+  int e;
+  frexpf(xmax, &e);
+  return max(-100, min(100, 14 - e));
 }
 
 // Packed fp32 pairs (two lanes of one 64-bit register pair per instruction).
@@ -284,12 +311,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Power-of-two prescale so that |x| * 2^e <= 2^14 for |x| <= xmax (keeps split halves
 // normal and far from overflow).  Returns 2^e as a float.
 __device__ __forceinline__ float prescale_for(float xmax) {
-  if (!(xmax > 0.f)) return 1.f;
-  int e;
-  frexpf(xmax, &e);             // xmax = m * 2^e, m in [0.5, 1)
-  int s = 14 - e;
-  s = max(-100, min(100, s));
-  return ldexpf(1.f, s);
+  return ldexpf(1.f, prescale_exp(xmax));   // xmax = m 2^e, m in [0.5, 1): 2^(14 - e)
 }
 
 // ---------------------------------------------------------------------------------

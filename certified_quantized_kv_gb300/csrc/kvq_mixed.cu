@@ -50,7 +50,7 @@ struct __align__(16) MixSmem {
   float p[2][MAXREP][BLK];    // INT4-path weights
   float pn[2][MAXREP][BLK];   // FP16-value weights / FP16 scores
   float qf[MAXREP][D];
-  float M[MAXREP];
+  float fac[MAXREP];          // per head: factor that moved the item's sums to a raised reference
   uint32_t bw[4][MW_WORDS];   // per warp: the INT4-path B words of its value group
   struct {
     __half kbuf[BLK][KROW];
@@ -155,10 +155,13 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
         const int r = i / D, c = i % D;
         sm.qf[r][c] = (r < V.n_rep) ? __half2float(V.q[head_row(V, b, g, r) * D + c]) : 0.f;
       }
-      if (tid < MAXREP) sm.M[tid] = (tid < V.n_rep) ? V.hst[head_row(V, b, g, tid)].M : 0.f;
       pre_v = prescale_for(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
       __syncthreads();
     }
+    // the item's softmax reference for head `warp`: the head's reference after the
+    // selection (round 0) or the first combine (round 1), raised only where an FP16-key
+    // block of this item scores above it (its sums so far are then rescaled)
+    float Mr = (warp < V.n_rep) ? V.hst[head_row(V, b, g, warp)].M : 0.f;
 
     float acc[2][4];
 #pragma unroll
@@ -208,17 +211,24 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
         __syncthreads();
         sn0 = sm.pn[par][r][lane];
         sn1 = sm.pn[par][r][lane + 32];
+        float fac = 1.f;
         if (act) {
           const float m = warp_max(fmaxf(sn0, sn1));
           const float l = warp_sum(expf(sn0 - m) + expf(sn1 - m));
           if (lane == 0) V.lse16[head_row(V, b, g, r) * V.nbmax + blk] = m + logf(l);
           shat_r[lane] = sn0;
           shat_r[lane + 32] = sn1;
+          if (m > Mr) {
+            fac = expf(Mr - m);
+            Mr = m;
+            lsum *= fac;   // head `warp`'s weight sum, before this block's weights join it
+          }
         }
+        if (lane == 0) sm.fac[r] = fac;
       }
       float pn0 = 0.f, pn1 = 0.f, pi0 = 0.f, pi1 = 0.f;
       if (act) {
-        const float M = sm.M[r];
+        const float M = Mr;
         if (round == 0) {
           pn0 = kp0 ? expf(sn0 - M) : __expf(sn0 - M);
           pn1 = kp0 ? expf(sn1 - M) : __expf(sn1 - M);
@@ -244,6 +254,16 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
       sm.pn[par][r][lane] = pn0;
       sm.pn[par][r][lane + 32] = pn1;
       __syncthreads();
+      if (need_k16) {   // sums so far to the raised references (factor 1 where unchanged)
+        const float ft = sm.fac[tig], fh = sm.fac[lane >> 3];
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] *= ft;   // accumulator columns: head tig
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc16[j] *= ft;     // FP16 values: head tig
+        off *= fh;                                       // offsets: head lane / 8
+      }
       // ---- stage 2: weights x V for the warp's value group ----
       if (!v16) {
         const uint4* vcp = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES) + (warp * 2) * 32 + lane;
@@ -292,7 +312,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t w = (kk == 0) ? C.x : (kk == 1) ? C.y : (kk == 2) ? C.z : C.w;
             uint32_t a0, a1, a2, a3;
-            nib8_to_f16x4(w, a0, a1, a2, a3);
+            nib8_to_sub_f16x4(w, a0, a1, a2, a3);
             mma16816(acc[mt], a0, a1, a2, a3, bb0[kk], bb1[kk]);
           }
         }
@@ -322,18 +342,23 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
     off += __shfl_xor_sync(0xffffffffu, off, 2);
     off += __shfl_xor_sync(0xffffffffu, off, 4);
     const float offh = __shfl_sync(0xffffffffu, off, 8 * tig);  // head tig
+    // undo 2^e (the products) and 2^-24 / 2^-20 (subnormal code rows); powers of two
     const float inv = 1.f / pre_v;
+    const float inv_lo = inv * NIB_ROW_SCALE_LO, inv_hi = inv * NIB_ROW_SCALE_HI;
     float* pp = (round == 0 ? V.part : V.part1) + (((size_t)hs * NCH + ch) * MAXREP) * (D + 4);
     if (tig < V.n_rep) {
       float* pr = pp + tig * (D + 4);
       const int c0 = 32 * warp + gid;
-      pr[c0] = (acc[0][0] + acc[0][1]) * inv + acc16[0] + offh;
-      pr[c0 + 8] = (acc[0][2] + acc[0][3]) * inv + acc16[1] + offh;
-      pr[c0 + 16] = (acc[1][0] + acc[1][1]) * inv + acc16[2] + offh;
-      pr[c0 + 24] = (acc[1][2] + acc[1][3]) * inv + acc16[3] + offh;
+      pr[c0] = (acc[0][0] + acc[0][1]) * inv_lo + acc16[0] + offh;
+      pr[c0 + 8] = (acc[0][2] + acc[0][3]) * inv_hi + acc16[1] + offh;
+      pr[c0 + 16] = (acc[1][0] + acc[1][1]) * inv_lo + acc16[2] + offh;
+      pr[c0 + 24] = (acc[1][2] + acc[1][3]) * inv_hi + acc16[3] + offh;
     }
     lsum = warp_sum(lsum);
-    if (lane == 0 && warp < V.n_rep) pp[warp * (D + 4) + D] = lsum;
+    if (lane == 0 && warp < V.n_rep) {
+      pp[warp * (D + 4) + D] = lsum;
+      pp[warp * (D + 4) + D + 1] = Mr;
+    }
 
     __syncthreads();
   }
@@ -395,7 +420,19 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   }
   // (1) work-item partials of this pass in a fixed order: warp w sums items w, w + 8, ...
   //     (lane = four channels), then the eight warp sums are added in warp order; the
-  //     second pass adds its deltas to the first pass's sums
+  //     second pass adds its deltas to the first pass's sums.  Each item's weights are
+  //     exp(s - M_item); the sums are taken to the largest reference Mc of the pass (and
+  //     of the first pass's sums in round 1), a factor of exactly 1 for every item that
+  //     kept the head's reference.
+  const float M_prev = hsd.M;   // reference of the first pass's sums (round 1)
+  float Mc;
+  {
+    const float* P = (round == 0) ? V.part : V.part1;
+    float mloc = (round == 1) ? M_prev : -INFINITY;
+    for (int ch = tid; ch < nch; ch += BS_THREADS)
+      mloc = fmaxf(mloc, P[(((size_t)hs * NCH + ch) * MAXREP + r) * (D + 4) + D + 1]);
+    Mc = block_max(mloc, ws.red);
+  }
   {
     const int warp = tid >> 5, lane = tid & 31;
     const float* P = (round == 0) ? V.part : V.part1;
@@ -404,13 +441,17 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
 #pragma unroll 8
     for (int ch = warp; ch < nch; ch += BS_WARPS) {
       const size_t o = (((size_t)hs * NCH + ch) * MAXREP + r) * (D + 4);
+      const float Mi = P[o + D + 1];
+      const float w = (Mi == Mc) ? 1.f : expf(Mi - Mc);
       const float4 x = *reinterpret_cast<const float4*>(P + o + 4 * lane);
-      a.x += x.x; a.y += x.y; a.z += x.z; a.w += x.w;
-      if (lane == 0) l += P[o + D];
+      a.x = fmaf(x.x, w, a.x); a.y = fmaf(x.y, w, a.y); a.z = fmaf(x.z, w, a.z); a.w = fmaf(x.w, w, a.w);
+      if (lane == 0) l = fmaf(P[o + D], w, l);
     }
     *reinterpret_cast<float4*>(&acc_s[warp][4 * lane]) = a;
     if (lane == 0) l_s[warp] = l;
   }
+  hsd.M = Mc;
+  const float w_prev = (round == 0 || M_prev == Mc) ? 1.f : expf(M_prev - Mc);
   // (2) the partial FP16 block with exact scores
   float lt = 0.f;
   if (tid < V.n_tail) {
@@ -420,13 +461,13 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   }
   lt = block_sum(lt, ws.red);   // synchronises acc_s, l_s and tail_p too
   float* red = V.red0 + hb * (D + 4);
-  float L0 = (round == 1) ? red[D] : 0.f;
+  float L0 = (round == 1) ? red[D] * w_prev : 0.f;
 #pragma unroll
   for (int w = 0; w < BS_WARPS; ++w) L0 += l_s[w];
   const float L = L0 + lt;
   if (round == 0 && tid == 0) red[D] = L0;
   if (tid < D) {
-    float a = (round == 1) ? red[tid] : 0.f;
+    float a = (round == 1) ? red[tid] * w_prev : 0.f;
 #pragma unroll
     for (int w = 0; w < BS_WARPS; ++w) a += acc_s[w][tid];
     if (round == 0) red[tid] = a;
@@ -641,7 +682,8 @@ struct __align__(16) R0Smem {
   float p[MAXREP][BLK];          // weights of an FP16-key block
   float s16[MAXREP][BLK];        // its FP16 scores
   float qf[MAXREP][D];
-  float M[MAXREP];
+  float M[MAXREP];               // the item's reference per head after an FP16-key block
+  float fac[MAXREP];             // factor that moved the item's sums to that reference
   uint32_t bw[4][MW_WORDS];      // per warp: the B words of its value group
   __half kbuf[BLK][KROW];
   R0Stage ring[4][R0_STAGES];
@@ -666,7 +708,8 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
   const unsigned long long pol = evict_first_policy();
   R0Stage* ring = sm.ring[warp];
   int cur_hs = -1;
-  float pre_v = 1.f, Mh = 0.f;
+  int pre_e = 0;
+  float pre_v = 1.f, pre_ef = 0.f;
 
   for (;;) {
     if (tid == 0) sm.item = (int)atomicAdd(&V.counters[CNT_MIX_Q], 1u);
@@ -682,11 +725,16 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
         const int r = i / D, c = i % D;
         sm.qf[r][c] = (r < V.n_rep) ? __half2float(V.q[(hrow + r) * D + c]) : 0.f;
       }
-      if (tid < MAXREP) sm.M[tid] = (tid < V.n_rep) ? V.hst[hrow + tid].M : 0.f;
-      pre_v = prescale_for(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
+      pre_e = prescale_exp(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
+      pre_v = ldexpf(1.f, pre_e);
+      pre_ef = (float)pre_e;
       __syncthreads();
-      Mh = sm.M[hp];
     }
+    // the item's softmax reference per head starts at the selection's (>= every INT8
+    // score) and rises only where an FP16-key block of the item scores above it, so it
+    // depends on the item's own blocks alone
+    float Mh = act ? V.hst[hrow + hp].M : 0.f;      // head hp: INT8 weights, offsets, sums
+    float Mw = wact ? V.hst[hrow + warp].M : 0.f;   // head `warp`: FP16 scoring role
 
     const int blk0 = ch * V.chunk, blk_end = min(V.nb, blk0 + V.chunk);
     const size_t bi0 = (size_t)hs * V.nbmax + blk0;
@@ -761,7 +809,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
         __syncthreads();
         score_f16_block(sm.kbuf, sm.qf, sm.s16);
         __syncthreads();
-        float p0 = 0.f, p1 = 0.f;
+        float p0 = 0.f, p1 = 0.f, fac = 1.f;
         if (wact) {
           const float sn0 = sm.s16[warp][lane], sn1 = sm.s16[warp][lane + 32];
           const float m = warp_max(fmaxf(sn0, sn1));
@@ -770,12 +818,30 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
           float* shat_r = V.shat + (hrow + warp) * ((size_t)V.nbmax * BLK) + (size_t)blk * BLK;
           shat_r[lane] = sn0;
           shat_r[lane + 32] = sn1;
-          p0 = expf(sn0 - sm.M[warp]);
-          p1 = expf(sn1 - sm.M[warp]);
+          if (m > Mw) {   // an FP16 score above the reference: raise it, rescale the sums
+            fac = expf(Mw - m);
+            Mw = m;
+          }
+          p0 = expf(sn0 - Mw) * pre_v;
+          p1 = expf(sn1 - Mw) * pre_v;
+        }
+        if (lane == 0) {
+          sm.fac[warp] = fac;
+          sm.M[warp] = Mw;
         }
         sm.p[warp][lane] = p0;
         sm.p[warp][lane + 32] = p1;
         __syncthreads();
+        {
+          const float ft = sm.fac[tig], fh = sm.fac[hp];   // accumulator columns: head tig
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[mt][j] *= ft;
+          off *= fh;
+          lsum *= fh;
+          if (act) Mh = sm.M[hp];
+        }
         const float4 pa = *reinterpret_cast<const float4*>(&sm.p[hp][8 * sub]);
         const float4 pc = *reinterpret_cast<const float4*>(&sm.p[hp][8 * sub + 4]);
         pv[0] = pa.x; pv[1] = pa.y; pv[2] = pa.z; pv[3] = pa.w;
@@ -784,12 +850,12 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
         const float4 sa = T.s[hp * (BLK / 4) + 2 * sub], sb = T.s[hp * (BLK / 4) + 2 * sub + 1];
         const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) pv[i] = act ? __expf(sv[i] - Mh) : 0.f;
+        for (int i = 0; i < 8; ++i) pv[i] = act ? exp2_approx(fmaf(sv[i] - Mh, LOG2E_F, pre_ef)) : 0.f;
       }
 #pragma unroll
       for (int i = 0; i < 8; ++i) lsum += pv[i];
-      // products p_t s_{t,g} 2^e of head hp at tokens 8 sub + [0, 8) as hi + lo halves,
-      // exchanged through shared memory as B fragments
+      // products p_t s_{t,g} 2^e of head hp at tokens 8 sub + [0, 8) as hi + lo halves
+      // (the weights carry 2^e), exchanged through shared memory as B fragments
       {
         const uint4 S0 = T.so[2 * sub], S1 = T.so[2 * sub + 1];   // (scale, offset), 8 tokens
         const uint32_t sw[8] = {S0.x, S0.y, S0.z, S0.w, S1.x, S1.y, S1.z, S1.w};
@@ -800,7 +866,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
           const float2 p2 = make_float2(pv[2 * i], pv[2 * i + 1]);
           off = fmaf(p2.x, a.y, off);
           off = fmaf(p2.y, c.y, off);
-          const float2 w = mul2(mul2(p2, make_float2(a.x, c.x)), make_float2(pre_v, pre_v));
+          const float2 w = mul2(p2, make_float2(a.x, c.x));
           const __half2 hi = __floats2half2_rn(w.x, w.y);
           const float2 rem = sub2(w, __half22float2(hi));   // exact remainders
           hw[i] = h2_as_u32(hi);
@@ -826,7 +892,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           uint32_t a0, a1, a2, a3;
-          nib8_to_f16x4(word_of(C, kk), a0, a1, a2, a3);
+          nib8_to_sub_f16x4(word_of(C, kk), a0, a1, a2, a3);
           mma16816(acc[mt], a0, a1, a2, a3, bb0[kk], bb1[kk]);
         }
       }
@@ -843,17 +909,22 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
     const float offh = __shfl_sync(0xffffffffu, off, 8 * tig);   // head tig
-    const float inv = 1.f / pre_v;
+    // undo 2^e (weights) and 2^-24 / 2^-20 (subnormal code rows); powers of two, exact
+    const float inv = ldexpf(1.f, -pre_e);
+    const float inv_lo = inv * NIB_ROW_SCALE_LO, inv_hi = inv * NIB_ROW_SCALE_HI;
     float* pp = V.part + (((size_t)hs * NCH + ch) * MAXREP) * (D + 4);
     if (tig < V.n_rep) {
       float* pr = pp + tig * (D + 4);
       const int c0 = 32 * warp + gid;
-      pr[c0] = (acc[0][0] + acc[0][1]) * inv + offh;
-      pr[c0 + 8] = (acc[0][2] + acc[0][3]) * inv + offh;
-      pr[c0 + 16] = (acc[1][0] + acc[1][1]) * inv + offh;
-      pr[c0 + 24] = (acc[1][2] + acc[1][3]) * inv + offh;
+      pr[c0] = (acc[0][0] + acc[0][1]) * inv_lo + offh * inv;
+      pr[c0 + 8] = (acc[0][2] + acc[0][3]) * inv_hi + offh * inv;
+      pr[c0 + 16] = (acc[1][0] + acc[1][1]) * inv_lo + offh * inv;
+      pr[c0 + 24] = (acc[1][2] + acc[1][3]) * inv_hi + offh * inv;
     }
-    if (warp == 0 && sub == 0 && act) pp[hp * (D + 4) + D] = lsum;   // every warp has the sums
+    if (warp == 0 && sub == 0 && act) {   // every warp has the sums
+      pp[hp * (D + 4) + D] = lsum * inv;
+      pp[hp * (D + 4) + D + 1] = Mh;
+    }
     __syncthreads();
   }
   if (tid == 0) {

@@ -176,7 +176,10 @@ __global__ void __launch_bounds__(128) noalloc_dense_kernel(NaArgs a) {
   }
 }
 
-// Device address of this device's scratch array, looked up once per device.
+// Device address of this device's scratch array, looked up once per device (the first
+// call on a device; the lookup also makes the driver load this library's device code on
+// that device, which is when the array's memory is reserved).  A cudaDeviceReset unloads
+// the code and frees the array; this entry point is not for use after one.
 cudaError_t scratch_for_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -193,13 +196,16 @@ cudaError_t scratch_for_current_device(void** out) {
   return cudaSuccess;
 }
 
-bool is_device(const void* p) {
+// Device (or managed) memory of device `dev`: the kernel runs on the current device, so a
+// buffer of another device would be read through a foreign address.
+bool on_device(const void* p, int dev) {
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
-  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+  if (at.type == cudaMemoryTypeDevice) return at.device == dev;
+  return at.type == cudaMemoryTypeManaged;
 }
 
 }  // namespace
@@ -217,8 +223,15 @@ extern "C" kvq_status kvq_dense_decode_noalloc(const void* q, const void* k, con
                         "n_q_heads / n_kv_heads an integer in 1..4");
     return KVQ_ERR_INVALID;
   }
-  if (!is_device(q) || !is_device(k) || !is_device(v) || !is_device(out)) {
-    kvq::set_last_error("kvq_dense_decode_noalloc: q, k, v and out must be device memory");
+  int cur = 0;
+  if (cudaGetDevice(&cur) != cudaSuccess) {
+    cudaGetLastError();
+    kvq::set_last_error("kvq_dense_decode_noalloc: no current CUDA device");
+    return KVQ_ERR_CUDA;
+  }
+  if (!on_device(q, cur) || !on_device(k, cur) || !on_device(v, cur) || !on_device(out, cur)) {
+    kvq::set_last_error("kvq_dense_decode_noalloc: q, k, v and out must be device memory of the "
+                        "current device");
     return KVQ_ERR_INVALID;
   }
   for (const void* p : {q, k, v, static_cast<const void*>(out)}) {
@@ -257,9 +270,8 @@ extern "C" kvq_status kvq_dense_decode_noalloc(const void* q, const void* k, con
   a.BG = BG; a.N = n_tokens; a.nch = nch;
   a.cnt = static_cast<unsigned int*>(base);
   a.part = reinterpret_cast<float*>(static_cast<char*>(base) + cnt_bytes);
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, cur);
   const int grid = std::min(BG * nch, std::max(1, sms) * 3);
   noalloc_dense_kernel<<<grid, 128, 0, st>>>(a);
   e = cudaGetLastError();

@@ -272,23 +272,21 @@ __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
   const float tail_lse = V.n_tail > 0 ? tmax + logf(tl) : -INFINITY;
   // block log-masses: staged in shared memory (16-byte loads; rows padded to 16 blocks)
   const float* lse8 = V.lse8 + hb * V.nbmax;
-  const float* dl = V.delta + hb * V.nbmax;
-  float m = -INFINITY, mref = -INFINITY;
+  float m = -INFINITY;
   for (int i4 = tid; i4 < nbp / 4; i4 += BS_THREADS) {
     const float4 x = reinterpret_cast<const float4*>(lse8)[i4];
-    const float4 d = reinterpret_cast<const float4*>(dl)[i4];
-    const float xv[4] = {x.x, x.y, x.z, x.w}, dv[4] = {d.x, d.y, d.z, d.w};
+    const float xv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (4 * i4 + j < nb) {
-        m = fmaxf(m, xv[j]);
-        mref = fmaxf(mref, xv[j] + dv[j]);
-      }
-    }
+    for (int j = 0; j < 4; ++j)
+      if (4 * i4 + j < nb) m = fmaxf(m, xv[j]);
     reinterpret_cast<float4*>(xs)[i4] = x;
   }
-  m = block_max(fmaxf(m, tail_lse), ws.red);
-  mref = block_max(fmaxf(mref, tmax), ws.red);
+  m = block_max(m, ws.red);
+  // softmax reference of the passes that follow: >= every INT8 score (a block's log-mass
+  // bounds its scores) and every partial-block score; a pass that meets a larger FP16
+  // score raises its own reference
+  const float mref = fmaxf(m, tmax);
+  m = fmaxf(m, tail_lse);
   float sp = 0.f;
   for (int i = tid; i < nb; i += BS_THREADS) sp += expf(xs[i] - m);
   float s = block_sum(sp, ws.red);

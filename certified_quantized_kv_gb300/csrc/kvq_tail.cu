@@ -12,8 +12,11 @@
 // Work split: one warp per run of consecutive blocks of one KV group (runs per group =
 // warps / groups), no CTA barrier; each block's codes, scales/offsets and scores reach
 // shared memory by cp.async through a two-stage ring per warp, so the next block is in
-// flight while the current one is multiplied.  Each run writes one partial (sum p v_hat
-// and sum p per head) into its own slot, which the combine kernel adds in a fixed order.
+// flight while the current one is multiplied.  Each run writes one partial (sum p v_hat,
+// sum p and the reference M per head) into its own slot, which the combine kernel adds
+// in a fixed order.  The weights carry the value prescale 2^e from the start
+// (p 2^e = 2^((s - M) log2 e + e)), and the INT4 codes enter the MMA as binary16
+// subnormals (see nib8_to_sub_f16x4); both scalings are undone once per run.
 #include "kvq_common.cuh"
 #include "kvq_launch.h"
 
@@ -60,7 +63,8 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
     const int hrow = hs * V.n_rep;
     const bool act = hp < V.n_rep;
     const float M = act ? V.hst[hrow + hp].M : 0.f;
-    const float pre_v = prescale_for(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
+    const int pre_e = prescale_exp(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
+    const float pre_ef = (float)pre_e;
     const uint8_t* kp0 = V.kprom0 + (size_t)hs * V.nbmax;
     // the run's blocks that keep INT8 scores (FP16-key blocks are the mixed pass's)
     auto next_block = [&](int b) {
@@ -106,14 +110,14 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
       cp_async_wait<1>();
       __syncwarp();
       const TailStage& T = ring[it % TAIL_STAGES];
-      // weights of head hp at tokens 8 sub + [0, 8), prescaled by 2^e (exact)
+      // weights of head hp at tokens 8 sub + [0, 8), times the prescale 2^e
       float pp[8];
       {
         const float4 sa = T.s[hp * (BLK / 4) + 2 * sub], sb = T.s[hp * (BLK / 4) + 2 * sub + 1];
         const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float p = act ? __expf(sv[i] - M) : 0.f;
+          const float p = act ? exp2_approx(fmaf(sv[i] - M, LOG2E_F, pre_ef)) : 0.f;
           lsum += p;
           pp[i] = p;
         }
@@ -128,10 +132,9 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
           const uint4& S = (i < 2) ? S0 : S1;
           const float2 a = __half22float2(u32_as_h2(word_of(S, 2 * (i & 1))));       // (scale, offset)
           const float2 c = __half22float2(u32_as_h2(word_of(S, 2 * (i & 1) + 1)));
-          const float2 pv = make_float2(pp[2 * i], pp[2 * i + 1]);
-          const float2 o2 = mul2(pv, make_float2(a.y, c.y));
-          off[g] += o2.x + o2.y;
-          const float2 w = mul2(mul2(pv, make_float2(pre_v, pre_v)), make_float2(a.x, c.x));
+          off[g] = fmaf(pp[2 * i], a.y, off[g]);
+          off[g] = fmaf(pp[2 * i + 1], c.y, off[g]);
+          const float2 w = mul2(make_float2(pp[2 * i], pp[2 * i + 1]), make_float2(a.x, c.x));
           const __half2 hi = __floats2half2_rn(w.x, w.y);
           const float2 rem = sub2(w, __half22float2(hi));   // exact remainders
           hw[i] = h2_as_u32(hi);
@@ -152,7 +155,7 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             uint32_t a0, a1, a2, a3;
-            nib8_to_f16x4(word_of(Cw, kk), a0, a1, a2, a3);
+            nib8_to_sub_f16x4(word_of(Cw, kk), a0, a1, a2, a3);
             mma16816(acc[g][mt], a0, a1, a2, a3, bb[2 * kk], bb[2 * kk + 1]);
           }
         }
@@ -176,7 +179,9 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
     float offh[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) offh[g] = __shfl_sync(0xffffffffu, off[g], 8 * tig);
-    const float inv = 1.f / pre_v;
+    // undo 2^e (weights) and 2^-24 / 2^-20 (subnormal code rows); powers of two, exact
+    const float inv = ldexpf(1.f, -pre_e);
+    const float inv_lo = inv * NIB_ROW_SCALE_LO, inv_hi = inv * NIB_ROW_SCALE_HI;
     float* pp = V.part + (((size_t)hs * NCH + run) * MAXREP) * (D + 4);
     if (tig < V.n_rep) {
       float* pr = pp + tig * (D + 4);
@@ -185,11 +190,14 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
           const int c0 = 32 * g + 16 * mt + gid;
-          pr[c0] = (acc[g][mt][0] + acc[g][mt][1]) * inv + offh[g];
-          pr[c0 + 8] = (acc[g][mt][2] + acc[g][mt][3]) * inv + offh[g];
+          pr[c0] = (acc[g][mt][0] + acc[g][mt][1]) * inv_lo + offh[g] * inv;
+          pr[c0 + 8] = (acc[g][mt][2] + acc[g][mt][3]) * inv_hi + offh[g] * inv;
         }
     }
-    if (sub == 0 && act) pp[hp * (D + 4) + D] = lsum;
+    if (sub == 0 && act) {
+      pp[hp * (D + 4) + D] = lsum * inv;
+      pp[hp * (D + 4) + D + 1] = M;
+    }
   }
 }
 

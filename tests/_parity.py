@@ -7,8 +7,13 @@ Tolerances (stated once, used everywhere):
     covered mass lies within SEL_BAND of tau_cov (and blocks whose mass is within
     SEL_BAND of the boundary block's), and heads whose deciding quantity is within
     relative DECIDE_REL of its threshold;
-  * outputs: |gpu - oracle| <= OUT_ATOL + OUT_RTOL |oracle|;
-  * bounds: |gpu - oracle| <= BOUND_RTOL |oracle| + BOUND_ATOL.
+  * outputs: max-abs |gpu - oracle| <= OUT_ATOL (2e-3) for every head whose oracle
+    outputs lie within +-OUT_STRICT_RANGE, and |gpu - oracle| <= OUT_ATOL + OUT_RTOL |oracle|
+    beyond (the returned output is binary16, whose rounding alone is 2^-11 relative and
+    exceeds 2e-3 above |x| = 4);
+  * bounds: |gpu - oracle| <= BOUND_RTOL |oracle| + BOUND_ATOL;
+  * coverage: at least MIN_STRICT_FRAC of the heads of every call are compared strictly
+    (level, ranking verdict and bounds), unless a test states a lower share and why.
 """
 
 from __future__ import annotations
@@ -25,6 +30,8 @@ SEL_BAND = 1e-6
 DECIDE_REL = 1e-4
 OUT_ATOL = 2e-3
 OUT_RTOL = 1e-2
+OUT_STRICT_RANGE = 2.0
+MIN_STRICT_FRAC = 0.5
 BOUND_RTOL = 1e-4
 BOUND_ATOL = 1e-6
 
@@ -123,7 +130,11 @@ def ambiguous_blocks(r: O.DecodeResult, b: int, h: int, tau: float, band: float 
 def marginal_head(r: O.DecodeResult, b: int, h: int, eps: float) -> bool:
     """Head whose rung is decided within DECIDE_REL of a threshold."""
     def near(x, t):
-        return math.isfinite(t) and abs(x - t) <= DECIDE_REL * max(abs(t), 1e-30)
+        if not math.isfinite(t):
+            return False
+        if t == 0:   # an exact zero bound (nothing left in INT8) is exact on both sides
+            return 0 < abs(x) <= 1e-30
+        return abs(x - t) <= DECIDE_REL * abs(t)
     e0 = r.e_key0[b, h] + r.e_val0[b, h]
     if near(e0, eps) or near(r.e_key0[b, h], eps / 2):
         return True
@@ -138,15 +149,17 @@ def marginal_head(r: O.DecodeResult, b: int, h: int, eps: float) -> bool:
     return False
 
 
-def compare_decode(g, t1, r: O.DecodeResult, tau, eps, n_rep, check_sets=True):
+def compare_decode(g, t1, r: O.DecodeResult, tau, eps, n_rep, check_sets=True,
+                   min_strict=MIN_STRICT_FRAC):
     """Compare one decode call; returns a dict of counters for reporting."""
     out_g = g["out"].float().numpy()
     cert = g["cert"]
     B, Hq, _ = out_g.shape
     Hkv = Hq // n_rep
     nb = g["nb"]
-    stats = dict(heads=0, strict=0, excluded=0, set_mismatch_groups=0, max_out_err=0.0,
-                 max_bound_rel=0.0)
+    stats = dict(heads=0, strict=0, excluded=0, out_compared=0, set_mismatch_groups=0,
+                 max_out_err=0.0, max_out_err_unit_range=0.0, max_bound_rel=0.0)
+    assert np.all(np.isfinite(out_g)), "non-finite output"
     group_exact = np.ones((B, Hkv), bool)
     if check_sets and g["state"] is not None and nb > 0:
         sel_g = g["state"]["sel"].numpy().astype(bool)
@@ -182,7 +195,12 @@ def compare_decode(g, t1, r: O.DecodeResult, tau, eps, n_rep, check_sets=True):
                 continue
             ref = r.out64[b, h]
             err = np.abs(out_g[b, h] - ref)
+            stats["out_compared"] += 1
             stats["max_out_err"] = max(stats["max_out_err"], float(err.max()))
+            if np.max(np.abs(ref)) <= OUT_STRICT_RANGE:
+                stats["max_out_err_unit_range"] = max(stats["max_out_err_unit_range"], float(err.max()))
+                assert err.max() <= OUT_ATOL, \
+                    f"output of (b={b}, h={h}) off by {err.max():.3e} > {OUT_ATOL} (level {lv_o})"
             assert np.all(err <= OUT_ATOL + OUT_RTOL * np.abs(ref)), \
                 f"output of (b={b}, h={h}) off by {err.max():.3e} (level {lv_o})"
             if not marg:
@@ -201,4 +219,6 @@ def compare_decode(g, t1, r: O.DecodeResult, tau, eps, n_rep, check_sets=True):
     for b in range(B):
         if all(not marginal_head(r, b, h, eps) and group_exact[b, h // n_rep] for h in range(Hq)):
             assert int(g["level"][b]) == int(r.ladder_level[b])
+    assert stats["strict"] >= min_strict * stats["heads"], \
+        f"only {stats['strict']} of {stats['heads']} heads compared strictly: {stats}"
     return stats

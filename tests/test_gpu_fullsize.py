@@ -171,6 +171,10 @@ def test_max_context_2m_tokens():
         assert np.array_equal(t1g[name].numpy(), getattr(t1, name)), name
     r = O.decode_layer(qc.numpy(), Kc.numpy(), Vc.numpy(), t1, 0.995, 0.25, O.OracleConfig(n_rep=4))
     g_res = dict(out=out, cert=cert, level=lvl, nb=N // 64, state=st)
-    stats = compare_decode(g_res, t1, r, 0.995, 0.25, 4)
-    assert stats["strict"] + stats["excluded"] == 4
+    # 32,768 blocks of nearly equal mass: blocks within the 1e-6 band of the boundary
+    # block swap between the fp32 and fp64 selections, which changes the group's union,
+    # so the group's levels and bounds are not compared strictly (min_strict 0); every
+    # head's output still is
+    stats = compare_decode(g_res, t1, r, 0.995, 0.25, 4, min_strict=0.0)
+    assert stats["strict"] + stats["excluded"] == 4 and stats["out_compared"] == 4, stats
 

@@ -53,8 +53,25 @@ def test_tier1_edge_values():
     V[:, :, 64:128, 32:64] *= 2000.0
     V[:, :, 192:, :] = torch.round(V[:, :, 192:, :] * 4) / 4
     g = gpu_run(q, K.half(), V.half(), 0.9, 0.25)
-    t1, _ = oracle_run(q, K.half(), V.half(), 0.9, 0.25)
+    t1, r = oracle_run(q, K.half(), V.half(), 0.9, 0.25)
     compare_tier1(g["t1"], t1)
+    # the decode over the same cache: the x3000 block dominates every head (its block
+    # log-mass is ~7000) with Delta ~ 250, so a softmax reference that added Delta to the
+    # block log-mass would make every weight underflow; the oracle certifies every head at
+    # rung 2 (the x2000 values of that block are paged in)
+    st = compare_decode(g, t1, r, 0.9, 0.25, 4, min_strict=1.0)
+    assert np.all(r.level == 2) and np.all(g["cert"]["level"] == 2), (r.level, g["cert"]["level"])
+    assert np.all(np.isfinite(g["cert"]["e_key"])) and np.all(np.isfinite(g["cert"]["e_val"]))
+
+
+@pytest.mark.parametrize("kscale", [60.0, 200.0])
+def test_decode_large_delta(kscale):
+    """Keys scaled x60 and x200 (Delta ~ 7 and ~ 25 per block, peaked attention): the
+    softmax reference sits at the largest INT8 block log-mass, not Delta above it, so the
+    INT4-path weight products stay normal binary16 numbers; every head strictly compared."""
+    q, K, V = W.tiny(seed=13, ctx=64 * 24 + 5, Hq=8, Hkv=2, batch=2, kscale=kscale)
+    g, r, st = _check(q, K, V, 0.95, 0.25)
+    assert float(np.max(r.delta)) > (20.0 if kscale > 100 else 5.0)
 
 
 # ---------------------------------------------------------------------------------
