@@ -28,6 +28,8 @@ DEBUG_FORCE_RANK_FAIL = 0x1
 DEBUG_FORCE_DENSE = 0x2
 DEBUG_SYNC = 0x4
 DEBUG_PROFILE = 0x8
+DEBUG_BOUNDS = 0x10
+DEBUG_FAIL_MIRROR = 0x20
 
 HEAD_DIM = 128
 BLOCK = 64

@@ -45,6 +45,13 @@ kvq_status cuda_fail(cudaError_t e, const char* where) {
   } while (0)
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Names of the kernels that record bounds violations (BoundsSite order).
+const char* kBoundsSites[SITE_COUNT] = {"", "score", "select", "mixed_round0",
+                                        "mixed (second pass or FP16 values)", "combine",
+                                        "int4_tail", "dense_fallback", "finalize",
+                                        "quantize_append"};
+
 bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
 
 __global__ void fill_u32(uint32_t* p, uint32_t v, size_t n) {
@@ -140,7 +147,27 @@ LayerAppend append_view(kvq_cache* c, int l) {
   const int p = c->tail_parity[l];
   a.tail_k_in = layer_tail(c, l, p, 0); a.tail_v_in = layer_tail(c, l, p, 1);
   a.tail_k_out = layer_tail(c, l, 1 - p, 0); a.tail_v_out = layer_tail(c, l, 1 - p, 1);
+  a.counters = c->counters;
+  a.debug = c->debug;
   return a;
+}
+
+// KVQ_DEBUG_BOUNDS: the two bounds words are cleared before a call's kernels and read
+// (after a synchronise) once they have run; a recorded site fails the call.
+kvq_status bounds_clear(kvq_cache* c, cudaStream_t st) {
+  if (!(c->debug & KVQ_DEBUG_BOUNDS)) return KVQ_OK;
+  KVQ_CUDA(cudaMemsetAsync(c->counters + CNT_BOUNDS, 0, 2 * sizeof(unsigned int), st), "bounds: clear");
+  return KVQ_OK;
+}
+kvq_status bounds_report(kvq_cache* c, cudaStream_t st, const std::string& f) {
+  if (!(c->debug & KVQ_DEBUG_BOUNDS)) return KVQ_OK;
+  unsigned int w[2] = {0u, 0u};
+  KVQ_CUDA(cudaMemcpyAsync(w, c->counters + CNT_BOUNDS, sizeof(w), cudaMemcpyDeviceToHost, st), "bounds: read");
+  KVQ_CUDA(cudaStreamSynchronize(st), "bounds: sync");
+  if (w[0] == 0u) return KVQ_OK;
+  const char* site = w[0] < SITE_COUNT ? kBoundsSites[w[0]] : "unknown kernel";
+  return fail(KVQ_ERR_INVALID, f + ": bounds check failed in " + site + " (index " + std::to_string(w[1]) +
+                                   " out of range); the access was skipped");
 }
 
 bool is_device_ptr(const void* p) {
@@ -487,15 +514,19 @@ kvq_status kvq_append(kvq_cache* c, int layer, const void* k, const void* v, int
     // Earlier mirrors may still read the buffer this kernel overwrites (the ping-pong
     // partner of the last append): they are waited for first.
     KVQ_CUDA(cudaStreamWaitEvent(st, c->ev_mirror, 0), "kvq_append: wait mirror");
+    if (kvq_status bs = bounds_clear(c, st)) return bs;
     {
       KernelScope ks(c, K_APPEND, st);
       KVQ_CUDA(ks.done(launch_append(append_view(c, layer), k, v, n, pos, st)), "quantize_append");
     }
+    if (kvq_status bs = bounds_report(c, st, "kvq_append")) return bs;
     KVQ_CUDA(cudaEventRecord(c->ev_in, st), "kvq_append: event");
     KVQ_CUDA(cudaStreamWaitEvent(c->side, c->ev_in, 0), "kvq_append: wait");
     const int p_out = 1 - c->tail_parity[layer];
     const size_t spitch = (size_t)BLK * D * sizeof(__half);
     const size_t row0 = (size_t)(pos % BLK) * D;
+    if (c->debug & KVQ_DEBUG_FAIL_MIRROR)
+      return cuda_fail(cudaErrorInvalidValue, "kvq_append: mirror K (injected failure)");
     KVQ_CUDA(cudaMemcpy2DAsync(c->t2k_host[layer] + (size_t)pos * D, dpitch,
                                layer_tail(c, layer, p_out, 0) + row0, spitch, width, c->BG,
                                cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror K");
@@ -513,17 +544,21 @@ kvq_status kvq_append(kvq_cache* c, int layer, const void* k, const void* v, int
   // by the next decode, and the caller may reuse k and v)
   KVQ_CUDA(cudaEventRecord(c->ev_in, st), "kvq_append: event");
   KVQ_CUDA(cudaStreamWaitEvent(c->side, c->ev_in, 0), "kvq_append: wait");
+  if (c->debug & KVQ_DEBUG_FAIL_MIRROR)
+    return cuda_fail(cudaErrorInvalidValue, "kvq_append: mirror K (injected failure)");
   KVQ_CUDA(cudaMemcpy2DAsync(c->t2k_host[layer] + (size_t)pos * D, dpitch, k, width, width, c->BG,
                              cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror K");
   if (!c->v16)
     KVQ_CUDA(cudaMemcpy2DAsync(c->t2v_host[layer] + (size_t)pos * D, dpitch, v, width, width, c->BG,
                                cudaMemcpyDeviceToHost, c->side), "kvq_append: mirror V");
   KVQ_CUDA(cudaEventRecord(c->ev_mirror, c->side), "kvq_append: event");
+  if (kvq_status bs = bounds_clear(c, st)) return bs;
   {
     KernelScope ks(c, K_APPEND, st);
     KVQ_CUDA(ks.done(launch_append(append_view(c, layer), k, v, n, pos, st)), "quantize_append");
   }
   KVQ_CUDA(cudaStreamWaitEvent(st, c->ev_mirror, 0), "kvq_append: join");
+  if (kvq_status bs = bounds_report(c, st, "kvq_append")) return bs;
   c->n_tokens[layer] = pos + n;
   c->tail_parity[layer] ^= 1;
   return KVQ_OK;
@@ -615,6 +650,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   }
 
   const bool all_dense = certified && ((tau >= 1.f) || (c->debug & KVQ_DEBUG_FORCE_DENSE));
+  if (kvq_status bs = bounds_clear(c, st)) return bs;
   if (!all_dense) {
     { KernelScope s(c, K_SCORE, st); KVQ_CUDA(s.done(launch_score(V, score_grid(c->num_sms), st)), "score"); }
     { KernelScope s(c, K_SELECT, st); KVQ_CUDA(s.done(launch_select(V, st)), "select"); }
@@ -640,6 +676,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   }
   { KernelScope s(c, K_FINAL, st); KVQ_CUDA(s.done(launch_finalize(V, cd, ld, st)), "finalize"); }
   if (V.nres > 0) { KernelScope s(c, K_RESIDENT, st); KVQ_CUDA(s.done(launch_residency(V, st)), "residency"); }
+  if (kvq_status bs = bounds_report(c, st, f)) return bs;
 
   if (!out_dev) KVQ_CUDA(cudaMemcpyAsync(out, od, HQ * D * 2, cudaMemcpyDeviceToHost, st), "copy out");
   if (cert && !cert_dev) KVQ_CUDA(cudaMemcpyAsync(cert, cd, HQ * sizeof(kvq_certificate), cudaMemcpyDeviceToHost, st), "copy cert");

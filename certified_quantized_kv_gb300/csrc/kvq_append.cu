@@ -26,6 +26,9 @@ struct AppendArgs {
   __half* tail_v_out;
   int nbmax;
   __half* v16;              // FP16 values of full blocks (value_bits 16), or nullptr
+  unsigned int* counters;   // bounds-check words (KVQ_DEBUG_BOUNDS)
+  int debug;
+  int BG;
 };
 
 __device__ __forceinline__ int kc_offset(int t, int c) {
@@ -63,6 +66,9 @@ __global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
   const int tid = threadIdx.x;
   const int hs = blockIdx.y;
   const int blk = a.first_blk + blockIdx.x;
+  if (!bounds_ok(a.counters, a.debug, blk, a.nbmax, SITE_APPEND) ||
+      !bounds_ok(a.counters, a.debug, hs, a.BG, SITE_APPEND))
+    return;
   const int t0 = blk * BLK;                         // first token of the block
   const int end = a.pos + a.n;                      // tokens after the append
   const int t_hi = min(t0 + BLK, end);
@@ -297,6 +303,7 @@ cudaError_t launch_append(const LayerAppend& L, const void* k, const void* v, in
   a.tail_k_in = L.tail_k_in; a.tail_v_in = L.tail_v_in;
   a.tail_k_out = L.tail_k_out; a.tail_v_out = L.tail_v_out; a.nbmax = L.nbmax;
   a.v16 = L.v16;
+  a.counters = L.counters; a.debug = L.debug; a.BG = L.BG;
   const int last_blk = (pos + n - 1) / BLK;
   dim3 grid(last_blk - a.first_blk + 1, L.BG);
   const bool aligned = ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) == 0;

@@ -148,11 +148,35 @@ constexpr int CNT_DENSE_Q = 4;
 constexpr int CNT_DENSE_EXIT = 5;
 constexpr int CNT_ANY_DENSE = 6;    // set when a head reaches rung 3 (reset by the finaliser)
 constexpr int CNT_NEED_R1 = 7;      // set when a head plans rung 1 or 2 (reset by the finaliser)
+constexpr int CNT_BOUNDS = 8;       // KVQ_DEBUG_BOUNDS: site of the first violation (0: none)
+constexpr int CNT_BOUNDS_AT = 9;    // ... and the index that was out of range (low 32 bits)
 constexpr int CNT_GROUP_BASE = 16;  // + stage*BG + hs: per-group completion counters
 constexpr int N_STAGE_COUNTERS = 3;
 // + b after the four per-group stages: heads of sequence b at rung 3 after the ladder
 // plan (kept by the combine kernels, read by the dense pass, cleared by the finaliser)
 __host__ __device__ constexpr int cnt_rung3(int BG, int b) { return CNT_GROUP_BASE + 4 * BG + b; }
+
+// ---------------------------------------------------------------------------------
+// bounds checks (KVQ_DEBUG_BOUNDS)
+// ---------------------------------------------------------------------------------
+
+constexpr int DBG_BOUNDS = 0x10;   // the KVQ_DEBUG_BOUNDS bit of kvq_set_debug
+// Kernels that check their indices; the host turns a recorded site into the kernel name.
+enum BoundsSite : unsigned {
+  SITE_SCORE = 1, SITE_SELECT, SITE_MIX0, SITE_MIX, SITE_COMBINE, SITE_TAIL, SITE_DENSE,
+  SITE_FINAL, SITE_APPEND, SITE_COUNT
+};
+
+// With DBG_BOUNDS set, an index about to address an array of n elements is checked: the
+// first index outside [0, n) of the call is recorded (site, index) in two counter words
+// and false is returned, so the caller skips the access.  Nothing traps; the host reads
+// the words after the call.  Without the flag this is one test of a uniform value.
+__device__ __forceinline__ bool bounds_ok(unsigned int* counters, int debug, long long i, long long n,
+                                          unsigned site) {
+  if (!(debug & DBG_BOUNDS) || (i >= 0 && i < n)) return true;
+  if (atomicCAS(&counters[CNT_BOUNDS], 0u, site) == 0u) counters[CNT_BOUNDS_AT] = (unsigned int)i;
+  return false;
+}
 
 // ---------------------------------------------------------------------------------
 // small helpers

@@ -155,6 +155,16 @@ __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) 
     if (mask == 0) { __syncthreads(); continue; }
     const int hs = item / nch, ch = item % nch;
     const int b = hs / V.Hkv, g = hs % V.Hkv;
+    {   // the item's group, partial slot, blocks (tier 1, scratch) and tier-2 rows
+      const long long be = min(V.nb, (ch + 1) * V.chunk);
+      if (!bounds_ok(V.counters, V.debug, hs, V.BG, SITE_DENSE) ||
+          !bounds_ok(V.counters, V.debug, ch, V.nslot, SITE_DENSE) ||
+          !bounds_ok(V.counters, V.debug, be, (long long)V.nbmax + 1, SITE_DENSE) ||
+          !bounds_ok(V.counters, V.debug, be * BLK, V.cap + 1, SITE_DENSE)) {
+        __syncthreads();
+        continue;
+      }
+    }
     if (hs != cur_hs) {
       cur_hs = hs;
       for (int i = tid; i < MAXREP * D; i += blockDim.x) {

@@ -18,6 +18,8 @@ struct LayerAppend {
   __half* v16;   // FP16 values of full blocks (value_bits 16), or nullptr
   const __half* tail_k_in; const __half* tail_v_in;
   __half* tail_k_out; __half* tail_v_out;
+  unsigned int* counters;   // bounds-check words (KVQ_DEBUG_BOUNDS)
+  int debug;
 };
 
 cudaError_t launch_append(const LayerAppend& L, const void* k, const void* v, int n, int pos,

@@ -148,6 +148,16 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
     if (sm.skip) { __syncthreads(); continue; }
     const int hs = item / nch, ch = item % nch;
     const int b = hs / V.Hkv, g = hs % V.Hkv;
+    {   // the item's group, partial slot, blocks (tier 1, scratch) and tier-2 rows
+      const long long be = min(V.nb, (ch + 1) * V.chunk);
+      if (!bounds_ok(V.counters, V.debug, hs, V.BG, SITE_MIX) ||
+          !bounds_ok(V.counters, V.debug, ch, V.nslot, SITE_MIX) ||
+          !bounds_ok(V.counters, V.debug, be, (long long)V.nbmax + 1, SITE_MIX) ||
+          !bounds_ok(V.counters, V.debug, be * BLK, V.cap + 1, SITE_MIX)) {
+        __syncthreads();
+        continue;
+      }
+    }
 
     if (hs != cur_hs) {
       cur_hs = hs;
@@ -391,6 +401,10 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   const int nb = V.nb;
   const int nch = V.nparts > 0 ? V.nparts : max(1, (nb + V.chunk - 1) / V.chunk);
   const int NCH = V.nslot;
+  if (!bounds_ok(V.counters, V.debug, hs, V.BG, SITE_COMBINE) ||
+      !bounds_ok(V.counters, V.debug, nch, (long long)NCH + 1, SITE_COMBINE) ||
+      !bounds_ok(V.counters, V.debug, nb, (long long)V.nbmax + 1, SITE_COMBINE))
+    return;
   const uint8_t* kfl = (round == 0 ? V.kprom0 : V.kprom1) + (size_t)hs * V.nbmax;
   // first pass: no FP16 values yet (every head's rung 2 plans against this empty set,
   // while its marks accumulate in vprom1 for the second pass)
@@ -719,6 +733,16 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
     const int hs = item / nch, ch = item % nch;
     const int b = hs / V.Hkv, g = hs % V.Hkv;
     const size_t hrow = head_row(V, b, g, 0);
+    {   // the item's group, partial slot, blocks (tier 1, scratch) and tier-2 rows
+      const long long be = min(V.nb, (ch + 1) * V.chunk);
+      if (!bounds_ok(V.counters, V.debug, hs, V.BG, SITE_MIX0) ||
+          !bounds_ok(V.counters, V.debug, ch, V.nslot, SITE_MIX0) ||
+          !bounds_ok(V.counters, V.debug, be, (long long)V.nbmax + 1, SITE_MIX0) ||
+          !bounds_ok(V.counters, V.debug, be * BLK, V.cap + 1, SITE_MIX0)) {
+        __syncthreads();
+        continue;
+      }
+    }
     if (hs != cur_hs) {
       cur_hs = hs;
       for (int i = tid; i < MAXREP * D; i += blockDim.x) {

@@ -84,11 +84,13 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
       if (h == 0 && pblk == V.nb) { pblk = 0; ++phs; }
       const size_t pbi = (size_t)phs * V.nbmax + pblk;
       ScoreHalf& st = ring[u % SCORE_STAGES];
-      const uint4* kp = reinterpret_cast<const uint4*>(V.kc + pbi * KC_BYTES) + 256 * h;
+      if (bounds_ok(V.counters, V.debug, (long long)pbi, (long long)V.BG * V.nbmax, SITE_SCORE)) {
+        const uint4* kp = reinterpret_cast<const uint4*>(V.kc + pbi * KC_BYTES) + 256 * h;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) cp_async16_hint(&st.codes[lane + 32 * j], kp + lane + 32 * j, pol);
-      if (h == 0 && lane < 16)
-        cp_async16_hint(&st.scales[lane], reinterpret_cast<const uint4*>(V.ks + pbi * D) + lane, pol);
+        for (int j = 0; j < 8; ++j) cp_async16_hint(&st.codes[lane + 32 * j], kp + lane + 32 * j, pol);
+        if (h == 0 && lane < 16)
+          cp_async16_hint(&st.scales[lane], reinterpret_cast<const uint4*>(V.ks + pbi * D) + lane, pol);
+      }
       if (h == 1) ++pblk;
     }
     cp_async_commit();
@@ -141,6 +143,7 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
   if (units > 0) setup_q((int)(g0 / V.nb));   // overlaps the first copy
 
   int hs = (int)(g0 / V.nb), blk = (int)(g0 % V.nb) - 1;
+  bool wok = true;   // the block's result rows are inside the score scratch
   uint32_t bf[16];
   float x[8];
   for (int u = 0; u < units; ++u) {
@@ -151,6 +154,7 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
     const int h = u & 1;
     if (h == 0) {
       if (++blk == V.nb) { blk = 0; ++hs; }
+      wok = bounds_ok(V.counters, V.debug, (long long)hs * V.nbmax + blk, (long long)V.BG * V.nbmax, SITE_SCORE);
       if (hs != cur_hs) setup_q(hs);
       // products q_c s_c 2^e of head hp at channels 16 sub + [0, 16), split hi + lo
       const uint4 S0 = cur.scales[2 * sub], S1 = cur.scales[2 * sub + 1];
@@ -176,7 +180,7 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
       dp += __shfl_xor_sync(0xffffffffu, dp, 1);   // sum_c |q_c| s_c 2^e of head hp
       dp += __shfl_xor_sync(0xffffffffu, dp, 2);
       dp += __shfl_xor_sync(0xffffffffu, dp, 4);
-      if (sub == 0 && hp < V.n_rep)
+      if (wok && sub == 0 && hp < V.n_rep)
         V.delta[(size_t)(hs * V.n_rep + hp) * V.nbmax + blk] = KAPPA * INV_SQRT_D * (dp * inv_pre);
       __syncwarp();
       // B fragments of column gid = (head gid>>1, hi or lo): k-step kk takes pairs
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
     __syncwarp();   // every lane is done with this slot before it is refilled
     if (h == 1) {
       const int hrow = hs * V.n_rep;   // query-head row of slot 0 (b Hq + g n_rep)
-      if (tig < V.n_rep) {
+      if (wok && tig < V.n_rep) {
         float* sh = V.shat + (size_t)(hrow + tig) * ((size_t)V.nbmax * BLK) + (size_t)blk * BLK + gid;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
       l += __shfl_xor_sync(0xffffffffu, l, 8);
       l += __shfl_xor_sync(0xffffffffu, l, 16);
       // lane tig (gid 0) holds lse of head tig
-      if (gid == 0 && tig < V.n_rep)
+      if (wok && gid == 0 && tig < V.n_rep)
         V.lse8[(size_t)(hrow + tig) * V.nbmax + blk] = m + logf(l);
     }
   }
@@ -259,6 +263,9 @@ __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
   const int hs = b * V.Hkv + g;
   const int nb = V.nb, nbp = (nb + 15) & ~15;
   const size_t hb = (size_t)bh;
+  if (!bounds_ok(V.counters, V.debug, nb, (long long)V.nbmax + 1, SITE_SELECT) ||
+      !bounds_ok(V.counters, V.debug, hs, V.BG, SITE_SELECT))
+    return;
   // exact scores of the partial FP16 block (counts as covered)
   float tmax = -INFINITY;
   if (tid < V.n_tail) {

@@ -62,6 +62,10 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
     const int b1 = (int)((long long)(run + 1) * V.nb / runs);
     const int hrow = hs * V.n_rep;
     const bool act = hp < V.n_rep;
+    if (!bounds_ok(V.counters, V.debug, hs, V.BG, SITE_TAIL) ||
+        !bounds_ok(V.counters, V.debug, run, V.nslot, SITE_TAIL) ||
+        !bounds_ok(V.counters, V.debug, b1, (long long)V.nbmax + 1, SITE_TAIL))
+      continue;
     const float M = act ? V.hst[hrow + hp].M : 0.f;
     const int pre_e = prescale_exp(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
     const float pre_ef = (float)pre_e;

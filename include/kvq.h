@@ -111,6 +111,14 @@ typedef struct kvq_cache kvq_cache;
 #define KVQ_DEBUG_FORCE_DENSE     0x2  /* every head takes rung 4 */
 #define KVQ_DEBUG_SYNC            0x4  /* synchronise and check after every kernel */
 #define KVQ_DEBUG_PROFILE         0x8  /* time every kernel with CUDA events */
+#define KVQ_DEBUG_BOUNDS          0x10 /* kernels check the indices they address tier 1, tier 2
+                                          and scratch with; the first one out of range is
+                                          recorded (the access skipped, nothing traps) and
+                                          the call synchronises and returns KVQ_ERR_INVALID
+                                          naming the kernel */
+#define KVQ_DEBUG_FAIL_MIRROR     0x20 /* test aid: kvq_append's tier-2 mirror copy reports a
+                                          CUDA error without being issued; the call returns
+                                          KVQ_ERR_CUDA and the cache keeps its length */
 
 /* kvq_cache_create -- allocate tier 1 (device), tier 2 (pinned, mapped host memory) and
  * scratch for `n_layers` layers of `batch` sequences of up to `max_ctx` tokens (Method §1).
