@@ -64,6 +64,36 @@ def test_tier1_edge_values():
     assert np.all(np.isfinite(g["cert"]["e_key"])) and np.all(np.isfinite(g["cert"]["e_val"]))
 
 
+def test_tier1_exact_ties():
+    """Keys and values at exact half steps of their scales (code ties, resolved to even on
+    both sides), next to values just off them: the quantiser's codes, scales and eta stay
+    bit-exact with the oracle, including the rare path that divides exactly."""
+    gen = torch.Generator().manual_seed(21)
+    n_blk, D = 6, 128
+    N = 64 * n_blk + 7
+    s0, v0 = 2.0 ** -5, 2.0 ** -3
+    K = torch.zeros(1, 2, N, D, dtype=torch.float64)
+    V = torch.zeros(1, 2, N, D, dtype=torch.float64)
+    for b in range(n_blk):
+        rows = slice(64 * b, 64 * b + 64)
+        n = torch.randint(-126, 126, (64, D), generator=gen).double()
+        K[0, :, rows] = (n + 0.5) * s0                       # K / s = n + 1/2 exactly
+        K[0, :, 64 * b] = 127 * s0                            # pins every channel scale to s0
+        m = torch.randint(0, 15, (64, D), generator=gen).double()
+        V[0, :, rows] = (m + 0.5) * v0
+        V[0, :, rows, 0::32] = 0.0                            # group min 0 ...
+        V[0, :, rows, 1::32] = 15 * v0                        # ... and max 15 v0: scale v0
+        if b % 2:                                             # just off the ties: +- 2^-11 v0
+            V[0, :, rows, 2::5] += v0 * 2.0 ** -11 * torch.sign(torch.randn(64, 26, generator=gen)).double()[:, :1]
+    K[0, :, 64 * n_blk:] = torch.randn(2, 7, D, generator=gen).double()
+    V[0, :, 64 * n_blk:] = torch.randn(2, 7, D, generator=gen).double()
+    q = torch.randn(1, 8, D, generator=gen).half()
+    g = gpu_run(q, K.half(), V.half(), 0.9, 0.25, chunks=[100, N - 100])
+    t1, _ = oracle_run(q, K.half(), V.half(), 0.9, 0.25)
+    compare_tier1(g["t1"], t1)
+    assert np.any(t1.kc % 2 == 0) and np.any(t1.kc % 2 != 0)
+
+
 @pytest.mark.parametrize("kscale", [60.0, 200.0])
 def test_decode_large_delta(kscale):
     """Keys scaled x60 and x200 (Delta ~ 7 and ~ 25 per block, peaked attention): the
