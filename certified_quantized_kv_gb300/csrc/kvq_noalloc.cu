@@ -19,7 +19,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <mutex>
 #include <string>
 
 #include "kvq.h"
@@ -36,12 +35,9 @@ using namespace kvq;
 constexpr size_t NOALLOC_SCRATCH_BYTES = 8u << 20;   // 8 MiB per device
 constexpr int NA_CHUNK = 16;                           // blocks per work item
 constexpr int NA_PART = MAXREP * (D + 4);              // floats per (group, chunk) partial
-constexpr int NA_MAX_DEVICES = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
-std::mutex g_mu;
-void* g_scratch_ptr[NA_MAX_DEVICES] = {};
 
 struct NaArgs {
   const __half* q;    // [B][Hq][128]
@@ -176,23 +172,15 @@ __global__ void __launch_bounds__(128) noalloc_dense_kernel(NaArgs a) {
   }
 }
 
-// Device address of this device's scratch array, looked up once per device (the first
-// call on a device; the lookup also makes the driver load this library's device code on
-// that device, which is when the array's memory is reserved).  A cudaDeviceReset unloads
-// the code and frees the array; this entry point is not for use after one.
+// Device address of this device's scratch array, looked up on every call (the lookup is
+// cheap and allocates nothing; the first one on a device also makes the driver load this
+// library's device code there, which is when the array's memory is reserved).  Looking
+// it up each time keeps the address right if the device code was loaded again.
 cudaError_t scratch_for_current_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= NA_MAX_DEVICES) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

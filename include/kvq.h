@@ -256,12 +256,12 @@ kvq_status kvq_debug_fill_tier2(kvq_cache* cache, int layer, uint16_t bits);
  * Size limit: B * Hkv * ceil(n_tokens / 1024) * 2112 bytes of partials (plus a few
  * counters) must fit in the 8 MiB array, e.g. B * Hkv = 8 with up to 507904 tokens.
  * The array exists once per device that loads the library and is held until the
- * process exits.  The first call on a device, with that device current, looks up the
- * array's device address; make that first call before any stream capture.  With the
- * CUDA driver's lazy loading that first call is also when the library's device code,
- * and with it the 8 MiB array, is loaded onto the device: make it while 8 MiB of device
- * memory are still free (before another pool takes the rest), or it fails with
- * KVQ_ERR_CUDA.  A cudaDeviceReset frees the array; the call is not for use after one.
+ * process exits.  Every call, with the device current, looks up the array's device
+ * address (no allocation); make the first call on a device before any stream capture.
+ * With the CUDA driver's lazy loading that first call is also when the library's device
+ * code, and with it the 8 MiB array, is loaded onto the device: make it while 8 MiB of
+ * device memory are still free (before another pool takes the rest), or it fails with
+ * KVQ_ERR_CUDA.  After a cudaDeviceReset the next call loads the array again.
  * Every call shares the array and clears the counters it needs itself; calls whose work
  * overlaps on the GPU (other streams, other host threads) race on it and must be
  * serialised.  The kernel runs on the current device, on `stream`.
