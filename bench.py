@@ -548,10 +548,68 @@ def measure_residency(args, wl, frac=0.25, layers=4):
 
 
 
+def time_back_to_back(torch, call, reps=20, batches=5, warmup=3):
+    """Device time per call (ms): `reps` calls enqueued back to back between two CUDA
+    events, so the host's enqueue time hides behind the GPU; median over `batches`."""
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    res = []
+    for _ in range(batches):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        res.append(e0.elapsed_time(e1) / reps)
+    return statistics.median(res)
+
+
+def time_dense_hbm(torch, kvq, q, K, V):
+    """Device time (ms) of one kvq_dense_attention call (dense FP16 attention over K/V in
+    HBM) on these device tensors; K and V are read once per call."""
+    out = torch.empty(q.shape, dtype=torch.float16, device="cuda")
+    ws = kvq.dense_attention(q, K, V, out)
+    return time_back_to_back(torch, lambda: kvq.dense_attention(q, K, V, out, ws))
+
+
+def measure_dense_hbm(args, wl, t_cert_layer_us, t_unc_layer_us):
+    """Dense FP16 decode attention with the whole FP16 cache in HBM (kvq_dense_attention)
+    on one layer of the headline caches: the dense baseline the pages quote the certified
+    step against (Results, performance overhead: 2.7-4.8x slower than dense attention,
+    hardware unstated).  K and V (512 B per token and KV head) exceed L2 many times over,
+    so every call streams them from HBM."""
+    import torch
+    import certified_quantized_kv_gb300 as kvq
+    import workloads as W
+    B, N, Hq, Hkv = wl["batch"], wl["ctx"], wl["q_heads"], wl["kv_heads"]
+    q, K, V = W.c3_layer(0, device="cuda", seed=wl["seed"], batch=B, ctx=N, Hq=Hq, Hkv=Hkv)
+    q, K, V = q.contiguous(), K.contiguous(), V.contiguous()
+    ms = time_dense_hbm(torch, kvq, q, K, V)
+    del K, V
+    torch.cuda.empty_cache()
+    hbm_peak, peak_kind = _peaks()
+    b = B * Hkv * N * F16_BYTES_PER_TOKEN_HEAD
+    us = 1e3 * ms
+    return {"value": B / (ms / 1e3), "unit": UNIT, "us_per_layer": us,
+            "roofline": {"bound": "hbm", "kernel": "dense_hbm (split pass + combine)", "achieved": b / (us * 1e-6) / 1e9,
+                         "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": b / (us * 1e-6) / 1e9 / hbm_peak, "algorithmic_bytes_per_launch": b},
+            "certified_over_dense": t_cert_layer_us / us,
+            "uncertified_over_dense": t_unc_layer_us / us,
+            "pages_certified_over_dense": "2.7-4.8x (Results, performance overhead; hardware unstated)",
+            "vram_bytes_per_token_head": {"dense_fp16": 512, "certified_tier1": TIER1_BYTES_PER_TOKEN_HEAD},
+            "what": "kvq_dense_attention: exact FP16 attention, K/V resident in HBM, one 128K layer of the headline "
+                    "caches; device time per call from batches of back-to-back calls between CUDA events"}
+
+
 def measure_configs(args, with_oracle: bool) -> dict:
     """The other workloads' shapes (4K x 1, concentrated 32K x 4, planted-needle 64K x 8):
-    the median of 20 certified decode calls after 5 warm-up calls on the GPU, next to
-    the oracle on all host cores and on one core (bounded samples, scaled to the layer)."""
+    device time per certified decode call (batches of 20 back-to-back calls after 5
+    warm-up calls, median over the batches) and per dense FP16 call over the same K/V in
+    HBM, next to the oracle on all host cores and on one core (bounded samples, scaled
+    to the layer)."""
     import torch
     import certified_quantized_kv_gb300 as kvq
     import workloads as W
@@ -564,25 +622,18 @@ def measure_configs(args, with_oracle: bool) -> dict:
         B, Hq, Hkv, N = q.shape[0], q.shape[1], K.shape[1], K.shape[2]
         cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=N)
         cache.append(0, K.contiguous(), V.contiguous())
-        del K, V
         q = q.contiguous()
+        dense_ms = time_dense_hbm(torch, kvq, q, K.contiguous(), V.contiguous())
+        del K, V
         out = torch.empty(B, Hq, 128, dtype=torch.float16, device="cuda")
         cert = torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda")
-        for _ in range(5):
-            cache.decode(0, q, cfg.tau_cov, cfg.eps, out, cert)
-        times = []
-        for _ in range(20):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            cache.decode(0, q, cfg.tau_cov, cfg.eps, out, cert)
-            e1.record()
-            torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1))
-        ms = statistics.median(times)
+        ms = time_back_to_back(torch, lambda: cache.decode(0, q, cfg.tau_cov, cfg.eps, out, cert), warmup=5)
         c = kvq.certificates(cert).reshape(B, Hq)
         res[name] = {"gpu": {"value": B / (ms / 1e3), "unit": UNIT, "us_per_call": 1e3 * ms,
                              "ladder_histogram": [int(x) for x in np.bincount(c["level"].ravel(), minlength=5)],
-                             "promoted_bytes": int(c["promoted_bytes"][:, :: Hq // Hkv].sum())}}
+                             "promoted_bytes": int(c["promoted_bytes"][:, :: Hq // Hkv].sum())},
+                     "dense_fp16_hbm": {"us_per_call": 1e3 * dense_ms, "value": B / (dense_ms / 1e3), "unit": UNIT,
+                                        "certified_over_dense": ms / dense_ms}}
         cache.close()
         torch.cuda.empty_cache()
     if with_oracle:
@@ -867,6 +918,7 @@ def our_arm(args, wl):
         "append": append,
     })
     cache.close()
+    line["dense_fp16_hbm"] = measure_dense_hbm(args, wl, t_layer_us, 1e3 * unc_ms / L)
     line["fp16_values"] = measure_fp16_values(args, wl)
     line["residency"] = measure_residency(args, wl)
     line["configs"] = measure_configs(args, args.cpu_baseline)

@@ -84,6 +84,8 @@ def load_library() -> ctypes.CDLL:
         "kvq_export_decode_state": [vp, vp, vp, vp, vp, vp, vp, vp],
         "kvq_profile_read": [vp, ctypes.POINTER(kvq_kernel_stat), i32, ctypes.POINTER(i32), i32],
         "kvq_dense_decode_noalloc": [vp, vp, vp, i32, i32, i32, i32, vp, vp],
+        "kvq_dense_attention_workspace": [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_size_t)],
+        "kvq_dense_attention": [vp, vp, vp, i32, i32, i32, i32, vp, vp, ctypes.c_size_t, vp],
         "kvq_debug_fill_tier2": [vp, i32, ctypes.c_uint16],
         "kvq_residency_stats": [vp, i32, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64),
                                 ctypes.POINTER(i32), i32],
@@ -297,6 +299,42 @@ def dense_decode_noalloc(q, k, v, out, stream=None):
         return
     _check(load_library().kvq_dense_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N,
                                                    _ptr(out), _stream(stream)))
+
+
+def dense_attention_workspace(batch: int, n_q_heads: int, n_kv_heads: int, n_tokens: int) -> int:
+    """Workspace bytes kvq_dense_attention needs for this shape on the current device."""
+    n = ctypes.c_size_t(0)
+    _check(load_library().kvq_dense_attention_workspace(batch, n_q_heads, n_kv_heads, n_tokens, ctypes.byref(n)))
+    return int(n.value)
+
+
+def dense_attention(q, k, v, out, workspace=None, stream=None):
+    """Exact dense FP16 decode attention over K/V in device memory (kvq_dense_attention).
+
+    q, out: device fp16 [B, Hq, 128]; k, v: device fp16 [B, Hkv, n_tokens, 128].
+    `workspace` is a device uint8 tensor of at least dense_attention_workspace(...) bytes
+    (allocated here when omitted).  Returns `workspace` so a caller can reuse it.
+    """
+    import torch
+    if q.dim() != 3 or k.dim() != 4:
+        raise ValueError("q must be [batch, n_q_heads, 128] and k, v [batch, n_kv_heads, n_tokens, 128]")
+    B, Hq, _ = q.shape
+    Hkv, N = k.shape[1], k.shape[2]
+    _need(q, "q", torch.float16, (B, Hq, HEAD_DIM))
+    _need(k, "k", torch.float16, (B, Hkv, N, HEAD_DIM))
+    _need(v, "v", torch.float16, (B, Hkv, N, HEAD_DIM))
+    _need(out, "out", torch.float16, (B, Hq, HEAD_DIM))
+    dev = q.device
+    if dev.type != "cuda" or any(t.device != dev for t in (k, v, out)):
+        raise ValueError("q, k, v and out must be on one CUDA device")
+    with torch.cuda.device(dev):
+        need = dense_attention_workspace(B, Hq, Hkv, N)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+        _need(workspace, "workspace", torch.uint8, nbytes=need)
+        _check(load_library().kvq_dense_attention(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, N, _ptr(out),
+                                                  _ptr(workspace), workspace.numel(), _stream(stream)))
+    return workspace
 
 
 def header_functions(header_path: str | None = None) -> list[str]:

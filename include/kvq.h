@@ -242,6 +242,32 @@ kvq_status kvq_residency_stats(kvq_cache* cache, int layer, int64_t* resident_by
  * Errors: KVQ_ERR_INVALID (NULL cache, layer out of range), KVQ_ERR_CUDA. */
 kvq_status kvq_debug_fill_tier2(kvq_cache* cache, int layer, uint16_t bits);
 
+/* kvq_dense_attention_workspace -- device workspace bytes that kvq_dense_attention needs
+ * for this shape on the current device (it depends on the device's SM count).
+ * Errors: KVQ_ERR_INVALID (NULL bytes, bad shape), KVQ_ERR_CUDA. */
+kvq_status kvq_dense_attention_workspace(int batch, int n_q_heads, int n_kv_heads, int n_tokens,
+                                         size_t* bytes);
+
+/* kvq_dense_attention -- exact dense FP16 decode attention, softmax(q K^T / sqrt(D)) V,
+ * over keys and values held in device memory.  This is the dense FP16 attention that
+ * Method §1 names as the ground truth and that Results (performance overhead) sets the
+ * certified step against; the library uses it as that baseline on the same GPU.
+ *   q         [B, Hq, D] FP16, device;  k, v [B, Hkv, n_tokens, D] FP16, device
+ *   out       [B, Hq, D] FP16, device (caller-owned)
+ *   workspace device buffer of at least kvq_dense_attention_workspace(...) bytes,
+ *             caller-owned; its contents need no initialisation and are overwritten
+ *   Hq / Hkv in 1..4, n_tokens >= 1; q, k, v, out and workspace 16-byte aligned and on
+ *   the current device.
+ * Two kernels on `stream`: a split pass that streams every key and value once from HBM
+ * and a fixed-order combine.  Every device-side wait of the split pass is bounded (2 s);
+ * a wait that runs out, which does not happen in correct operation, makes the affected
+ * heads' outputs NaN.  Calls that share a workspace must not overlap on the GPU.
+ * Stream-ordered.  Errors: KVQ_ERR_INVALID (NULL, host, unaligned or other-device
+ * pointers, bad shape, workspace too small), KVQ_ERR_CUDA. */
+kvq_status kvq_dense_attention(const void* q, const void* k, const void* v, int batch, int n_q_heads,
+                               int n_kv_heads, int n_tokens, void* out, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
 /* kvq_dense_decode_noalloc -- exact dense FP16 decode attention that allocates no memory.
  * The paper has no counterpart to this call.  It is for callers that cannot allocate
  * device memory when they call: a process whose device memory is fully held by another
