@@ -9,14 +9,21 @@
 // mixed pass (channels as MMA rows, tokens as k, the eight columns = four heads x the hi
 // and lo halves of p s 2^e, exact in f16), the second on the CUDA cores.
 //
+// This pass runs in the uncertified call, where no block is paged in: every full block
+// of the layer keeps its INT8 scores and INT4 values.
+//
 // Work split: one warp per run of consecutive blocks of one KV group (runs per group =
 // warps / groups), no CTA barrier; each block's codes, scales/offsets and scores reach
 // shared memory by cp.async through a two-stage ring per warp, so the next block is in
 // flight while the current one is multiplied.  Each run writes one partial (sum p v_hat,
 // sum p and the reference M per head) into its own slot, which the combine kernel adds
-// in a fixed order.  The weights carry the value prescale 2^e from the start
-// (p 2^e = 2^((s - M) log2 e + e)), and the INT4 codes enter the MMA as binary16
-// subnormals (see nib8_to_sub_f16x4); both scalings are undone once per run.
+// in a fixed order.  The weights carry a prescale 2^e from the start
+// (p 2^e = 2^((s - M) log2 e + e)) and are split once per token into binary16 halves
+// p_hi + p_lo; each product p s (s a binary16 scale) is then formed as two binary16
+// halves in three packed-half instructions per token pair: hi = rn(p_hi s), the exact
+// remainder p_hi s - hi by a fused multiply-add, plus p_lo s in a second one (together
+// within about 2^-21 of p s).  The INT4 codes enter the MMA as binary16 subnormals (see
+// nib8_to_sub_f16x4); both scalings are undone once per run.
 #include "kvq_common.cuh"
 #include "kvq_launch.h"
 
@@ -67,15 +74,10 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
         !bounds_ok(V.counters, V.debug, b1, (long long)V.nbmax + 1, SITE_TAIL))
       continue;
     const float M = act ? V.hst[hrow + hp].M : 0.f;
-    const int pre_e = prescale_exp(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
+    // weights p 2^e <= 2^e must be finite binary16 values: e <= 15
+    const int pre_e = min(15, prescale_exp(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs]))));
     const float pre_ef = (float)pre_e;
-    const uint8_t* kp0 = V.kprom0 + (size_t)hs * V.nbmax;
-    // the run's blocks that keep INT8 scores (FP16-key blocks are the mixed pass's)
-    auto next_block = [&](int b) {
-      while (b < b1 && kp0[b]) ++b;
-      return b;
-    };
-    int pb = next_block(b0);   // producer: next block to copy
+    int pb = b0;   // producer: next block to copy
     auto issue = [&](int st) {
       if (pb < b1) {
         const size_t bi = (size_t)hs * V.nbmax + pb;
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
           if (h < V.n_rep)
             cp_async16_hint(&T.s[idx], V.shat + (size_t)(hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)pb * BLK + 4 * (idx & 15), pol);
         }
-        pb = next_block(pb + 1);
+        ++pb;
       }
       cp_async_commit();
     };
@@ -104,26 +106,34 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[g][mt][j] = 0.f;
-    float off[NG] = {0.f, 0.f, 0.f, 0.f};   // sum p o per value group, head hp, tokens of this lane
-    float lsum = 0.f;                        // sum p, head hp, tokens of this lane
+    float2 off[NG];   // sum p o per value group, head hp, tokens of this lane (pairs)
+#pragma unroll
+    for (int g = 0; g < NG; ++g) off[g] = make_float2(0.f, 0.f);
+    float lsum = 0.f;  // sum p, head hp, tokens of this lane
 
     issue(0);
     int it = 0;
-    for (int blk = next_block(b0); blk < b1; blk = next_block(blk + 1), ++it) {
+    for (int blk = b0; blk < b1; ++blk, ++it) {
       issue((it + 1) % TAIL_STAGES);
       cp_async_wait<1>();
       __syncwarp();
       const TailStage& T = ring[it % TAIL_STAGES];
-      // weights of head hp at tokens 8 sub + [0, 8), times the prescale 2^e
-      float pp[8];
+      // weights of head hp at tokens 8 sub + [0, 8), times 2^e: fp32 pairs and their
+      // binary16 halves (token pair i = tokens 8 sub + 2i, +1)
+      float2 pf[4];
+      __half2 ph[4], pl[4];
       {
         const float4 sa = T.s[hp * (BLK / 4) + 2 * sub], sb = T.s[hp * (BLK / 4) + 2 * sub + 1];
         const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float p = act ? exp2_approx(fmaf(sv[i] - M, LOG2E_F, pre_ef)) : 0.f;
-          lsum += p;
-          pp[i] = p;
+        for (int i = 0; i < 4; ++i) {
+          const float p0 = act ? exp2_approx(fmaf(sv[2 * i] - M, LOG2E_F, pre_ef)) : 0.f;
+          const float p1 = act ? exp2_approx(fmaf(sv[2 * i + 1] - M, LOG2E_F, pre_ef)) : 0.f;
+          lsum += p0 + p1;
+          pf[i] = make_float2(p0, p1);
+          ph[i] = __floats2half2_rn(p0, p1);
+          const float2 r = sub2(pf[i], __half22float2(ph[i]));   // exact
+          pl[i] = __floats2half2_rn(r.x, r.y);
         }
       }
 #pragma unroll
@@ -134,15 +144,15 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
 #pragma unroll
         for (int i = 0; i < 4; ++i) {   // token pair 4 sub + i: tokens 8 sub + 2i, +1
           const uint4& S = (i < 2) ? S0 : S1;
-          const float2 a = __half22float2(u32_as_h2(word_of(S, 2 * (i & 1))));       // (scale, offset)
-          const float2 c = __half22float2(u32_as_h2(word_of(S, 2 * (i & 1) + 1)));
-          off[g] = fmaf(pp[2 * i], a.y, off[g]);
-          off[g] = fmaf(pp[2 * i + 1], c.y, off[g]);
-          const float2 w = mul2(make_float2(pp[2 * i], pp[2 * i + 1]), make_float2(a.x, c.x));
-          const __half2 hi = __floats2half2_rn(w.x, w.y);
-          const float2 rem = sub2(w, __half22float2(hi));   // exact remainders
+          const __half2 a = u32_as_h2(word_of(S, 2 * (i & 1)));       // (scale, offset) of token 2i
+          const __half2 c = u32_as_h2(word_of(S, 2 * (i & 1) + 1));   // ... of token 2i + 1
+          const __half2 s2 = __lows2half2(a, c), o2 = __highs2half2(a, c);
+          const __half2 hi = __hmul2_rn(ph[i], s2);
+          __half2 lo = __hfma2(ph[i], s2, __hneg2(hi));   // p_hi s - hi, exact
+          lo = __hfma2(pl[i], s2, lo);
           hw[i] = h2_as_u32(hi);
-          lw[i] = h2_as_u32(__floats2half2_rn(rem.x, rem.y));
+          lw[i] = h2_as_u32(lo);
+          off[g] = fma2(pf[i], __half22float2(o2), off[g]);
         }
         uint32_t* wr = tw + hp * (2 * TW_ROW) + 4 * sub;
         *reinterpret_cast<uint4*>(wr) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
@@ -170,11 +180,13 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
     __syncwarp();
 
     // head hp's sums are spread over its eight product lanes
+    float offs[NG];
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
-      off[g] += __shfl_xor_sync(0xffffffffu, off[g], 1);
-      off[g] += __shfl_xor_sync(0xffffffffu, off[g], 2);
-      off[g] += __shfl_xor_sync(0xffffffffu, off[g], 4);
+      offs[g] = off[g].x + off[g].y;
+      offs[g] += __shfl_xor_sync(0xffffffffu, offs[g], 1);
+      offs[g] += __shfl_xor_sync(0xffffffffu, offs[g], 2);
+      offs[g] += __shfl_xor_sync(0xffffffffu, offs[g], 4);
     }
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
@@ -182,7 +194,7 @@ __global__ void __launch_bounds__(128, TAIL_CTAS_PER_SM) tail_kernel(LayerView V
     // this lane writes head tig: its offsets sit in lane 8 tig
     float offh[NG];
 #pragma unroll
-    for (int g = 0; g < NG; ++g) offh[g] = __shfl_sync(0xffffffffu, off[g], 8 * tig);
+    for (int g = 0; g < NG; ++g) offh[g] = __shfl_sync(0xffffffffu, offs[g], 8 * tig);
     // undo 2^e (weights) and 2^-24 / 2^-20 (subnormal code rows); powers of two, exact
     const float inv = ldexpf(1.f, -pre_e);
     const float inv_lo = inv * NIB_ROW_SCALE_LO, inv_hi = inv * NIB_ROW_SCALE_HI;
