@@ -48,202 +48,342 @@ __device__ __forceinline__ void vc_offset(int t, int c, int& word_byte, int& bit
 }
 
 constexpr int SROW = D + 8;   // padded shared row (272 bytes): fewer bank conflicts
+constexpr int APP_R = 4;      // blocks per CTA (value-range and scale-maximum atomics once per CTA)
 
-// One CTA per (touched block, sequence x KV head), 128 threads.  The block's FP16 tokens
-// (old partial-block tokens, then new ones) are staged in shared memory with 16-byte
-// loads (VEC; element loads when the caller's buffers are not 16-byte aligned).  A
-// completed block is quantised with each thread producing whole 16-byte key chunks and
-// whole 32-bit value words of the fragment-ordered layouts, written straight to tier 1.
+// Codes are rint(x / s) for an IEEE fp32 divide followed by rounding to the nearest
+// integer, ties to even.  They are computed through the reciprocal r = rn(1 / s):
+// q = rn(x r) is within 3 * 2^-24 |x / s| of rn(x / s), so rint(q) is the code unless q
+// lies within a margin of a half-integer -- 2^-15 for keys (|x / s| <= 127.5, error below
+// 2.3e-5), 2^-17 for values (|x / s| <= 15.5, error below 2.8e-6).  Every 32-bit code
+// word whose quotients all clear the margin keeps the fast codes; the others are formed
+// again by dividing exactly.  rint(q) itself is q + 1.5 * 2^23 - 1.5 * 2^23 (the sum's
+// unit in the last place is 1, so the addition rounds q to an integer, ties to even), and
+// the sum's bit pattern is 0x4B400000 + rint(q), which the packing uses directly.
+constexpr float RND_C = 12582912.f;            // 1.5 * 2^23
+constexpr uint32_t RND_BITS = 0x4B400000u;     // bit pattern of RND_C
+constexpr float KEY_TIE_MARGIN = 0.000030517578125f;   // 2^-15
+constexpr float VAL_TIE_MARGIN = 0.00000762939453125f; // 2^-17
+// packed = sum_e (bits_e << 8e) + KC_INIT = sum_e (code_e + 128) << 8e (mod 2^32)
+constexpr uint32_t KC_INIT = (uint32_t)(128u - RND_BITS) + ((uint32_t)(128u - RND_BITS) << 8) +
+                             ((uint32_t)(128u - RND_BITS) << 16) + ((uint32_t)(128u - RND_BITS) << 24);
+__host__ __device__ constexpr uint32_t vc_shift(int tpos, int chhalf) { return 4 * ((tpos >> 1) * 2 + chhalf) + 16 * (tpos & 1); }
+__host__ __device__ constexpr uint32_t vc_init() {
+  uint32_t w = 0u;
+  for (int tpos = 0; tpos < 4; ++tpos)
+    for (int chhalf = 0; chhalf < 2; ++chhalf) w -= RND_BITS << vc_shift(tpos, chhalf);
+  return w;
+}
+constexpr uint32_t VC_INIT = vc_init();   // word = sum (bits << shift) + VC_INIT = sum code << shift
+
+// rint(x / s) by the IEEE divide (the exact path)
+__device__ __forceinline__ int rint_div_exact(float x, float s) {
+  return s > 0.f ? (int)rintf(__fdiv_rn(x, s)) : 0;
+}
+
+// Staged values: 16-byte chunk k of row t sits at chunk k ^ ((t >> 4) & 3), so that the
+// value-code pass, whose lanes read four rows 16 apart in one instruction, hits distinct
+// banks.  Index of element (t, c) in a row.
+__device__ __forceinline__ int svi(int t, int c) { return ((((c >> 3) ^ (t >> 4)) & 3) | ((c >> 3) & ~3)) * 8 + (c & 7); }
+
+// One CTA per run of up to APP_R touched blocks of one (sequence x KV head), 128 threads.
+// Each block's FP16 tokens (old partial-block tokens, then new ones) are staged in shared
+// memory with 16-byte loads (VEC; element loads when the caller's buffers are not 16-byte
+// aligned).  Per-channel maxima and value ranges are taken in exact packed-half
+// arithmetic, two channels and half of the rows per thread.  A completed block is
+// quantised with each thread producing whole 16-byte chunks of the fragment-ordered key
+// and value layouts, written straight to tier 1; the lanes of a warp are assigned so
+// that each quarter warp's shared-memory reads fall in distinct banks or broadcast.
+// Codes come from the reciprocal, with an exact division where a quotient is near a
+// half-integer: bit-identical to dividing every element.
 template <bool VEC>
-__global__ void __launch_bounds__(128) append_kernel(AppendArgs a) {
+__global__ void __launch_bounds__(128, 5) append_kernel(AppendArgs a) {
   __shared__ __align__(16) __half sk[BLK][SROW];
-  __shared__ __align__(16) __half sv[BLK][SROW];
+  __shared__ __align__(16) __half sv[BLK][SROW];   // chunks swizzled (svi)
   __shared__ __align__(16) float kscale[D];
-  __shared__ float vsc[BLK][NG], voff[BLK][NG];
+  __shared__ __align__(16) float krcp[D];
+  __shared__ __align__(16) float4 vsm[NG][BLK];    // (scale, scale, offset, offset) per (group, token)
+  __shared__ __align__(16) float2 vrr[NG][BLK + 4];   // (rn(1 / scale), same) at t + t / 16
+  __shared__ __half2 xred[3][D / 2];   // the second row half's partial maxima / minima
   __shared__ float red[4];
-  __shared__ uint32_t smax_k, smax_v;
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int hs = blockIdx.y;
-  const int blk = a.first_blk + blockIdx.x;
-  if (!bounds_ok(a.counters, a.debug, blk, a.nbmax, SITE_APPEND) ||
-      !bounds_ok(a.counters, a.debug, hs, a.BG, SITE_APPEND))
-    return;
-  const int t0 = blk * BLK;                         // first token of the block
-  const int end = a.pos + a.n;                      // tokens after the append
-  const int t_hi = min(t0 + BLK, end);
-  const int rows = t_hi - t0;
-  const bool complete = rows == BLK;
+  const int cp = tid & 63, rh = tid >> 6;   // statistics role: channels 2cp, 2cp+1; rows 32rh..+31
+  const int cgid = lane & 7, ctig = lane >> 3;   // code role: fragment (gid, tig) of this lane
+  const int end = a.pos + a.n;              // tokens after the append
+  const int last_blk = (end - 1) / BLK;
+  if (!bounds_ok(a.counters, a.debug, hs, a.BG, SITE_APPEND)) return;
+  const __half2 hinf = __floats2half2_rn(INFINITY, INFINITY);
+  __half2 vlo = hinf, vhi = __hneg2(hinf);   // value range of the new tokens (this role)
+  uint32_t smax_k = 0u, smax_v = 0u;         // largest key / value scale bits (thread's own)
 
-  // ---- gather the block's FP16 tokens ----
-  if (VEC) {
-    uint4 kr[8], vr[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = tid + 128 * j, row = i >> 4, col = (i & 15) * 8;
-      const int t = t0 + row;
-      kr[j] = make_uint4(0, 0, 0, 0);
-      vr[j] = kr[j];
-      if (row < rows) {
-        const size_t o = (t < a.pos) ? ((size_t)hs * BLK + row) * D + col
-                                     : ((size_t)hs * a.n + (t - a.pos)) * D + col;
-        const __half* kp = (t < a.pos) ? a.tail_k_in : a.k;
-        const __half* vp = (t < a.pos) ? a.tail_v_in : a.v;
-        kr[j] = *reinterpret_cast<const uint4*>(kp + o);
-        vr[j] = *reinterpret_cast<const uint4*>(vp + o);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int i = tid + 128 * j, row = i >> 4, col = (i & 15) * 8;
-      *reinterpret_cast<uint4*>(&sk[row][col]) = kr[j];
-      *reinterpret_cast<uint4*>(&sv[row][col]) = vr[j];
-    }
-  } else {
-    for (int row = 0; row < rows; ++row) {
-      const int t = t0 + row;
-      const size_t o = (t < a.pos) ? ((size_t)hs * BLK + row) * D + tid
-                                   : ((size_t)hs * a.n + (t - a.pos)) * D + tid;
-      sk[row][tid] = (t < a.pos) ? a.tail_k_in[o] : a.k[o];
-      sv[row][tid] = (t < a.pos) ? a.tail_v_in[o] : a.v[o];
-    }
-  }
-  __syncthreads();
+  for (int rb = 0; rb < APP_R; ++rb) {
+    const int blk = a.first_blk + blockIdx.x * APP_R + rb;
+    if (blk > last_blk) break;
+    if (!bounds_ok(a.counters, a.debug, blk, a.nbmax, SITE_APPEND)) break;
+    const int t0 = blk * BLK;                         // first token of the block
+    const int rows = min(t0 + BLK, end) - t0;
+    const bool complete = rows == BLK;
+    if (rb > 0) __syncthreads();   // the previous block is done with the staging buffers
 
-  // ---- value ranges over the new tokens (thread = channel) ----
-  {
-    const int r0 = max(a.pos, t0) - t0;
-    if (r0 < rows) {
-      float lo = INFINITY, hi = -INFINITY;
-      for (int row = r0; row < rows; ++row) {
-        const float f = __half2float(sv[row][tid]);
-        lo = fminf(lo, f);
-        hi = fmaxf(hi, f);
-      }
-      atomicMin(&a.vmin[hs * D + tid], f2ord(lo));
-      atomicMax(&a.vmax[hs * D + tid], f2ord(hi));
-    }
-  }
-
-  if (!complete) {
-    // the block stays FP16: copy it (old and new tokens) to the outgoing partial buffer
-    for (int i = tid; i < rows * (D / 8); i += 128) {
-      const int row = i >> 4, col = (i & 15) * 8;
-      const size_t o = ((size_t)hs * BLK + row) * D + col;
-      *reinterpret_cast<uint4*>(a.tail_k_out + o) = *reinterpret_cast<const uint4*>(&sk[row][col]);
-      *reinterpret_cast<uint4*>(a.tail_v_out + o) = *reinterpret_cast<const uint4*>(&sv[row][col]);
-    }
-    return;
-  }
-  if (tid == 0) { smax_k = 0u; smax_v = 0u; }
-  const size_t blk_index = (size_t)hs * a.nbmax + blk;
-
-  // ---- key scales: one fp16 per channel, rounded up (thread = channel) ----
-  {
-    float amax = 0.f;
-    for (int t = 0; t < BLK; ++t) amax = fmaxf(amax, fabsf(__half2float(sk[t][tid])));
-    const __half s_h = __float2half_ru(__fdiv_rn(amax, 127.f));
-    a.ks[blk_index * D + tid] = s_h;
-    kscale[tid] = __half2float(s_h);
-    __syncthreads();   // smax_k initialised, kscale complete
-    atomicMax(&smax_k, (uint32_t)__half_as_ushort(s_h));
-  }
-  if (a.v16) {
-    // FP16-values configuration: the block's values are stored as they are; eta = 0
-    __half* dst = a.v16 + blk_index * (BLK * D);
-    for (int i = tid; i < BLK * (D / 8); i += 128) {
-      const int row = i >> 4, col = (i & 15) * 8;
-      *reinterpret_cast<uint4*>(dst + row * D + col) = *reinterpret_cast<const uint4*>(&sv[row][col]);
-    }
-  }
-  // ---- value scale/offset per (token, 32-channel group): offset = min, scale rounded up ----
-  for (int p = tid; p < BLK * NG && !a.v16; p += 128) {
-    const int t = p >> 2, g = p & 3;
-    float mn = INFINITY, mx = -INFINITY;
+    // ---- gather the block's FP16 tokens ----
+    if (VEC) {
+      // straight into shared memory (cp.async): no registers held while the loads fly
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 w = *reinterpret_cast<const uint4*>(&sv[t][g * VG + 8 * q]);
-      const __half2* h2 = reinterpret_cast<const __half2*>(&w);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 f = __half22float2(h2[e]);
-        mn = fminf(mn, fminf(f.x, f.y));
-        mx = fmaxf(mx, fmaxf(f.x, f.y));
-      }
-    }
-    const __half vs_h = __float2half_ru(__fdiv_rn(__fsub_rn(mx, mn), 15.f));
-    const __half vo_h = __float2half_rn(mn);  // exact: mn is an fp16 value
-    a.vsv[blk_index * VSV_WORDS + g * BLK + t] = __halves2half2(vs_h, vo_h);
-    vsc[t][g] = __half2float(vs_h);
-    voff[t][g] = mn;
-    atomicMax(&smax_v, (uint32_t)__half_as_ushort(vs_h));
-  }
-  __syncthreads();
-
-  // ---- key codes: 512 chunks of 16 codes (one token, 16 channels) in fragment order ----
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int q = tid + 128 * j;            // chunk index = ((w * 4 + jj) * 32 + gid * 4 + tig)
-    const int tig = q & 3, gid = (q >> 2) & 7, jj = (q >> 5) & 3, w = q >> 7;
-    const int t = w * 16 + (jj >> 1) * 8 + gid;
-    const int c0 = tig * 32 + (jj & 1) * 16;
-    uint32_t word[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint2 kh = *reinterpret_cast<const uint2*>(&sk[t][c0 + 4 * u]);
-      const float4 sc = *reinterpret_cast<const float4*>(&kscale[c0 + 4 * u]);
-      const __half2* h2 = reinterpret_cast<const __half2*>(&kh);
-      const float2 f01 = __half22float2(h2[0]), f23 = __half22float2(h2[1]);
-      const float fv[4] = {f01.x, f01.y, f23.x, f23.y}, sv4[4] = {sc.x, sc.y, sc.z, sc.w};
-      uint32_t packed = 0u;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        int code = 0;
-        if (sv4[e] > 0.f) {
-          const float r = rintf(__fdiv_rn(fv[e], sv4[e]));
-          code = (int)fminf(fmaxf(r, -127.f), 127.f);
+      for (int j = 0; j < 8; ++j) {
+        const int i = tid + 128 * j, row = i >> 4, col = (i & 15) * 8;
+        const int t = t0 + row;
+        if (row < rows) {
+          const size_t o = (t < a.pos) ? ((size_t)hs * BLK + row) * D + col
+                                       : ((size_t)hs * a.n + (t - a.pos)) * D + col;
+          const __half* kp = (t < a.pos) ? a.tail_k_in : a.k;
+          const __half* vp = (t < a.pos) ? a.tail_v_in : a.v;
+          cp_async16(&sk[row][col], kp + o);
+          cp_async16(&sv[row][svi(row, col)], vp + o);
+        } else {
+          *reinterpret_cast<uint4*>(&sk[row][col]) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(&sv[row][svi(row, col)]) = make_uint4(0, 0, 0, 0);
         }
-        packed |= ((uint32_t)(code + 128)) << (8 * e);   // offset binary: code + 128
       }
-      word[u] = packed;
+      cp_async_commit();
+      cp_async_wait<0>();
+    } else {
+      for (int row = 0; row < rows; ++row) {
+        const int t = t0 + row;
+        const size_t o = (t < a.pos) ? ((size_t)hs * BLK + row) * D + tid
+                                     : ((size_t)hs * a.n + (t - a.pos)) * D + tid;
+        sk[row][tid] = (t < a.pos) ? a.tail_k_in[o] : a.k[o];
+        sv[row][svi(row, tid)] = (t < a.pos) ? a.tail_v_in[o] : a.v[o];
+      }
     }
-    reinterpret_cast<uint4*>(a.kc + blk_index * KC_BYTES)[q] = make_uint4(word[0], word[1], word[2], word[3]);
+    __syncthreads();
+
+    // ---- value ranges over the new tokens (exact in binary16) ----
+    {
+      const int r0 = max(a.pos, t0) - t0;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {   // rows 32rh + 16hh + [0, 16): one swizzled column
+        const int rbase = 32 * rh + 16 * hh;
+        const __half* col = &sv[rbase][svi(rbase, 2 * cp)];
+        if (r0 <= rbase && rbase + 16 <= rows) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __half2 v2 = *reinterpret_cast<const __half2*>(col + i * SROW);
+            vlo = __hmin2(vlo, v2);
+            vhi = __hmax2(vhi, v2);
+          }
+        } else {
+          for (int i = max(0, r0 - rbase); i < min(16, rows - rbase); ++i) {
+            const __half2 v2 = *reinterpret_cast<const __half2*>(col + i * SROW);
+            vlo = __hmin2(vlo, v2);
+            vhi = __hmax2(vhi, v2);
+          }
+        }
+      }
+    }
+
+    if (!complete) {
+      // the block stays FP16 (it is the last one): copy its old and new tokens to the
+      // outgoing partial buffer
+      for (int i = tid; i < rows * (D / 8); i += 128) {
+        const int row = i >> 4, col = (i & 15) * 8;
+        const size_t o = ((size_t)hs * BLK + row) * D + col;
+        *reinterpret_cast<uint4*>(a.tail_k_out + o) = *reinterpret_cast<const uint4*>(&sk[row][col]);
+        *reinterpret_cast<uint4*>(a.tail_v_out + o) = *reinterpret_cast<const uint4*>(&sv[row][svi(row, col)]);
+      }
+      break;
+    }
+    const size_t blk_index = (size_t)hs * a.nbmax + blk;
+
+    // ---- key scales: one fp16 per channel, rounded up; their reciprocals ----
+    {
+      __half2 m2 = __float2half2_rn(0.f);
+#pragma unroll 8
+      for (int row = 32 * rh; row < 32 * rh + 32; ++row)
+        m2 = __hmax2(m2, __habs2(*reinterpret_cast<const __half2*>(&sk[row][2 * cp])));
+      xred[rh][cp] = m2;
+      __syncthreads();
+      // thread = channel: the larger of the two row halves' maxima
+      const __half2 p0 = xred[0][tid >> 1], p1 = xred[1][tid >> 1];
+      const float amax = (tid & 1) ? fmaxf(__high2float(p0), __high2float(p1)) : fmaxf(__low2float(p0), __low2float(p1));
+      const __half s_h = __float2half_ru(__fdiv_rn(amax, 127.f));
+      a.ks[blk_index * D + tid] = s_h;
+      const float f = __half2float(s_h);
+      kscale[tid] = f;
+      krcp[tid] = f > 0.f ? __frcp_rn(f) : 0.f;
+      smax_k = max(smax_k, (uint32_t)__half_as_ushort(s_h));
+    }
+    if (a.v16) {
+      // FP16-values configuration: the block's values are stored as they are; eta = 0
+      __half* dst = a.v16 + blk_index * (BLK * D);
+      for (int i = tid; i < BLK * (D / 8); i += 128) {
+        const int row = i >> 4, col = (i & 15) * 8;
+        *reinterpret_cast<uint4*>(dst + row * D + col) = *reinterpret_cast<const uint4*>(&sv[row][svi(row, col)]);
+      }
+    } else {
+      // ---- value scale/offset per (token, 32-channel group): offset = min, scale rounded up ----
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        const int p = tid + 128 * pp, t = p & 63, g = p >> 6;
+        __half2 mn2 = hinf, mx2 = __hneg2(hinf);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 w = *reinterpret_cast<const uint4*>(&sv[t][svi(t, g * VG + 8 * q)]);
+          const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            mn2 = __hmin2(mn2, u32_as_h2(ww[e]));
+            mx2 = __hmax2(mx2, u32_as_h2(ww[e]));
+          }
+        }
+        const float mn = fminf(__low2float(mn2), __high2float(mn2));
+        const float mx = fmaxf(__low2float(mx2), __high2float(mx2));
+        const __half vs_h = __float2half_ru(__fdiv_rn(__fsub_rn(mx, mn), 15.f));
+        const __half vo_h = __float2half_rn(mn);  // exact: mn is an fp16 value
+        a.vsv[blk_index * VSV_WORDS + g * BLK + t] = __halves2half2(vs_h, vo_h);
+        const float vs = __half2float(vs_h);
+        vsm[g][t] = make_float4(vs, vs, mn, mn);
+        const float vr = vs > 0.f ? __frcp_rn(vs) : 0.f;
+        vrr[g][t + (t >> 4)] = make_float2(vr, vr);
+        smax_v = max(smax_v, (uint32_t)__half_as_ushort(vs_h));
+      }
+    }
+    __syncthreads();
+
+    // ---- key codes: 512 chunks of 16 codes (one token, 16 channels) in fragment order ----
+    // chunk ((w * 4 + jj) * 32 + gid * 4 + tig): w = j, jj = warp; a quarter warp shares tig
+    {
+      const float2 C2 = make_float2(RND_C, RND_C);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int q = (j * 4 + warp) * 32 + cgid * 4 + ctig;
+        const int t = j * 16 + (warp >> 1) * 8 + cgid;
+        const int c0 = ctig * 32 + (warp & 1) * 16;
+        uint32_t word[4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint4 kh = *reinterpret_cast<const uint4*>(&sk[t][c0 + 8 * h]);
+          const uint32_t kw[4] = {kh.x, kh.y, kh.z, kh.w};
+#pragma unroll
+          for (int uu = 0; uu < 2; ++uu) {
+            const int u = 2 * h + uu, cc = c0 + 4 * u;
+            const float4 rc = *reinterpret_cast<const float4*>(&krcp[cc]);
+            // |code| <= 127 without clamping: s >= rn(amax / 127) makes |K / s| < 127.5
+            uint32_t packed = KC_INIT;
+            float dmax = 0.f;
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+              const float2 x = __half22float2(u32_as_h2(kw[2 * uu + pr]));
+              const float2 qq = mul2(x, pr ? make_float2(rc.z, rc.w) : make_float2(rc.x, rc.y));
+              const float2 tt = add2(qq, C2);
+              const float2 d = sub2(qq, sub2(tt, C2));
+              dmax = fmaxf(dmax, fmaxf(fabsf(d.x), fabsf(d.y)));
+              packed += __float_as_uint(tt.x) << (16 * pr);
+              packed += __float_as_uint(tt.y) << (16 * pr + 8);
+            }
+            if (dmax > 0.5f - KEY_TIE_MARGIN) {   // a quotient near a half-integer: divide
+              packed = 0u;
+#pragma unroll 1
+              for (int e = 0; e < 4; ++e) {
+                const uint32_t kwe = (e >> 1) ? kw[2 * uu + 1] : kw[2 * uu];
+                const float xe = __half2float(__ushort_as_half((unsigned short)(kwe >> (16 * (e & 1)))));
+                packed |= (uint32_t)(rint_div_exact(xe, kscale[cc + e]) + 128) << (8 * e);
+              }
+            }
+            word[u] = packed;
+          }
+        }
+        reinterpret_cast<uint4*>(a.kc + blk_index * KC_BYTES)[q] = make_uint4(word[0], word[1], word[2], word[3]);
+      }
+    }
+
+    // ---- value codes: 256 chunks of 4 words of 8 nibbles (4 tokens x 2 channels) ----
+    // chunk ((g * 2 + mt) * 32 + gid * 4 + tig), word kk: g = warp; a quarter warp shares tig
+    float errmax = 0.f;
+    if (!a.v16) {
+      const int g = warp;
+      const float2 C2 = make_float2(RND_C, RND_C);
+#pragma unroll 1
+      for (int mt = 0; mt < 2; ++mt) {
+        const int cb = g * VG + mt * 16 + cgid;
+        // this lane's tokens are 16 ctig + [0, 16): one swizzle for all of them
+        const __half* colA = &sv[ctig * 16][svi(ctig * 16, cb)];
+        const __half* colB = &sv[ctig * 16][svi(ctig * 16, cb + 8)];
+        const float4* inf = &vsm[g][ctig * 16];
+        const float2* rcp = &vrr[g][ctig * 17];   // padded: the two 16-token groups of a half warp use distinct banks
+        uint32_t word[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t wv = VC_INIT;
+          float dmax = 0.f, werr = 0.f;   // the word's largest |q - rint(q)| and |v - v_hat|
+#pragma unroll
+          for (int tpos = 0; tpos < 4; ++tpos) {
+            const int i = kk * 4 + tpos;
+            const float4 so = inf[i];     // (scale, scale, offset, offset)
+            const float2 r2 = rcp[i];
+            const float2 f = make_float2(__half2float(colA[i * SROW]), __half2float(colB[i * SROW]));
+            // 0 <= (v - o) / s < 15.5 (s rounded up from (max - min) / 15): no clamping
+            const float2 qq = mul2(sub2(f, make_float2(so.z, so.w)), r2);
+            const float2 tt = add2(qq, C2);
+            const float2 k = sub2(tt, C2);
+            const float2 d = sub2(qq, k);
+            dmax = fmaxf(dmax, fmaxf(fabsf(d.x), fabsf(d.y)));
+            const float2 vhat = add2(mul2(make_float2(so.x, so.y), k), make_float2(so.z, so.w));
+            const float2 err = sub2(f, vhat);
+            werr = fmaxf(werr, fmaxf(fabsf(err.x), fabsf(err.y)));
+            wv += __float_as_uint(tt.x) << vc_shift(tpos, 0);
+            wv += __float_as_uint(tt.y) << vc_shift(tpos, 1);
+          }
+          if (dmax > 0.5f - VAL_TIE_MARGIN) {   // a quotient near a half-integer: divide
+            wv = 0u;
+            werr = 0.f;
+#pragma unroll 1
+            for (int e = 0; e < 8; ++e) {
+              const int i = kk * 4 + (e >> 1);
+              const float4 so = inf[i];
+              const float fv = __half2float((e & 1) ? colB[i * SROW] : colA[i * SROW]);
+              const int code = rint_div_exact(__fsub_rn(fv, so.z), so.x);
+              const float vhat = __fadd_rn(__fmul_rn(so.x, (float)code), so.z);
+              werr = fmaxf(werr, fabsf(__fsub_rn(fv, vhat)));
+              wv |= (uint32_t)code << vc_shift(e >> 1, e & 1);
+            }
+          }
+          errmax = fmaxf(errmax, werr);
+          word[kk] = wv;
+        }
+        reinterpret_cast<uint4*>(a.vc + blk_index * VC_BYTES)[(g * 2 + mt) * 32 + cgid * 4 + ctig] =
+            make_uint4(word[0], word[1], word[2], word[3]);
+      }
+    }
+    errmax = warp_max(errmax);
+    if (lane == 0) red[warp] = errmax;
+    __syncthreads();
+    if (tid == 0) a.eta[blk_index] = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   }
 
-  // ---- value codes: 1024 words of 8 nibbles (4 tokens x 2 channels) in fragment order ----
-  float errmax = 0.f;
-#pragma unroll 2
-  for (int j = 0; j < 8 && !a.v16; ++j) {
-    const int wi = tid + 128 * j;           // word = ((g * 2 + mt) * 32 + gid * 4 + tig) * 4 + kk
-    const int kk = wi & 3, tig = (wi >> 2) & 3, gid = (wi >> 4) & 7, mt = (wi >> 7) & 1, g = wi >> 8;
-    const int cb = g * VG + mt * 16 + gid;
-    uint32_t word = 0u;
-#pragma unroll
-    for (int tpos = 0; tpos < 4; ++tpos) {
-      const int t = tig * 16 + kk * 4 + tpos;
-      const float vs = vsc[t][g], mn = voff[t][g];
-#pragma unroll
-      for (int chhalf = 0; chhalf < 2; ++chhalf) {
-        const float f = __half2float(sv[t][cb + 8 * chhalf]);
-        int code = 0;
-        if (vs > 0.f) {
-          const float r = rintf(__fdiv_rn(__fsub_rn(f, mn), vs));
-          code = (int)fminf(fmaxf(r, 0.f), 15.f);
-        }
-        const float vhat = __fadd_rn(__fmul_rn(vs, (float)code), mn);
-        errmax = fmaxf(errmax, fabsf(__fsub_rn(f, vhat)));
-        word |= ((uint32_t)code) << (4 * ((tpos >> 1) * 2 + chhalf) + 16 * (tpos & 1));
-      }
-    }
-    reinterpret_cast<uint32_t*>(a.vc + blk_index * VC_BYTES)[wi] = word;
-  }
-  errmax = warp_max(errmax);
-  if ((tid & 31) == 0) red[tid >> 5] = errmax;
+  // ---- value ranges and scale maxima of the CTA's blocks: one atomic per channel ----
   __syncthreads();
-  if (tid == 0) {
-    a.eta[blk_index] = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    atomicMax(&a.kscale_max[hs], smax_k);
-    atomicMax(&a.vscale_max[hs], smax_v);
+  if (rh == 1) {
+    xred[1][cp] = vlo;
+    xred[2][cp] = vhi;
+  }
+  __syncthreads();
+  if (rh == 0) {
+    vlo = __hmin2(vlo, xred[1][cp]);
+    vhi = __hmax2(vhi, xred[2][cp]);
+    const float2 l2 = __half22float2(vlo), h2 = __half22float2(vhi);
+    if (l2.x <= h2.x) {   // the channel pair saw new tokens
+      atomicMin(&a.vmin[hs * D + 2 * cp], f2ord(l2.x));
+      atomicMin(&a.vmin[hs * D + 2 * cp + 1], f2ord(l2.y));
+      atomicMax(&a.vmax[hs * D + 2 * cp], f2ord(h2.x));
+      atomicMax(&a.vmax[hs * D + 2 * cp + 1], f2ord(h2.y));
+    }
+  }
+  smax_k = __reduce_max_sync(0xffffffffu, smax_k);
+  smax_v = __reduce_max_sync(0xffffffffu, smax_v);
+  if (lane == 0) {
+    if (smax_k) atomicMax(&a.kscale_max[hs], smax_k);
+    if (smax_v) atomicMax(&a.vscale_max[hs], smax_v);
   }
 }
 
@@ -305,7 +445,7 @@ cudaError_t launch_append(const LayerAppend& L, const void* k, const void* v, in
   a.v16 = L.v16;
   a.counters = L.counters; a.debug = L.debug; a.BG = L.BG;
   const int last_blk = (pos + n - 1) / BLK;
-  dim3 grid(last_blk - a.first_blk + 1, L.BG);
+  dim3 grid((last_blk - a.first_blk + APP_R) / APP_R, L.BG);
   const bool aligned = ((reinterpret_cast<uintptr_t>(k) | reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
   if (aligned) append_kernel<true><<<grid, 128, 0, st>>>(a);
   else append_kernel<false><<<grid, 128, 0, st>>>(a);

@@ -319,6 +319,10 @@ __device__ __forceinline__ void cp_async16_hint(void* dst_smem, const void* src,
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
                :: "r"(d), "l"(src), "l"(pol) : "memory");
 }
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  const unsigned d = (unsigned)__cvta_generic_to_shared(dst_smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(d), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
