@@ -1,4 +1,4 @@
-// kvq_blocksel.cuh -- block-wide (256-thread) reductions and the "top blocks covering a
+// kvq_blocksel.cuh -- block-wide (BS_THREADS-thread) reductions and the "top blocks covering a
 // target" selection used by the top-K* pass and by rungs 1-2 of the ladder.
 //
 // Selection rule ("Runtime-Certified Bounded-Error Quantized Attention", gist.science
@@ -9,8 +9,8 @@
 // the choice does not depend on summation order.
 //
 // Method: the threshold key is found 10 bits per level (keys of values <= 1 are below
-// 2^30): each warp accumulates its keys' weights into a private 1024-bucket histogram,
-// the warps' histograms are summed, a block scan finds the bucket where the running
+// 2^30): each group of warps accumulates its keys' weights into a private 1024-bucket
+// histogram, the groups' histograms are summed, a block scan finds the bucket where the running
 // weight from the top reaches the target, and once that bucket holds at most SEL_CAND
 // keys they are ranked exactly.
 #pragma once
@@ -19,9 +19,12 @@
 
 namespace kvq {
 
-constexpr int BS_THREADS = 256;
+constexpr int BS_THREADS = 512;                   // per (sequence, head): latency-bound work
 constexpr int BS_WARPS = BS_THREADS / 32;
+constexpr int BS_NHIST = 8;                        // private histograms, BS_WARPS / BS_NHIST warps each
+constexpr int BS_BPT = 1024 / BS_THREADS;          // histogram buckets per thread in the scan
 static_assert(SEL_CAND <= BS_THREADS, "one thread per exactly ranked candidate");
+static_assert(BS_WARPS % BS_NHIST == 0 && 1024 % BS_THREADS == 0, "block shape");
 
 struct BlockRed {
   float f[BS_WARPS];
@@ -110,7 +113,7 @@ __device__ __forceinline__ void hist_add(unsigned long long* bucket, unsigned lo
 
 // Shared-memory workspace of block_select_top (dynamic shared memory).
 struct BlockSelSmem {
-  unsigned long long hist[BS_WARPS][1024];   // per-warp private histograms
+  unsigned long long hist[BS_NHIST][1024];   // private histograms of groups of warps
   alignas(16) int cidx[SEL_CAND];
   alignas(16) uint32_t ckey[SEL_CAND];
   int order[SEL_CAND];
@@ -155,31 +158,32 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
   }
   for (; level >= 0 && level < 3; ++level) {
     const int sh = 20 - 10 * level;
-    for (int d = lane; d < 1024; d += 32) ws.hist[warp][d] = 0ull;
-    __syncwarp();
+    const int hg = warp / (BS_WARPS / BS_NHIST);
+    for (int d = tid; d < BS_NHIST * 1024; d += BS_THREADS) (&ws.hist[0][0])[d] = 0ull;
+    __syncthreads();
     for (int i = i0; i < i1; ++i) {
       const uint32_t k = keys[i];
       if (k != 0u && (level == 0 || (k >> (sh + 10)) == prefix))
-        hist_add(&ws.hist[warp][(k >> sh) & 1023u], key_weight(k));
+        hist_add(&ws.hist[hg][(k >> sh) & 1023u], key_weight(k));
     }
     __syncthreads();
-    // thread t owns buckets 1023-4t .. 1020-4t (descending)
-    unsigned long long bw[4], run = 0;
+    // thread t owns buckets 1023 - BS_BPT t - j, j < BS_BPT (descending)
+    unsigned long long bw[BS_BPT], run = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int bk = 1023 - 4 * tid - j;
+    for (int j = 0; j < BS_BPT; ++j) {
+      const int bk = 1023 - BS_BPT * tid - j;
       unsigned long long s = 0;
 #pragma unroll
-      for (int w = 0; w < BS_WARPS; ++w) s += ws.hist[w][bk];
+      for (int w = 0; w < BS_NHIST; ++w) s += ws.hist[w][bk];
       bw[j] = s;
       run += s;
     }
     unsigned long long total;
     unsigned long long c = above + block_excl_scan_u64(run, ws.red, &total);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < BS_BPT; ++j) {
       if (c < target && c + bw[j] >= target) {
-        ws.prefix = (prefix << 10) | (uint32_t)(1023 - 4 * tid - j);
+        ws.prefix = (prefix << 10) | (uint32_t)(1023 - BS_BPT * tid - j);
         ws.above = c;
       }
       c += bw[j];
@@ -254,7 +258,7 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
     }
     if (tid == 0) { ws.last = nc - 1; ws.take_w = 0ull; }
     __syncthreads();
-    // running weight in rank order; thread r handles rank r (nc <= SEL_CAND <= 256)
+    // running weight in rank order; thread r handles rank r (nc <= SEL_CAND <= BS_THREADS)
     const unsigned long long w = (tid < nc) ? key_weight(ws.ckey[ws.order[tid]]) : 0ull;
     unsigned long long tot_c;
     const unsigned long long excl = block_excl_scan_u64(w, ws.red, &tot_c);

@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
   }
 }
 
-// One CTA of 256 threads per (sequence, query head): combine the chunk partials of a
+// One CTA of BS_THREADS threads per (sequence, query head): combine the chunk partials of a
 // pass for the head, add the partial block, write the output and the certificate and,
 // after the first pass, run the ranking check and plan rungs 1-2.
 __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int round) {

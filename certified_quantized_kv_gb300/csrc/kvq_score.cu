@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
   cp_async_wait<0>();
 }
 
-// One CTA of 256 threads per (sequence, query head): the top-K* selection.  The last
+// One CTA of BS_THREADS threads per (sequence, query head): the top-K* selection.  The last
 // head of each KV group to finish forms the group's union of selected blocks.
 __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
   pdl_trigger();
