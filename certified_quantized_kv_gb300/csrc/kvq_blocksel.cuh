@@ -8,11 +8,15 @@
 // weighted in fixed point, w_i = floor(v_i 2^62), so every sum is an exact integer and
 // the choice does not depend on summation order.
 //
-// Method: the threshold key is found 10 bits per level (keys of values <= 1 are below
-// 2^30): each group of warps accumulates its keys' weights into a private 1024-bucket
-// histogram, the groups' histograms are summed, a block scan finds the bucket where the running
-// weight from the top reaches the target, and once that bucket holds at most SEL_CAND
-// keys they are ranked exactly.
+// Method: one block reduction gives the total weight, the number of candidates and the
+// smallest and largest candidate key.  The threshold key is then narrowed by histogram
+// levels over the current key range [lo, hi], cut linearly into 1024 buckets (keys are
+// order-preserving fp32 bits, so this is a logarithmic cut of the values): each group of
+// warps accumulates its keys' weights into a private histogram, the groups' histograms
+// are summed, a block scan finds the bucket where the running weight from the top
+// reaches the target, and that bucket's key range becomes the next [lo, hi].  Once it
+// holds at most SEL_CAND keys they are ranked exactly (one key value left: ties go to
+// the lower indices).  Near-uniform values usually need a single level.
 #pragma once
 
 #include "kvq_common.cuh"
@@ -28,9 +32,51 @@ static_assert(BS_WARPS % BS_NHIST == 0 && 1024 % BS_THREADS == 0, "block shape")
 
 struct BlockRed {
   float f[BS_WARPS];
+  float f1[BS_WARPS], f2[BS_WARPS], f3[BS_WARPS];
   unsigned long long u[BS_WARPS];
   int i[BS_WARPS];
 };
+
+// Several block reductions in one round of barriers: maxima of a and b (block_max2), or
+// the maximum of m and the sums of x, y, z (block_max_sum3).
+__device__ __forceinline__ void block_max2(float& a, float& b, BlockRed& r) {
+  a = warp_max(a);
+  b = warp_max(b);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) { r.f[threadIdx.x >> 5] = a; r.f1[threadIdx.x >> 5] = b; }
+  __syncthreads();
+  a = -INFINITY;
+  b = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < BS_WARPS; ++w) { a = fmaxf(a, r.f[w]); b = fmaxf(b, r.f1[w]); }
+}
+__device__ __forceinline__ void block_sum2(float& a, float& b, BlockRed& r) {
+  a = warp_sum(a);
+  b = warp_sum(b);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) { r.f[threadIdx.x >> 5] = a; r.f1[threadIdx.x >> 5] = b; }
+  __syncthreads();
+  a = 0.f;
+  b = 0.f;
+#pragma unroll
+  for (int w = 0; w < BS_WARPS; ++w) { a += r.f[w]; b += r.f1[w]; }
+}
+__device__ __forceinline__ void block_max_sum3(float& m, float& x, float& y, float& z, BlockRed& r) {
+  m = warp_max(m);
+  x = warp_sum(x);
+  y = warp_sum(y);
+  z = warp_sum(z);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) {
+    const int w = threadIdx.x >> 5;
+    r.f[w] = m; r.f1[w] = x; r.f2[w] = y; r.f3[w] = z;
+  }
+  __syncthreads();
+  m = -INFINITY;
+  x = y = z = 0.f;
+#pragma unroll
+  for (int w = 0; w < BS_WARPS; ++w) { m = fmaxf(m, r.f[w]); x += r.f1[w]; y += r.f2[w]; z += r.f3[w]; }
+}
 
 __device__ __forceinline__ float block_sum(float v, BlockRed& r) {
   v = warp_sum(v);
@@ -123,6 +169,7 @@ struct BlockSelSmem {
   int last;
   unsigned long long take_w;
   BlockRed red;
+  uint32_t kmin[BS_WARPS], kmax[BS_WARPS];
 };
 
 // keys: n keys in shared memory (thread t owns the contiguous range [t*kpt, t*kpt+kpt)).
@@ -133,38 +180,61 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int kpt = (n + BS_THREADS - 1) / BS_THREADS;
   const int i0 = tid * kpt, i1 = min(n, i0 + kpt);
+  // total weight, candidates (nonzero keys) and their key range in one reduction
   unsigned long long mytot = 0;
-  for (int i = i0; i < i1; ++i) mytot += key_weight(keys[i]);
-  const unsigned long long tot = block_sum_u64(mytot, ws.red);
+  int mynz = 0;
+  uint32_t kmn = 0xffffffffu, kmx = 0u;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t k = keys[i];
+    if (k != 0u) {
+      mytot += key_weight(k);
+      ++mynz;
+      kmn = min(kmn, k);
+      kmx = max(kmx, k);
+    }
+  }
+  mytot = warp_sum_u64(mytot);
+  mynz = (int)__reduce_add_sync(0xffffffffu, (unsigned)mynz);
+  kmn = __reduce_min_sync(0xffffffffu, kmn);
+  kmx = __reduce_max_sync(0xffffffffu, kmx);
+  __syncthreads();
+  if (lane == 0) {
+    ws.red.u[warp] = mytot;
+    ws.red.i[warp] = mynz;
+    ws.kmin[warp] = kmn;
+    ws.kmax[warp] = kmx;
+  }
+  __syncthreads();
+  unsigned long long tot = 0;
+  int nnz = 0;
+  uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+  for (int w = 0; w < BS_WARPS; ++w) {
+    tot += ws.red.u[w];
+    nnz += ws.red.i[w];
+    lo = min(lo, ws.kmin[w]);
+    hi = max(hi, ws.kmax[w]);
+  }
   *taken = 0ull;
   if (target == 0ull) return 0;
   if (tot < target) {  // out of reach: take every candidate
-    int cnt = 0;
     for (int i = i0; i < i1; ++i)
-      if (keys[i] != 0u) { mark(i); ++cnt; }
+      if (keys[i] != 0u) mark(i);
     *taken = tot;
-    return block_sum_int(cnt, ws.red);
+    return nnz;
   }
-  uint32_t prefix = 0;
+  // candidates are the keys in [lo, hi]; `above` = weight of the keys above hi
   unsigned long long above = 0;
-  int level = 0, ncand = 0;
-  if (n <= SEL_CAND) {
-    // every key fits the exact ranking: no histogram level (keys are below 2^30, so
-    // with the 30-bit shift below, prefix 0 makes every nonzero key a candidate)
-    level = -1;
-    int cnt = 0;
-    for (int i = i0; i < i1; ++i) cnt += keys[i] != 0u;
-    ncand = block_sum_int(cnt, ws.red);
-  }
-  for (; level >= 0 && level < 3; ++level) {
-    const int sh = 20 - 10 * level;
+  int ncand = nnz;
+  for (int level = 0; ncand > SEL_CAND && hi > lo && level < 4; ++level) {
+    const unsigned long long span = (unsigned long long)(hi - lo) + 1ull;
     const int hg = warp / (BS_WARPS / BS_NHIST);
     for (int d = tid; d < BS_NHIST * 1024; d += BS_THREADS) (&ws.hist[0][0])[d] = 0ull;
     __syncthreads();
     for (int i = i0; i < i1; ++i) {
       const uint32_t k = keys[i];
-      if (k != 0u && (level == 0 || (k >> (sh + 10)) == prefix))
-        hist_add(&ws.hist[hg][(k >> sh) & 1023u], key_weight(k));
+      if (k != 0u && k >= lo && k <= hi)
+        hist_add(&ws.hist[hg][(uint32_t)(((unsigned long long)(k - lo) * 1024ull) / span)], key_weight(k));
     }
     __syncthreads();
     // thread t owns buckets 1023 - BS_BPT t - j, j < BS_BPT (descending)
@@ -172,50 +242,54 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
 #pragma unroll
     for (int j = 0; j < BS_BPT; ++j) {
       const int bk = 1023 - BS_BPT * tid - j;
-      unsigned long long s = 0;
+      unsigned long long sum = 0;
 #pragma unroll
-      for (int w = 0; w < BS_NHIST; ++w) s += ws.hist[w][bk];
-      bw[j] = s;
-      run += s;
+      for (int w = 0; w < BS_NHIST; ++w) sum += ws.hist[w][bk];
+      bw[j] = sum;
+      run += sum;
     }
     unsigned long long total;
     unsigned long long c = above + block_excl_scan_u64(run, ws.red, &total);
 #pragma unroll
     for (int j = 0; j < BS_BPT; ++j) {
       if (c < target && c + bw[j] >= target) {
-        ws.prefix = (prefix << 10) | (uint32_t)(1023 - BS_BPT * tid - j);
+        ws.prefix = (uint32_t)(1023 - BS_BPT * tid - j);
         ws.above = c;
       }
       c += bw[j];
     }
     __syncthreads();
-    prefix = ws.prefix;
+    // the crossing bucket b holds the keys lo + ceil(b span / 1024) .. lo + ceil((b + 1) span / 1024) - 1
+    const unsigned long long b = ws.prefix;
     above = ws.above;
+    const uint32_t nlo = lo + (uint32_t)((b * span + 1023ull) / 1024ull);
+    const uint32_t nhi = lo + (uint32_t)(((b + 1ull) * span + 1023ull) / 1024ull) - 1u;
+    lo = nlo;
+    hi = nhi;
     int cnt = 0;
     for (int i = i0; i < i1; ++i) {
       const uint32_t k = keys[i];
-      cnt += (k != 0u && (k >> sh) == prefix);
+      cnt += (k != 0u && k >= lo && k <= hi);
     }
     ncand = block_sum_int(cnt, ws.red);
-    if (ncand <= SEL_CAND || level == 2) break;
   }
-  const int sh = 20 - 10 * level;
   const unsigned long long rem = target - above;
   int cnt = 0;
   unsigned long long take_w = 0;
   if (ncand > SEL_CAND) {
-    // level 2 reached with one key value left: ties, lowest indices first
-    const unsigned long long wt = key_weight(prefix);
+    // one key value left (lo == hi) with more keys than the exact ranking takes: ties,
+    // lowest indices first
+    const unsigned long long wt = key_weight(lo);
     const unsigned long long need = wt ? (rem + wt - 1) / wt : 0ull;
     int mine = 0;
-    for (int i = i0; i < i1; ++i) mine += (keys[i] != 0u && keys[i] == prefix);
+    for (int i = i0; i < i1; ++i) mine += (keys[i] != 0u && keys[i] == lo);
     unsigned long long ties;
     unsigned long long rank = block_excl_scan_u64((unsigned long long)mine, ws.red, &ties);
     for (int i = i0; i < i1; ++i) {
       const uint32_t k = keys[i];
       if (k == 0u) continue;
-      if (k > prefix) { mark(i); ++cnt; }
-      else if (k == prefix) {
+      if (k > lo) { mark(i); ++cnt; }
+      else if (k == lo) {
         if (rank < need) { mark(i); ++cnt; }
         ++rank;
       }
@@ -227,8 +301,8 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
     for (int i = i0; i < i1; ++i) {
       const uint32_t k = keys[i];
       if (k == 0u) continue;
-      if ((k >> sh) > prefix) { mark(i); ++cnt; }
-      else if ((k >> sh) == prefix) {
+      if (k > hi) { mark(i); ++cnt; }
+      else if (k >= lo) {
         const int slot = atomicAdd(&ws.ncand, 1);
         ws.cidx[slot] = i;
         ws.ckey[slot] = k;
@@ -240,7 +314,7 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
     if (tid >= nc && tid < nc4) ws.ckey[tid] = 0u;   // padding ranks below every candidate
     __syncthreads();
     // rank of candidate a = number of candidates before it (key descending, index
-    // ascending); nc <= SEL_CAND = BS_THREADS, four candidates per 16-byte load
+    // ascending); nc <= SEL_CAND <= BS_THREADS, four candidates per 16-byte load
     if (tid < nc) {
       const uint32_t ka = ws.ckey[tid];
       const int ia = ws.cidx[tid];

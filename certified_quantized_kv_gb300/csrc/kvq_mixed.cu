@@ -489,8 +489,8 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
       a += tail_p[t] * __half2float(V.tail_v[((size_t)hs * BLK + t) * D + tid]);
     V.out[hb * D + tid] = __float2half_rn(a / L);
   }
-  // value range R = max_c (vmax_c - vmin_c)
-  const float R = block_max(tid < D ? ord2f(V.vmax[hs * D + tid]) - ord2f(V.vmin[hs * D + tid]) : -INFINITY, ws.red);
+  // value range R = max_c (vmax_c - vmin_c), reduced together with the certificate sums
+  float R = tid < D ? ord2f(V.vmax[hs * D + tid]) - ord2f(V.vmin[hs * D + tid]) : -INFINITY;
   // (3) certificate
   const float LSEp = hsd.M + logf(L);
   const float tail_mass = lt / L;
@@ -524,9 +524,8 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
       if (!vf[j]) Ev += pm * ee[j];
     }
   }
-  S = block_sum(S, ws.red);
-  A = block_sum(A, ws.red) + tail_mass;
-  Ev = block_sum(Ev, ws.red);
+  block_max_sum3(R, S, A, Ev, ws.red);
+  A += tail_mass;
   const float e_key = S / A * R;
   const float e_val = Ev;
   hsd.e_key = e_key;

@@ -274,9 +274,6 @@ __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
     tail_s[tid] = sc;
     tmax = sc;
   }
-  tmax = block_max(tmax, ws.red);
-  const float tl = block_sum(tid < V.n_tail ? expf(tail_s[tid] - tmax) : 0.f, ws.red);
-  const float tail_lse = V.n_tail > 0 ? tmax + logf(tl) : -INFINITY;
   // block log-masses: staged in shared memory (16-byte loads; rows padded to 16 blocks)
   const float* lse8 = V.lse8 + hb * V.nbmax;
   float m = -INFINITY;
@@ -288,17 +285,20 @@ __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
       if (4 * i4 + j < nb) m = fmaxf(m, xv[j]);
     reinterpret_cast<float4*>(xs)[i4] = x;
   }
-  m = block_max(m, ws.red);
+  block_max2(m, tmax, ws.red);   // also makes tail_s and xs visible
+  float sp = 0.f;
+  for (int i = tid; i < nb; i += BS_THREADS) sp += expf(xs[i] - m);
+  float tl = tid < V.n_tail ? expf(tail_s[tid] - tmax) : 0.f;
+  block_sum2(sp, tl, ws.red);
+  const float tail_lse = V.n_tail > 0 ? tmax + logf(tl) : -INFINITY;
   // softmax reference of the passes that follow: >= every INT8 score (a block's log-mass
   // bounds its scores) and every partial-block score; a pass that meets a larger FP16
   // score raises its own reference
   const float mref = fmaxf(m, tmax);
-  m = fmaxf(m, tail_lse);
-  float sp = 0.f;
-  for (int i = tid; i < nb; i += BS_THREADS) sp += expf(xs[i] - m);
-  float s = block_sum(sp, ws.red);
-  if (V.n_tail > 0) s += expf(tail_lse - m);
-  const float LSE = m + logf(s);
+  // log-sum-exp over the blocks (sum sp relative to m) and the partial block
+  const float mm = fmaxf(m, tail_lse);
+  float s = (nb > 0 ? sp * expf(m - mm) : 0.f) + (V.n_tail > 0 ? expf(tail_lse - mm) : 0.f);
+  const float LSE = mm + logf(s);
   const double tail_mass = (V.n_tail > 0) ? (double)expf(tail_lse - LSE) : 0.0;
   const double need = (double)V.tau - tail_mass;
   unsigned long long target = 0ull;
