@@ -429,7 +429,10 @@ def measure_append(torch, kvq, W, wl, hbm_peak, reps=2):
             "mirror_frac_of_d2h": units * F16_BYTES_PER_TOKEN_HEAD / (best_ms / 1e3) / 1e9 / d2h,
             "quantize_kernel_us": kern_us,
             "quantize_kernel_hbm": {"bytes": hbm_bytes, "achieved_gbs": hbm_bytes / (kern_us * 1e-6) / 1e9,
-                                    "peak": hbm_peak, "frac": hbm_bytes / (kern_us * 1e-6) / 1e9 / hbm_peak}}
+                                    "peak": hbm_peak, "frac": hbm_bytes / (kern_us * 1e-6) / 1e9 / hbm_peak,
+                                    "traffic": _ncu_traffic().get("quantize_append", {}).get("dram_bytes"),
+                                    "timing": "CUDA events around the kernel inside the append call, while the "
+                                              "tier-2 mirror copy runs beside it"}}
 
 
 def measure_fp16_values(args, wl):
@@ -595,7 +598,8 @@ def measure_dense_hbm(args, wl, t_cert_layer_us, t_unc_layer_us):
     return {"value": B / (ms / 1e3), "unit": UNIT, "us_per_layer": us,
             "roofline": {"bound": "hbm", "kernel": "dense_hbm (split pass + combine)", "achieved": b / (us * 1e-6) / 1e9,
                          "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": b / (us * 1e-6) / 1e9 / hbm_peak, "algorithmic_bytes_per_launch": b},
+                         "frac": b / (us * 1e-6) / 1e9 / hbm_peak, "algorithmic_bytes_per_launch": b,
+                         "traffic": _ncu_traffic().get("dense_hbm", {}).get("dram_bytes")},
             "certified_over_dense": t_cert_layer_us / us,
             "uncertified_over_dense": t_unc_layer_us / us,
             "pages_certified_over_dense": "2.7-4.8x (Results, performance overhead; hardware unstated)",
@@ -1086,6 +1090,40 @@ def sweep_vtol(args):
         cache.close()
 
 
+def profile_layer(args):
+    """A small fixed launch sequence for ncu captures (not a bench line): one 128K-token
+    layer of the headline caches, quantised twice (two caches), then three certified,
+    three uncertified and three dense-FP16-in-HBM decode calls on it.  Launch order:
+    append_kernel x2; (score, select, mixed_kernel_r0, combine, mixed_kernel, combine,
+    dense_kernel, finalize) x3; (score, select, tail_kernel, combine, finalize) x3;
+    (dense_hbm_kernel, dense_hbm_combine_kernel) x3."""
+    import torch
+    import certified_quantized_kv_gb300 as kvq
+    import workloads as W
+    wl = WORKLOAD
+    B, N, Hq, Hkv, D = wl["batch"], wl["ctx"], wl["q_heads"], wl["kv_heads"], wl["head_dim"]
+    torch.cuda.set_device(0)
+    q, K, V = W.c3_layer(0, device="cuda", seed=wl["seed"], batch=B, ctx=N, Hq=Hq, Hkv=Hkv)
+    q, K, V = q.contiguous(), K.contiguous(), V.contiguous()
+    first = kvq.Cache(1, B, Hq, Hkv, max_ctx=N)
+    first.append(0, K, V)
+    torch.cuda.synchronize()
+    first.close()
+    cache = kvq.Cache(1, B, Hq, Hkv, max_ctx=N)
+    cache.append(0, K, V)
+    out = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+    for _ in range(3):
+        cache.decode(0, q, wl["tau_cov"], wl["eps"], out)
+    for _ in range(3):
+        cache.decode_uncertified(0, q, out)
+    ws = None
+    for _ in range(3):
+        ws = kvq.dense_attention(q, K, V, out, ws)
+    torch.cuda.synchronize()
+    cache.close()
+    print(json.dumps({"profile_layer": "done", "workload": wl["name"] + " (layer 0)"}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1100,6 +1138,8 @@ def main():
                     help="with --loop: fraction of each layer's FP16 blocks kept resident in HBM")
     ap.add_argument("--loop", action="store_true",
                     help="token-by-token decode loop (append + decode per layer and step)")
+    ap.add_argument("--profile-layer", dest="profile_layer", action="store_true",
+                    help="run the fixed launch sequence of profile_layer (for ncu captures) and exit")
     ap.add_argument("--sweep", choices=["c5", "vtol"], default=None,
                     help="run a sweep instead of the headline (one JSON line per point)")
     args = ap.parse_args()
@@ -1111,6 +1151,9 @@ def main():
         return
     if args.loop:
         decode_loop(args)
+        return
+    if args.profile_layer:
+        profile_layer(args)
         return
     wl = dict(WORKLOAD)
     for k in ("layers", "ctx", "batch"):
