@@ -48,7 +48,7 @@ __device__ __forceinline__ void vc_offset(int t, int c, int& word_byte, int& bit
 }
 
 constexpr int SROW = D + 8;   // padded shared row (272 bytes): fewer bank conflicts
-constexpr int APP_R = 4;      // blocks per CTA (value-range and scale-maximum atomics once per CTA)
+constexpr int APP_R = 2;      // blocks per CTA (value-range and scale-maximum atomics once per CTA)
 
 // Codes are rint(x / s) for an IEEE fp32 divide followed by rounding to the nearest
 // integer, ties to even.  They are computed through the reciprocal r = rn(1 / s):

@@ -64,6 +64,8 @@ def _check(out, q, K, V, heads=None):
     (2, 4, 2, 9),              # n_rep 2, fewer tokens than one warp's slice
     (4, 32, 8, 64 * 40),       # exact blocks; one CTA range spans several groups
     (1, 4, 1, 64 * 1000 + 63), # one group split over every CTA
+    (32, 16, 4, 130),          # 128 groups of three blocks: CTA ranges cross many groups
+    (64, 8, 2, 100),           # fewer blocks than CTAs: one block per CTA
 ])
 def test_dense_hbm_matches_oracle(B, Hq, Hkv, N):
     q, K, V = _inputs(B, Hq, Hkv, N, seed=B * 1000 + N)
@@ -89,6 +91,14 @@ def test_dense_hbm_full_layer_128k():
     out, _ = _run(q, K, V)
     worst = _check(out, q, K, V)
     print(f"128K layer: max-abs error {worst:.2e}")
+
+
+def test_dense_hbm_max_context():
+    """The library's largest context, 2,097,152 tokens, one KV group of four query heads:
+    every head against the oracle."""
+    q, K, V = _inputs(1, 4, 1, 2097152, seed=13)
+    out, _ = _run(q, K, V)
+    _check(out, q, K, V)
 
 
 def test_dense_hbm_argument_checks():
