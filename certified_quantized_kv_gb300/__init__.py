@@ -188,7 +188,9 @@ class Cache:
     def decode(self, layer: int, q, tau_cov: float, eps: float, out, cert=None, ladder_level=None,
                stream=None):
         """q, out: contiguous fp16 tensors [B, Hq, 128] (device or host); cert: uint8 tensor
-        of B*Hq*32 bytes or None; ladder_level: int32 tensor [B] or None."""
+        of B*Hq*32 bytes or None; ladder_level: int32 tensor [B] or None.  Pinned host
+        tensors are copied in stream order (read the results after a synchronize);
+        pageable host tensors make the call wait for its copies."""
         self._check_decode_args(q, out, cert)
         if ladder_level is not None:
             import torch

@@ -179,6 +179,17 @@ bool is_device_ptr(const void* p) {
   return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
 }
 
+// Page-locked host memory (cudaHostAlloc, cudaHostRegister): copies to and from it are
+// ordered on the stream without the host waiting.
+bool is_pinned_host_ptr(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
 cudaEvent_t pooled_event(kvq_cache* c) {
   if (!c->ev_pool.empty()) {
     cudaEvent_t e = c->ev_pool.back();
@@ -597,7 +608,11 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   const bool q_dev = is_device_ptr(q), out_dev = is_device_ptr(out);
   const bool cert_dev = cert && is_device_ptr(cert);
   const bool lvl_dev = ladder_level && is_device_ptr(ladder_level);
-  bool host_any = !q_dev || !out_dev || (cert && !cert_dev) || (ladder_level && !lvl_dev);
+  // pageable host buffers make the call wait for its copies; page-locked ones are copied
+  // in stream order (valid once the stream has reached them)
+  const bool pageable_any = (!q_dev && !is_pinned_host_ptr(q)) || (!out_dev && !is_pinned_host_ptr(out)) ||
+                            (cert && !cert_dev && !is_pinned_host_ptr(cert)) ||
+                            (ladder_level && !lvl_dev && !is_pinned_host_ptr(ladder_level));
   // device buffers are read and written in place with vector accesses (host buffers are
   // staged through the cache's own)
   if ((q_dev && !aligned(q, 16)) || (out_dev && !aligned(out, 16)))
@@ -681,7 +696,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   if (!out_dev) KVQ_CUDA(cudaMemcpyAsync(out, od, HQ * D * 2, cudaMemcpyDeviceToHost, st), "copy out");
   if (cert && !cert_dev) KVQ_CUDA(cudaMemcpyAsync(cert, cd, HQ * sizeof(kvq_certificate), cudaMemcpyDeviceToHost, st), "copy cert");
   if (ladder_level && !lvl_dev) KVQ_CUDA(cudaMemcpyAsync(ladder_level, ld, c->B * 4, cudaMemcpyDeviceToHost, st), "copy level");
-  if (host_any) KVQ_CUDA(cudaStreamSynchronize(st), (f + ": sync").c_str());
+  if (pageable_any) KVQ_CUDA(cudaStreamSynchronize(st), (f + ": sync").c_str());
   c->last_layer = layer;
   c->last_nb = all_dense ? -1 : V.nb;
   return KVQ_OK;

@@ -153,8 +153,12 @@ kvq_status kvq_append(kvq_cache* cache, int layer, const void* k, const void* v,
  *   out          [B, Hq, D] FP16, device or host memory
  *   cert         [B * Hq] certificates (may be NULL), device or host memory
  *   ladder_level [B] highest rung reached per sequence (may be NULL), device or host
- * If any of q, out, cert or ladder_level is host memory, the call stages it through
- * device buffers and synchronises `stream` before returning.  Device buffers are used in
+ * Host memory for any of q, out, cert or ladder_level is staged through the cache's own
+ * device buffers.  Page-locked host buffers (cudaHostAlloc, cudaHostRegister) are copied
+ * in stream order, like cudaMemcpyAsync: q is read when the stream reaches the call, and
+ * out, cert and ladder_level hold the results once the stream has completed it.  If any
+ * host buffer is pageable, the call synchronises `stream` before returning, so every
+ * result is in place on return.  Device buffers are used in
  * place and must be aligned: q and out to 16 bytes, cert to 8, ladder_level to 4.  Tier-2 blocks are read
  * directly by the kernels through the host link (NVLink-C2C); no host round trip
  * happens inside the call.

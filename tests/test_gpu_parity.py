@@ -190,6 +190,34 @@ def test_host_buffers_match_device_buffers():
     assert np.array_equal(gd["cert"], gh["cert"]) and np.array_equal(gd["level"], gh["level"])
 
 
+def test_pageable_host_buffers_are_ready_on_return():
+    """Pageable host outputs hold the results when the call returns (no synchronise by
+    the caller); page-locked ones are copied in stream order and match after one."""
+    q, K, V = W.tiny(seed=12, ctx=64 * 7 + 5, Hq=8, Hkv=2, kscale=3.0)
+    B, Hq, D = q.shape
+    cache = kvq.Cache(1, B, Hq, K.shape[1], max_ctx=K.shape[2])
+    try:
+        cache.append(0, K.cuda().contiguous(), V.cuda().contiguous())
+        out_d = torch.empty(B, Hq, D, dtype=torch.float16, device="cuda")
+        cert_d = torch.empty(B * Hq * 32, dtype=torch.uint8, device="cuda")
+        cache.decode(0, q.cuda().contiguous(), 0.95, 0.25, out_d, cert_d)
+        torch.cuda.synchronize()
+        ref_out, ref_cert = out_d.cpu(), kvq.certificates(cert_d)
+        out_h = torch.full((B, Hq, D), float("nan"), dtype=torch.float16)   # pageable
+        cert_h = torch.zeros(B * Hq * 32, dtype=torch.uint8)
+        cache.decode(0, q.contiguous(), 0.95, 0.25, out_h, cert_h)
+        assert torch.equal(out_h, ref_out)
+        assert np.array_equal(kvq.certificates(cert_h), ref_cert)
+        out_p = torch.full((B, Hq, D), float("nan"), dtype=torch.float16).pin_memory()
+        cert_p = torch.zeros(B * Hq * 32, dtype=torch.uint8).pin_memory()
+        cache.decode(0, q.contiguous().pin_memory(), 0.95, 0.25, out_p, cert_p)
+        torch.cuda.synchronize()
+        assert torch.equal(out_p, ref_out)
+        assert np.array_equal(kvq.certificates(cert_p), ref_cert)
+    finally:
+        cache.close()
+
+
 def test_deterministic_repeat():
     q, K, V = W.c1(ctx=64 * 50 + 7, Hq=8, Hkv=2)
     g = gpu_run(q, K, V, 0.995, 0.25, repeat=3)
