@@ -276,6 +276,7 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
   const unsigned long long rem = target - above;
   int cnt = 0;
   unsigned long long take_w = 0;
+  bool small = false;   // the candidates were ranked by warp 0 alone
   if (ncand > SEL_CAND) {
     // one key value left (lo == hi) with more keys than the exact ranking takes: ties,
     // lowest indices first
@@ -310,6 +311,35 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
     }
     __syncthreads();
     const int nc = ws.ncand;
+    if (nc <= 32) {
+      // few candidates: warp 0 ranks them with shuffles (no block barrier)
+      if (warp == 0) {
+        const bool live = lane < nc;
+        const uint32_t ka = live ? ws.ckey[lane] : 0u;
+        const int ia = live ? ws.cidx[lane] : 0x7fffffff;
+        const unsigned long long wa = live ? key_weight(ka) : 0ull;
+        int rank = 0;
+        for (int j = 0; j < nc; ++j) {   // candidates before this one: key descending, index ascending
+          const uint32_t kb = __shfl_sync(0xffffffffu, ka, j);
+          const int ib = __shfl_sync(0xffffffffu, ia, j);
+          rank += (kb > ka) || (kb == ka && ib < ia);
+        }
+        unsigned long long excl = 0ull, tot_c = 0ull;   // weight of the candidates ranked before
+        for (int j = 0; j < nc; ++j) {
+          const int rb = __shfl_sync(0xffffffffu, rank, j);
+          const unsigned long long wb = __shfl_sync(0xffffffffu, wa, j);
+          if (rb < rank) excl += wb;
+          tot_c += wb;
+        }
+        // the candidate whose running weight first reaches the remainder is the last taken
+        const unsigned crossing = __ballot_sync(0xffffffffu, live && excl < rem && excl + wa >= rem);
+        const int last = crossing ? __shfl_sync(0xffffffffu, rank, __ffs(crossing) - 1) : nc - 1;
+        const unsigned long long tw = crossing ? __shfl_sync(0xffffffffu, excl + wa, __ffs(crossing) - 1) : tot_c;
+        if (live && rank <= last) { mark(ia); ++cnt; }
+        if (lane == 0) ws.take_w = tw;   // read after the count's barriers below
+      }
+      small = true;
+    } else {
     const int nc4 = (nc + 3) & ~3;
     if (tid >= nc && tid < nc4) ws.ckey[tid] = 0u;   // padding ranks below every candidate
     __syncthreads();
@@ -342,9 +372,12 @@ __device__ int block_select_top(int n, const uint32_t* keys, unsigned long long 
     take_w = (ws.take_w != 0ull || last < 0) ? ws.take_w : tot_c;
     if (tid <= last && tid < nc) { mark(ws.cidx[ws.order[tid]]); ++cnt; }
     __syncthreads();
+    }
   }
+  const int taken_cnt = block_sum_int(cnt, ws.red);
+  if (small) take_w = ws.take_w;
   *taken = above + take_w;
-  return block_sum_int(cnt, ws.red);
+  return taken_cnt;
 }
 
 }  // namespace kvq
