@@ -22,7 +22,9 @@ summary (Japanese and French editions).  Section names used below:
 The pages give no formulas.  Where they are silent, each function states the reading
 (A1..A8) it implements.  The pages print no worked example or bound value, so agreement
 with the paper's own numbers is parity unpinned; the functions are pinned instead by
-invariants, closed forms and brute force in tests/test_oracle_pins.py.
+invariants, closed forms and brute force in tests/test_oracle_pins.py, and the ladder
+planner (plan_ladder, ranking_consistent, the rung-4 rule) by subset enumeration and
+hand-built orders in tests/test_oracle_ladder_pins.py.
 
 Arithmetic.  Quantisation uses IEEE binary32 operations (numpy float32 ops are
 correctly rounded) and binary16 storage, spelled out step by step because they fix
