@@ -676,40 +676,59 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
 namespace {
 
 // Round 0 with INT4 values in VRAM.  Every block needs the INT4 codes and scale/offset of
-// its values, and a block that keeps its INT8 scores needs nothing else, so each warp
-// (one value group) forms the weights of all the group's heads for itself from the
-// stored scores: such blocks run without a CTA barrier, fed by a two-stage cp.async ring
-// per warp that holds the next block while the current one is multiplied.  Blocks with
-// FP16 keys are scored by the whole CTA (tier-2 read, then the dot products between two
-// barriers) and their weights handed to the warps through shared memory.
+// its values; a block that keeps its INT8 scores needs nothing else, a block with FP16
+// keys needs its keys from tier 2 (or a resident copy) scored by the whole CTA.
+//  - Blocks that keep INT8 scores are dealt to the warps by position in the work item
+//    (block j to warp j mod 4), and a warp multiplies each of its blocks whole, all four
+//    value groups, as the INT4 tail pass does: the weights of head hp at tokens
+//    8 sub + [0, 8) split once into binary16 halves, each group's products p s 2^e as
+//    exact halves by packed-half TwoProduct FMAs, INT4 codes as binary16 subnormals into
+//    the MMA.  Its copies come from a two-stage cp.async ring that holds its own
+//    positions only (the first one copied before the item's FP16-key flags are known; a
+//    position whose keys turn out FP16 leaves an empty group in the ring).
+//  - A block with FP16 keys is scored by the whole CTA between barriers, as before; each
+//    warp then multiplies the weights into its own value group, whose codes and
+//    scale/offset it loads directly while the keys are read.
+//  - The item's reference M per head starts at the selection's and rises only where an
+//    FP16-key block scores above it; every sum is then rescaled, so each item's partial
+//    depends on its own blocks alone.  At the end of the item the four warps' sums meet
+//    in shared memory and one partial per item is written, as before.
 constexpr int R0_STAGES = 2;
+constexpr int R0_CTAS_PER_SM = 3;
 static_assert(CHUNK <= 32, "one FP16-key flag per lane of a warp");
 
-struct __align__(16) R0Stage {   // one block, one value group
-  float4 s[MAXREP * BLK / 4];    // INT8 scores [head][token]
-  uint4 codes[64];               // the group's INT4 code chunks (this lane's: lane, lane + 32)
-  uint4 so[BLK / 4];             // the group's (scale, offset) half2 per token
+// One block that keeps its INT8 scores, whole: INT4 codes (a lane's chunks at lane + 32 j),
+// (scale, offset) per value group and token, and the INT8 scores of the group's heads.
+struct __align__(16) R0Stage {
+  uint4 codes[VC_BYTES / 16];     // 256 chunks
+  uint4 so[VSV_WORDS / 4];        // 64 x 4 half2: [group][token]
+  float4 s[MAXREP * BLK / 4];     // [head][token]
 };
 
-struct __align__(16) R0Smem {
-  float p[MAXREP][BLK];          // weights of an FP16-key block
-  float s16[MAXREP][BLK];        // its FP16 scores
+struct __align__(16) R0Smem {     // dynamic shared memory
+  R0Stage ring[4][R0_STAGES];     // per warp
+  uint32_t tw[4][MW_WORDS];       // per warp: the B words of one value group
+  float p[MAXREP][BLK];           // weights of an FP16-key block
+  float s16[MAXREP][BLK];         // its FP16 scores
   float qf[MAXREP][D];
-  float M[MAXREP];               // the item's reference per head after an FP16-key block
-  float fac[MAXREP];             // factor that moved the item's sums to that reference
-  uint32_t bw[4][MW_WORDS];      // per warp: the B words of its value group
-  __half kbuf[BLK][KROW];
-  R0Stage ring[4][R0_STAGES];
+  float M[MAXREP];                // the item's reference per head after an FP16-key block
+  float fac[MAXREP];              // factor that moved the item's sums to that reference
+  union {
+    __half kbuf[BLK][KROW];                   // keys of an FP16-key block
+    float red[4][NG][MAXREP][VG];             // item end: each warp's sums per group, head, channel
+  } u;
+  float lred[4][MAXREP];          // item end: each warp's weight sums per head
   int item;
   int res[2];
 };
 
 }  // namespace
 
-__global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
+__global__ void __launch_bounds__(128, R0_CTAS_PER_SM) mixed_kernel_r0(LayerView V) {
   pdl_trigger();
   pdl_wait();   // selection: FP16-key flags, reference maxima; scores of the scoring pass
-  __shared__ R0Smem sm;
+  extern __shared__ __align__(16) unsigned char r0_dsm[];
+  R0Smem& sm = *reinterpret_cast<R0Smem*>(r0_dsm);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int hp = lane >> 3, sub = lane & 7;   // weight role: head hp, tokens 8 sub + [0, 8)
@@ -720,6 +739,7 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
   const bool wact = warp < V.n_rep;           // head `warp` exists (FP16-key role)
   const unsigned long long pol = evict_first_policy();
   R0Stage* ring = sm.ring[warp];
+  uint32_t* tw = sm.tw[warp];
   int cur_hs = -1;
   int pre_e = 0;
   float pre_v = 1.f, pre_ef = 0.f;
@@ -748,89 +768,83 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
         const int r = i / D, c = i % D;
         sm.qf[r][c] = (r < V.n_rep) ? __half2float(V.q[(hrow + r) * D + c]) : 0.f;
       }
-      pre_e = prescale_exp(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs])));
+      // weights p 2^e <= 2^e must be finite binary16 values on the INT8 path: e <= 15
+      pre_e = min(15, prescale_exp(__half2float(__ushort_as_half((unsigned short)V.vscale_max[hs]))));
       pre_v = ldexpf(1.f, pre_e);
       pre_ef = (float)pre_e;
       __syncthreads();
     }
-    // the item's softmax reference per head starts at the selection's (>= every INT8
-    // score) and rises only where an FP16-key block of the item scores above it, so it
-    // depends on the item's own blocks alone
-    float Mh = act ? V.hst[hrow + hp].M : 0.f;      // head hp: INT8 weights, offsets, sums
+    float Mh = act ? V.hst[hrow + hp].M : 0.f;      // head hp: weights, offsets, sums
     float Mw = wact ? V.hst[hrow + warp].M : 0.f;   // head `warp`: FP16 scoring role
 
     const int blk0 = ch * V.chunk, blk_end = min(V.nb, blk0 + V.chunk);
+    const int nblk = blk_end - blk0;
     const size_t bi0 = (size_t)hs * V.nbmax + blk0;
-    int pb = blk0;          // producer: next block to copy
-    unsigned kmask = 0;     // bit j: block blk0 + j has FP16 keys
-    auto issue_vals = [&](int st) {   // the group's INT4 codes and (scale, offset) of block pb
-      const size_t bi = bi0 + (pb - blk0);
-      R0Stage& T = ring[st];
-      const uint4* vc = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES) + warp * 64;
-      cp_async16_hint(&T.codes[lane], vc + lane, pol);
-      cp_async16_hint(&T.codes[lane + 32], vc + lane + 32, pol);
-      if (lane < BLK / 4)
-        cp_async16_hint(&T.so[lane], reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS + warp * BLK) + lane, pol);
-    };
-    auto issue_scores = [&](int st) {   // INT8 scores of block pb, unless its keys are FP16
-      if ((kmask >> (pb - blk0)) & 1u) return;
-      R0Stage& T = ring[st];
+    unsigned kmask = 0;   // bit j: block blk0 + j has FP16 keys
+    // copy of this warp's k-th position (block blk0 + warp + 4k) into slot k % R0_STAGES:
+    // the whole block if it keeps its INT8 scores (or when `always`), else nothing; one
+    // commit group either way
+    auto issue = [&](int k, bool always) {
+      const int j = warp + 4 * k;
+      if (j < nblk && (always || !((kmask >> j) & 1u))) {
+        const size_t bi = bi0 + j;
+        R0Stage& T = ring[k % R0_STAGES];
+        const uint4* vc = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES);
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {   // 64 float4 of scores: head (lane + 32 j) / 16
-        const int idx = lane + 32 * j, h = idx >> 4;
-        if (h < V.n_rep)
-          cp_async16_hint(&T.s[idx], V.shat + (hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)pb * BLK + 4 * (idx & 15), pol);
-      }
-    };
-    auto issue = [&](int st) {
-      if (pb < blk_end) {
-        issue_vals(st);
-        issue_scores(st);
-        ++pb;
+        for (int jj = 0; jj < 8; ++jj) cp_async16_hint(&T.codes[lane + 32 * jj], vc + lane + 32 * jj, pol);
+        const uint4* so = reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS);
+        cp_async16_hint(&T.so[lane], so + lane, pol);
+        cp_async16_hint(&T.so[lane + 32], so + lane + 32, pol);
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {   // 64 float4 of scores: head (lane + 32 jj) / 16
+          const int idx = lane + 32 * jj, h = idx >> 4;
+          if (h < V.n_rep)
+            cp_async16_hint(&T.s[idx], V.shat + (hrow + h) * ((size_t)V.nbmax * BLK) + (size_t)(blk0 + j) * BLK + 4 * (idx & 15), pol);
+        }
       }
       cp_async_commit();
     };
-    // the item's FP16-key flags (one block per lane), fetched while the first block is in
-    // flight; that block's scores are copied whatever its flag, so that no copy waits on it
+    // the first position is copied before the item's FP16-key flags arrive
+    issue(0, true);
     {
-      const int nblk = blk_end - blk0;
       const unsigned char f = (lane < nblk) ? V.kprom0[bi0 + lane] : 0;
-      if (nblk > 0) {
-        issue_vals(0);
-        issue_scores(0);   // kmask is still 0
-        ++pb;
-      }
-      cp_async_commit();
       kmask = __ballot_sync(0xffffffffu, f != 0);
     }
+    issue(1, false);
 
-    float acc[2][4];
+    float accT[NG][2][4];   // INT8-score blocks of this warp: all four groups
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int gg = 0; gg < NG; ++gg)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    float off = 0.f;    // sum p * offset: head hp, this lane's tokens, group = warp
-    float lsum = 0.f;   // sum p: head hp, this lane's tokens
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) accT[gg][mt][j] = 0.f;
+    float2 offT[NG];        // sum p o per group, head hp, this lane's tokens (pairs)
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) offT[gg] = make_float2(0.f, 0.f);
+    float accF[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};   // FP16-key blocks: group `warp`
+    float offF = 0.f;       // sum p o, group `warp`, head hp, this lane's tokens
+    float lsumT = 0.f, lsumF = 0.f;   // sum p, head hp, this lane's tokens
 
-    for (int blk = blk0, it = 0; blk < blk_end; ++blk, ++it) {
-      const bool kp0 = (kmask >> (blk - blk0)) & 1u;
-      issue((it + 1) % R0_STAGES);
-      cp_async_wait<1>();
-      __syncwarp();
-      const R0Stage& T = ring[it % R0_STAGES];
-      // weights p = exp(s' - M) of head hp at tokens 8 sub + [0, 8)
-      float pv[8];
-      if (kp0) {
-        // FP16 keys from tier 2 (or their resident copy); the FP16 scores replace the
-        // INT8 ones in the score scratch for the second pass
+    for (int j = 0; j < nblk; ++j) {
+      const int blk = blk0 + j;
+      if ((kmask >> j) & 1u) {
+        // ---- FP16 keys from tier 2 (or their resident copy), scored by the whole CTA;
+        //      the FP16 scores replace the INT8 ones in the score scratch for round 1 ----
         const size_t bi = (size_t)hs * V.nbmax + blk;
+        // this warp's value group of the block: codes (two chunks) and the (scale,
+        // offset) of this lane's eight tokens, loaded while the keys are read
+        const uint4* vcp = reinterpret_cast<const uint4*>(V.vc + bi * VC_BYTES);
+        const uint4 vcode0 = vcp[lane + 32 * (2 * warp)], vcode1 = vcp[lane + 32 * (2 * warp + 1)];
+        const uint4* sop = reinterpret_cast<const uint4*>(V.vsv + bi * VSV_WORDS + warp * BLK);
+        const uint4 S0 = sop[2 * sub], S1 = sop[2 * sub + 1];
         const ResPick pk = res_pick(V, 0, bi, sm.res);
-        load_f16_block<KROW>(&sm.kbuf[0][0],
+        load_f16_block<KROW>(&sm.u.kbuf[0][0],
                              res_src(V, pk, V.t2k + ((size_t)hs * V.cap + (size_t)blk * BLK) * D),
                              res_dst(V, pk));
         res_commit(V, 0, bi, pk);
         __syncthreads();
-        score_f16_block(sm.kbuf, sm.qf, sm.s16);
+        score_f16_block(sm.u.kbuf, sm.qf, sm.s16);
         __syncthreads();
         float p0 = 0.f, p1 = 0.f, fac = 1.f;
         if (wact) {
@@ -857,95 +871,186 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
         __syncthreads();
         {
           const float ft = sm.fac[tig], fh = sm.fac[hp];   // accumulator columns: head tig
+          if (__any_sync(0xffffffffu, ft != 1.f || fh != 1.f)) {
 #pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
+            for (int gg = 0; gg < NG; ++gg) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) acc[mt][j] *= ft;
-          off *= fh;
-          lsum *= fh;
+              for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) accT[gg][mt][q] *= ft;
+              offT[gg].x *= fh;
+              offT[gg].y *= fh;
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+              for (int q = 0; q < 4; ++q) accF[mt][q] *= ft;
+            offF *= fh;
+            lsumT *= fh;
+            lsumF *= fh;
+          }
           if (act) Mh = sm.M[hp];
         }
-        const float4 pa = *reinterpret_cast<const float4*>(&sm.p[hp][8 * sub]);
-        const float4 pc = *reinterpret_cast<const float4*>(&sm.p[hp][8 * sub + 4]);
-        pv[0] = pa.x; pv[1] = pa.y; pv[2] = pa.z; pv[3] = pa.w;
-        pv[4] = pc.x; pv[5] = pc.y; pv[6] = pc.z; pv[7] = pc.w;
-      } else {
-        const float4 sa = T.s[hp * (BLK / 4) + 2 * sub], sb = T.s[hp * (BLK / 4) + 2 * sub + 1];
-        const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) pv[i] = act ? exp2_approx(fmaf(sv[i] - Mh, LOG2E_F, pre_ef)) : 0.f;
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) lsum += pv[i];
-      // products p_t s_{t,g} 2^e of head hp at tokens 8 sub + [0, 8) as hi + lo halves
-      // (the weights carry 2^e), exchanged through shared memory as B fragments
-      {
-        const uint4 S0 = T.so[2 * sub], S1 = T.so[2 * sub + 1];   // (scale, offset), 8 tokens
-        const uint32_t sw[8] = {S0.x, S0.y, S0.z, S0.w, S1.x, S1.y, S1.z, S1.w};
-        uint32_t hw[4], lw[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {   // token pair 4 sub + i
-          const float2 a = __half22float2(u32_as_h2(sw[2 * i])), c = __half22float2(u32_as_h2(sw[2 * i + 1]));
-          const float2 p2 = make_float2(pv[2 * i], pv[2 * i + 1]);
-          off = fmaf(p2.x, a.y, off);
-          off = fmaf(p2.y, c.y, off);
-          const float2 w = mul2(p2, make_float2(a.x, c.x));
-          const __half2 hi = __floats2half2_rn(w.x, w.y);
-          const float2 rem = sub2(w, __half22float2(hi));   // exact remainders
-          hw[i] = h2_as_u32(hi);
-          lw[i] = h2_as_u32(__floats2half2_rn(rem.x, rem.y));
+        float pv[8];
+        {
+          const float4 pa = *reinterpret_cast<const float4*>(&sm.p[hp][8 * sub]);
+          const float4 pc = *reinterpret_cast<const float4*>(&sm.p[hp][8 * sub + 4]);
+          pv[0] = pa.x; pv[1] = pa.y; pv[2] = pa.z; pv[3] = pa.w;
+          pv[4] = pc.x; pv[5] = pc.y; pv[6] = pc.z; pv[7] = pc.w;
         }
-        uint32_t* wr = sm.bw[warp] + hp * (2 * MW_ROW) + 4 * sub;
-        *reinterpret_cast<uint4*>(wr) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        *reinterpret_cast<uint4*>(wr + MW_ROW) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) lsumF += pv[i];
+        // products p_t s_{t,g} 2^e of head hp at tokens 8 sub + [0, 8) as hi + lo halves,
+        // exchanged through shared memory as B fragments
+        {
+          const uint32_t sw[8] = {S0.x, S0.y, S0.z, S0.w, S1.x, S1.y, S1.z, S1.w};
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {   // token pair 4 sub + i
+            const float2 a = __half22float2(u32_as_h2(sw[2 * i])), c = __half22float2(u32_as_h2(sw[2 * i + 1]));
+            const float2 p2 = make_float2(pv[2 * i], pv[2 * i + 1]);
+            offF = fmaf(p2.x, a.y, offF);
+            offF = fmaf(p2.y, c.y, offF);
+            const float2 w = mul2(p2, make_float2(a.x, c.x));
+            const __half2 hi = __floats2half2_rn(w.x, w.y);
+            const float2 rem = sub2(w, __half22float2(hi));   // exact remainders
+            hw[i] = h2_as_u32(hi);
+            lw[i] = h2_as_u32(__floats2half2_rn(rem.x, rem.y));
+          }
+          uint32_t* wr = tw + hp * (2 * MW_ROW) + 4 * sub;
+          *reinterpret_cast<uint4*>(wr) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(wr + MW_ROW) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        __syncwarp();
+        {
+          // column gid = (head gid>>1, hi or lo): k-step kk takes token pairs 8 tig + 2kk and
+          // 8 tig + 2kk + 1 (tokens 16 tig + 4kk + {0,1} and {2,3})
+          const uint32_t* rd = tw + (gid >> 1) * (2 * MW_ROW) + (gid & 1) * MW_ROW + 8 * tig;
+          const uint4 B0 = *reinterpret_cast<const uint4*>(rd), B1 = *reinterpret_cast<const uint4*>(rd + 4);
+          const uint32_t bb[8] = {B0.x, B0.y, B0.z, B0.w, B1.x, B1.y, B1.z, B1.w};
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const uint4 Cw = mt ? vcode1 : vcode0;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              uint32_t a0, a1, a2, a3;
+              nib8_to_sub_f16x4(word_of(Cw, kk), a0, a1, a2, a3);
+              mma16816(accF[mt], a0, a1, a2, a3, bb[2 * kk], bb[2 * kk + 1]);
+            }
+          }
+        }
+        __syncwarp();   // every lane has read the B words
       }
+      if ((j & 3) != warp) continue;
+      // ---- this warp's position: its ring slot (empty if the keys are FP16) ----
+      const int k = j >> 2;
+      cp_async_wait<R0_STAGES - 1>();
       __syncwarp();
-      // column gid = (head gid>>1, hi or lo): k-step kk takes token pairs 8 tig + 2kk and
-      // 8 tig + 2kk + 1 (tokens 16 tig + 4kk + {0,1} and {2,3})
-      uint32_t bb0[4], bb1[4];
-      {
-        const uint32_t* rd = sm.bw[warp] + (gid >> 1) * (2 * MW_ROW) + (gid & 1) * MW_ROW + 8 * tig;
-        const uint4 B0 = *reinterpret_cast<const uint4*>(rd), B1 = *reinterpret_cast<const uint4*>(rd + 4);
-        bb0[0] = B0.x; bb1[0] = B0.y; bb0[1] = B0.z; bb1[1] = B0.w;
-        bb0[2] = B1.x; bb1[2] = B1.y; bb0[3] = B1.z; bb1[3] = B1.w;
-      }
+      if (!((kmask >> j) & 1u)) {
+        const R0Stage& T = ring[k % R0_STAGES];
+        // weights of head hp at tokens 8 sub + [0, 8), times 2^e, with their binary16
+        // halves (token pair i = tokens 8 sub + 2i, +1)
+        float2 pf[4];
+        __half2 ph[4], pl[4];
+        {
+          const float4 sa = T.s[hp * (BLK / 4) + 2 * sub], sb = T.s[hp * (BLK / 4) + 2 * sub + 1];
+          const float sv[8] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const uint4 C = T.codes[lane + 32 * mt];
+          for (int i = 0; i < 4; ++i) {
+            const float p0 = act ? exp2_approx(fmaf(sv[2 * i] - Mh, LOG2E_F, pre_ef)) : 0.f;
+            const float p1 = act ? exp2_approx(fmaf(sv[2 * i + 1] - Mh, LOG2E_F, pre_ef)) : 0.f;
+            lsumT += p0 + p1;
+            pf[i] = make_float2(p0, p1);
+            ph[i] = __floats2half2_rn(p0, p1);
+            const float2 r = sub2(pf[i], __half22float2(ph[i]));   // exact
+            pl[i] = __floats2half2_rn(r.x, r.y);
+          }
+        }
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          uint32_t a0, a1, a2, a3;
-          nib8_to_sub_f16x4(word_of(C, kk), a0, a1, a2, a3);
-          mma16816(acc[mt], a0, a1, a2, a3, bb0[kk], bb1[kk]);
+        for (int gg = 0; gg < NG; ++gg) {
+          const uint4 S0 = T.so[gg * (BLK / 4) + 2 * sub], S1 = T.so[gg * (BLK / 4) + 2 * sub + 1];
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {   // token pair 4 sub + i: tokens 8 sub + 2i, +1
+            const uint4& S = (i < 2) ? S0 : S1;
+            const __half2 a = u32_as_h2(word_of(S, 2 * (i & 1)));       // (scale, offset) of token 2i
+            const __half2 c = u32_as_h2(word_of(S, 2 * (i & 1) + 1));   // ... of token 2i + 1
+            const __half2 s2 = __lows2half2(a, c), o2 = __highs2half2(a, c);
+            const __half2 hi = __hmul2_rn(ph[i], s2);
+            __half2 lo = __hfma2(ph[i], s2, __hneg2(hi));   // p_hi s - hi, exact
+            lo = __hfma2(pl[i], s2, lo);
+            hw[i] = h2_as_u32(hi);
+            lw[i] = h2_as_u32(lo);
+            offT[gg] = fma2(pf[i], __half22float2(o2), offT[gg]);
+          }
+          uint32_t* wr = tw + hp * (2 * MW_ROW) + 4 * sub;
+          *reinterpret_cast<uint4*>(wr) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(wr + MW_ROW) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          __syncwarp();
+          const uint32_t* rd = tw + (gid >> 1) * (2 * MW_ROW) + (gid & 1) * MW_ROW + 8 * tig;
+          const uint4 B0 = *reinterpret_cast<const uint4*>(rd), B1 = *reinterpret_cast<const uint4*>(rd + 4);
+          const uint32_t bb[8] = {B0.x, B0.y, B0.z, B0.w, B1.x, B1.y, B1.z, B1.w};
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const uint4 Cw = T.codes[lane + 32 * (2 * gg + mt)];
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              uint32_t a0, a1, a2, a3;
+              nib8_to_sub_f16x4(word_of(Cw, kk), a0, a1, a2, a3);
+              mma16816(accT[gg][mt], a0, a1, a2, a3, bb[2 * kk], bb[2 * kk + 1]);
+            }
+          }
+          __syncwarp();   // every lane has read the B words before the next group's
         }
       }
-      __syncwarp();   // every lane is done with the B words and this ring stage
+      __syncwarp();       // the slot is free: refill it with position k + 2
+      issue(k + R0_STAGES, false);
     }
     cp_async_wait<0>();
     __syncwarp();
 
-    // ---- this chunk's partial: l and acc[D] per head ----
-    off += __shfl_xor_sync(0xffffffffu, off, 1);   // head hp: its eight product lanes
-    off += __shfl_xor_sync(0xffffffffu, off, 2);
-    off += __shfl_xor_sync(0xffffffffu, off, 4);
+    // ---- this item's partial: the four warps' sums meet in shared memory ----
+    float offs[NG];
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) {
+      offs[gg] = offT[gg].x + offT[gg].y + (gg == warp ? offF : 0.f);
+      offs[gg] += __shfl_xor_sync(0xffffffffu, offs[gg], 1);   // head hp: its eight product lanes
+      offs[gg] += __shfl_xor_sync(0xffffffffu, offs[gg], 2);
+      offs[gg] += __shfl_xor_sync(0xffffffffu, offs[gg], 4);
+    }
+    float lsum = lsumT + (warp == 0 ? lsumF : 0.f);   // the FP16-key weights are the same in every warp
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
     lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
-    const float offh = __shfl_sync(0xffffffffu, off, 8 * tig);   // head tig
     // undo 2^e (weights) and 2^-24 / 2^-20 (subnormal code rows); powers of two, exact
     const float inv = ldexpf(1.f, -pre_e);
     const float inv_lo = inv * NIB_ROW_SCALE_LO, inv_hi = inv * NIB_ROW_SCALE_HI;
-    float* pp = V.part + (((size_t)hs * NCH + ch) * MAXREP) * (D + 4);
-    if (tig < V.n_rep) {
-      float* pr = pp + tig * (D + 4);
-      const int c0 = 32 * warp + gid;
-      pr[c0] = (acc[0][0] + acc[0][1]) * inv_lo + offh * inv;
-      pr[c0 + 8] = (acc[0][2] + acc[0][3]) * inv_hi + offh * inv;
-      pr[c0 + 16] = (acc[1][0] + acc[1][1]) * inv_lo + offh * inv;
-      pr[c0 + 24] = (acc[1][2] + acc[1][3]) * inv_hi + offh * inv;
+#pragma unroll
+    for (int gg = 0; gg < NG; ++gg) {
+      const float offh = __shfl_sync(0xffffffffu, offs[gg], 8 * tig);   // head tig
+      float* rr = sm.u.red[warp][gg][tig];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        float lo = accT[gg][mt][0] + accT[gg][mt][1], hi = accT[gg][mt][2] + accT[gg][mt][3];
+        if (gg == warp) {
+          lo += accF[mt][0] + accF[mt][1];
+          hi += accF[mt][2] + accF[mt][3];
+        }
+        rr[16 * mt + gid] = lo * inv_lo + offh * inv;
+        rr[16 * mt + gid + 8] = hi * inv_hi + offh * inv;
+      }
     }
-    if (warp == 0 && sub == 0 && act) {   // every warp has the sums
-      pp[hp * (D + 4) + D] = lsum * inv;
+    if (sub == 0) sm.lred[warp][hp] = lsum;
+    __syncthreads();
+    float* pp = V.part + (((size_t)hs * NCH + ch) * MAXREP) * (D + 4);
+    for (int h = 0; h < V.n_rep; ++h) {   // warp = value group, lane = channel
+      const float s = ((sm.u.red[0][warp][h][lane] + sm.u.red[1][warp][h][lane]) + sm.u.red[2][warp][h][lane]) +
+                      sm.u.red[3][warp][h][lane];
+      pp[h * (D + 4) + VG * warp + lane] = s;
+    }
+    if (warp == 0 && sub == 0 && act) {
+      const float l = ((sm.lred[0][hp] + sm.lred[1][hp]) + sm.lred[2][hp]) + sm.lred[3][hp];
+      pp[hp * (D + 4) + D] = l * inv;
       pp[hp * (D + 4) + D + 1] = Mh;
     }
     __syncthreads();
@@ -962,7 +1067,13 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel_r0(LayerView V) {
 int mixed_grid(int num_sms) { return num_sms * 4; }
 
 cudaError_t launch_mixed(const LayerView& V, int round, int grid, cudaStream_t st) {
-  if (round == 0 && V.v16 == nullptr) return launch_dependent(mixed_kernel_r0, dim3(grid), dim3(128), 0, st, V);
+  if (round == 0 && V.v16 == nullptr) {
+    const int g0 = grid / 4 * R0_CTAS_PER_SM;   // grid = 4 CTAs per SM; round 0 holds fewer
+    cudaError_t e = cudaFuncSetAttribute(mixed_kernel_r0, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)sizeof(R0Smem));
+    if (e != cudaSuccess) return e;
+    return launch_dependent(mixed_kernel_r0, dim3(g0), dim3(128), sizeof(R0Smem), st, V);
+  }
   return launch_dependent(mixed_kernel, dim3(grid), dim3(128), 0, st, V, round);
 }
 
