@@ -175,6 +175,7 @@ __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) 
     }
     // online softmax over the chunk; thread = channel, all four head slots
     float m[MAXREP], l[MAXREP], a[MAXREP];
+#pragma unroll
     for (int r = 0; r < MAXREP; ++r) { m[r] = -INFINITY; l[r] = 0.f; a[r] = 0.f; }
     const int blk_end = min(V.nb, (ch + 1) * V.chunk);
     for (int blk = ch * V.chunk; blk < blk_end; ++blk) {
@@ -252,23 +253,29 @@ __global__ void __launch_bounds__(128) dense_kernel(LayerView V, int all_dense) 
         if (lane == 0) { sm.red[r][0] = mn; sm.red[r][1] = ls; }
       }
       __syncthreads();
-      for (int r = 0; r < V.n_rep; ++r) {
-        const float mn = sm.red[r][0];
-        const float sc = (m[r] == -INFINITY) ? 0.f : expf(m[r] - mn);
-        float as = 0.f;
-        for (int t = 0; t < BLK; ++t) as = fmaf(sm.s[r][t], __half2float(sm.vbuf[t][tid]), as);
-        l[r] = l[r] * sc + sm.red[r][1];
-        a[r] = a[r] * sc + as;
-        m[r] = mn;
+#pragma unroll
+      for (int r = 0; r < MAXREP; ++r) {   // head slots r < n_rep (unrolled: m, l, a stay in registers)
+        if (r < V.n_rep) {
+          const float mn = sm.red[r][0];
+          const float sc = (m[r] == -INFINITY) ? 0.f : expf(m[r] - mn);
+          float as = 0.f;
+          for (int t = 0; t < BLK; ++t) as = fmaf(sm.s[r][t], __half2float(sm.vbuf[t][tid]), as);
+          l[r] = l[r] * sc + sm.red[r][1];
+          a[r] = a[r] * sc + as;
+          m[r] = mn;
+        }
       }
       __syncthreads();
     }
     float* pp = V.dpart + (((size_t)hs * NCH + ch) * MAXREP) * (D + 4);
-    for (int r = 0; r < V.n_rep; ++r) {
-      pp[r * (D + 4) + tid] = a[r];
-      if (tid == 0) {
-        pp[r * (D + 4) + D] = m[r];
-        pp[r * (D + 4) + D + 1] = l[r];
+#pragma unroll
+    for (int r = 0; r < MAXREP; ++r) {
+      if (r < V.n_rep) {
+        pp[r * (D + 4) + tid] = a[r];
+        if (tid == 0) {
+          pp[r * (D + 4) + D] = m[r];
+          pp[r * (D + 4) + D + 1] = l[r];
+        }
       }
     }
     __syncthreads();
