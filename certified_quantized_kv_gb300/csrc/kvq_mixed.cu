@@ -381,19 +381,28 @@ __global__ void __launch_bounds__(128, 4) mixed_kernel(LayerView V, int round) {
   }
 }
 
-// One CTA of BS_THREADS threads per (sequence, query head): combine the chunk partials of a
-// pass for the head, add the partial block, write the output and the certificate and,
-// after the first pass, run the ranking check and plan rungs 1-2.
+// Per-block values of four consecutive blocks read by the certificate pass.
+struct BlockQuad {
+  uchar4 kf, vf, sl;        // FP16-key flag, FP16-value flag, selected (ranking check)
+  float4 l8, l16, dl, eta;  // log-masses (INT8, FP16 scores), Delta_b, eta_b
+};
+
+// One CTA of BS_THREADS threads per (sequence, query head): combine the work-item partials
+// of a pass for the head, add the partial block, write the output and the certificate
+// and, after the first pass, run the ranking check and plan rungs 1-2.
 __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int round) {
   pdl_trigger();
   pdl_wait();   // partials of the mixed pass
-  extern __shared__ __align__(16) unsigned char comb_dsm[];
-  BlockSelSmem& ws = *reinterpret_cast<BlockSelSmem*>(comb_dsm);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(comb_dsm + sizeof(BlockSelSmem));   // [nb padded]
+  BlockSelSmem& ws = sel_smem();
+  uint32_t* keys = sel_keys();   // [nb padded]
   __shared__ __align__(16) float acc_s[BS_WARPS][D];
-  __shared__ float l_s[BS_WARPS];
+  __shared__ float l_s[BS_WARPS], m_s[BS_WARPS], tl_s[2];
   __shared__ float tail_p[BLK];
-  const int tid = threadIdx.x;
+  __shared__ int wk[BS_WARPS], wv[BS_WARPS];
+  __shared__ float cR[BS_WARPS], cS[BS_WARPS], cA[BS_WARPS], cE[BS_WARPS];
+  __shared__ uint32_t c8[BS_WARPS], c16[BS_WARPS];
+  __shared__ int ci8[BS_WARPS], ci16[BS_WARPS];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x;
   const int b = bh / V.Hq, h = bh % V.Hq, g = h / V.n_rep, r = h % V.n_rep;
   const int hs = b * V.Hkv + g;
@@ -412,6 +421,9 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   HeadState hsd = V.hst[hb];
   if (round == 1) {
     if (!V.gst[hs].need_round1) return;
+    const bool planned12 = hsd.planned == 1 || hsd.planned == 2;
+    if (r != 0 && !planned12) return;
+    // the group's promoted key and value blocks of the second pass (head r = 0 records them)
     int nk = 0, nv = 0;
     for (int i16 = tid; i16 < (nb + 15) / 16; i16 += BS_THREADS) {
       const uint4 a = reinterpret_cast<const uint4*>(V.kprom1 + (size_t)hs * V.nbmax)[i16];
@@ -419,9 +431,115 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
       nk += __popc(a.x) + __popc(a.y) + __popc(a.z) + __popc(a.w);
       nv += __popc(c.x) + __popc(c.y) + __popc(c.z) + __popc(c.w);
     }
-    nk = block_sum_int(nk, ws.red);
-    nv = block_sum_int(nv, ws.red);
-    if (r == 0 && tid == 0) {
+    nk = (int)__reduce_add_sync(0xffffffffu, (unsigned)nk);
+    nv = (int)__reduce_add_sync(0xffffffffu, (unsigned)nv);
+    if (lane == 0) { wk[warp] = nk; wv[warp] = nv; }
+    if (!planned12) {   // head 0 of the group, not re-run itself: the counts only
+      __syncthreads();
+      if (tid == 0) {
+        nk = 0; nv = 0;
+        for (int w = 0; w < BS_WARPS; ++w) { nk += wk[w]; nv += wv[w]; }
+        GroupState gs = V.gst[hs];
+        gs.n_kprom1 = nk;
+        gs.n_vprom1 = nv;
+        gs.bytes += (long long)(nk - gs.n_kprom0 + nv) * F16_BLOCK_BYTES;
+        V.gst[hs] = gs;
+      }
+      return;
+    }
+    // otherwise thread 0 reads the counts after the merge barrier below
+  }
+  const float M_prev = hsd.M;   // reference of the selection (round 0) or the first pass's sums (round 1)
+  // (1) work-item partials of this pass, in a fixed order: warp w takes items w, w + 16, ...
+  //     (lane = four channels) in batches of eight, its sums kept relative to the largest
+  //     item reference seen so far (rescaled when it rises; a factor of exactly 1 for
+  //     every item that kept the head's reference)
+  {
+    const float* P = (round == 0) ? V.part : V.part1;
+    float Mw = -INFINITY, l = 0.f;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int base = warp; base < nch; base += BS_WARPS * 8) {
+      float Mi[8], Li[8];
+      float4 x[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int ch = base + BS_WARPS * j;
+        if (ch < nch) {
+          const size_t o = (((size_t)hs * NCH + ch) * MAXREP + r) * (D + 4);
+          Mi[j] = P[o + D + 1];
+          Li[j] = P[o + D];
+          x[j] = *reinterpret_cast<const float4*>(P + o + 4 * lane);
+        } else {
+          Mi[j] = -INFINITY;
+          Li[j] = 0.f;
+          x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float Mb = Mw;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) Mb = fmaxf(Mb, Mi[j]);
+      if (Mb > Mw) {
+        const float f = expf(Mw - Mb);
+        a.x *= f; a.y *= f; a.z *= f; a.w *= f;
+        l *= f;
+        Mw = Mb;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (Mi[j] == -INFINITY) continue;
+        const float w = (Mi[j] == Mw) ? 1.f : expf(Mi[j] - Mw);
+        a.x = fmaf(x[j].x, w, a.x); a.y = fmaf(x[j].y, w, a.y);
+        a.z = fmaf(x[j].z, w, a.z); a.w = fmaf(x[j].w, w, a.w);
+        l = fmaf(Li[j], w, l);
+      }
+    }
+    *reinterpret_cast<float4*>(&acc_s[warp][4 * lane]) = a;
+    if (lane == 0) { l_s[warp] = l; m_s[warp] = Mw; }
+  }
+  // (2) the partial FP16 block with exact scores, weighted against M_prev (which bounds
+  //     every partial-block score)
+  {
+    float lt = 0.f;
+    if (tid < V.n_tail) {
+      const float sc = dot_f16_row(V.q + hb * D, V.tail_k + ((size_t)hs * BLK + tid) * D);
+      lt = expf(sc * INV_SQRT_D - M_prev);
+      tail_p[tid] = lt;
+    }
+    if (warp < 2) {   // BLK <= 64 tail tokens
+      lt = warp_sum(lt);
+      if (lane == 0) tl_s[warp] = lt;
+    }
+  }
+  // this thread's blocks for the certificate pass, the first four read before the barrier
+  const int kpt = sel_kpt(nb);
+  const int i0 = min(nb, tid * kpt), i1 = min(nb, i0 + kpt);
+  const bool rank0 = round == 0 && hsd.k_star > 1;   // first ranking position in the pass
+  const uint8_t* sel = V.sel + hb * V.nbmax;
+  const float* lse8 = V.lse8 + hb * V.nbmax;
+  const float* lse16 = V.lse16 + hb * V.nbmax;
+  const float* dl = V.delta + hb * V.nbmax;
+  const float* eta = V.eta + (size_t)hs * V.nbmax;
+  auto load_quad = [&](int i) {
+    BlockQuad q;
+    const int i4 = i >> 2;   // rows are padded to 16 blocks, 16-byte aligned
+    q.kf = reinterpret_cast<const uchar4*>(kfl)[i4];
+    q.vf = vfl ? reinterpret_cast<const uchar4*>(vfl)[i4] : make_uchar4(0, 0, 0, 0);
+    q.sl = rank0 ? reinterpret_cast<const uchar4*>(sel)[i4] : make_uchar4(0, 0, 0, 0);
+    q.l8 = reinterpret_cast<const float4*>(lse8)[i4];
+    q.l16 = reinterpret_cast<const float4*>(lse16)[i4];
+    q.dl = reinterpret_cast<const float4*>(dl)[i4];
+    q.eta = reinterpret_cast<const float4*>(eta)[i4];
+    return q;
+  };
+  BlockQuad q0;
+  if (i0 < i1) q0 = load_quad(i0);
+  // value range R = max_c (vmax_c - vmin_c)
+  float R = tid < D ? ord2f(V.vmax[hs * D + tid]) - ord2f(V.vmin[hs * D + tid]) : -INFINITY;
+  __syncthreads();
+  if (round == 1 && tid == 0) {
+    int nk = 0, nv = 0;
+    for (int w = 0; w < BS_WARPS; ++w) { nk += wk[w]; nv += wv[w]; }
+    if (r == 0) {
       GroupState gs = V.gst[hs];
       gs.n_kprom1 = nk;
       gs.n_vprom1 = nv;
@@ -429,90 +547,49 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
       gs.bytes += (long long)(nk - gs.n_kprom0 + nv) * F16_BLOCK_BYTES;
       V.gst[hs] = gs;
     }
-    if (!(hsd.planned == 1 || hsd.planned == 2)) return;
     hsd.n_vprom = nv;
   }
-  // (1) work-item partials of this pass in a fixed order: warp w sums items w, w + 8, ...
-  //     (lane = four channels), then the eight warp sums are added in warp order; the
-  //     second pass adds its deltas to the first pass's sums.  Each item's weights are
-  //     exp(s - M_item); the sums are taken to the largest reference Mc of the pass (and
-  //     of the first pass's sums in round 1), a factor of exactly 1 for every item that
-  //     kept the head's reference.
-  const float M_prev = hsd.M;   // reference of the first pass's sums (round 1)
-  float Mc;
-  {
-    const float* P = (round == 0) ? V.part : V.part1;
-    float mloc = (round == 1) ? M_prev : -INFINITY;
-    for (int ch = tid; ch < nch; ch += BS_THREADS)
-      mloc = fmaxf(mloc, P[(((size_t)hs * NCH + ch) * MAXREP + r) * (D + 4) + D + 1]);
-    Mc = block_max(mloc, ws.red);
-  }
-  {
-    const int warp = tid >> 5, lane = tid & 31;
-    const float* P = (round == 0) ? V.part : V.part1;
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-    float l = 0.f;
-#pragma unroll 8
-    for (int ch = warp; ch < nch; ch += BS_WARPS) {
-      const size_t o = (((size_t)hs * NCH + ch) * MAXREP + r) * (D + 4);
-      const float Mi = P[o + D + 1];
-      const float w = (Mi == Mc) ? 1.f : expf(Mi - Mc);
-      const float4 x = *reinterpret_cast<const float4*>(P + o + 4 * lane);
-      a.x = fmaf(x.x, w, a.x); a.y = fmaf(x.y, w, a.y); a.z = fmaf(x.z, w, a.z); a.w = fmaf(x.w, w, a.w);
-      if (lane == 0) l = fmaf(P[o + D], w, l);
-    }
-    *reinterpret_cast<float4*>(&acc_s[warp][4 * lane]) = a;
-    if (lane == 0) l_s[warp] = l;
-  }
-  hsd.M = Mc;
-  const float w_prev = (round == 0 || M_prev == Mc) ? 1.f : expf(M_prev - Mc);
-  // (2) the partial FP16 block with exact scores
-  float lt = 0.f;
-  if (tid < V.n_tail) {
-    const float sc = dot_f16_row(V.q + hb * D, V.tail_k + ((size_t)hs * BLK + tid) * D);
-    lt = expf(sc * INV_SQRT_D - hsd.M);
-    tail_p[tid] = lt;
-  }
-  lt = block_sum(lt, ws.red);   // synchronises acc_s, l_s and tail_p too
+  // the pass's reference Mc: the largest of the warps' (and M_prev); lane l holds warp
+  // l mod 16's factor to it
+  const float mw = m_s[lane & 15];
+  const float Mc = fmaxf(M_prev, xw_max(mw));
+  const float fw = (mw == Mc) ? 1.f : expf(mw - Mc);
+  const float w_prev = (M_prev == Mc) ? 1.f : expf(M_prev - Mc);   // first-pass sums and tail
+  const float lt = (tl_s[0] + tl_s[1]) * w_prev;
   float* red = V.red0 + hb * (D + 4);
-  float L0 = (round == 1) ? red[D] * w_prev : 0.f;
-#pragma unroll
-  for (int w = 0; w < BS_WARPS; ++w) L0 += l_s[w];
+  float L0 = xw_sum(l_s[lane & 15] * fw);
+  if (round == 1) L0 += red[D] * w_prev;
   const float L = L0 + lt;
   if (round == 0 && tid == 0) red[D] = L0;
   if (tid < D) {
     float a = (round == 1) ? red[tid] * w_prev : 0.f;
 #pragma unroll
-    for (int w = 0; w < BS_WARPS; ++w) a += acc_s[w][tid];
+    for (int w = 0; w < BS_WARPS; ++w) a = fmaf(acc_s[w][tid], __shfl_sync(0xffffffffu, fw, w), a);
     if (round == 0) red[tid] = a;
+    float at = 0.f;
     for (int t = 0; t < V.n_tail; ++t)
-      a += tail_p[t] * __half2float(V.tail_v[((size_t)hs * BLK + t) * D + tid]);
+      at = fmaf(tail_p[t], __half2float(V.tail_v[((size_t)hs * BLK + t) * D + tid]), at);
+    a = fmaf(at, w_prev, a);
     V.out[hb * D + tid] = __float2half_rn(a / L);
   }
-  // value range R = max_c (vmax_c - vmin_c), reduced together with the certificate sums
-  float R = tid < D ? ord2f(V.vmax[hs * D + tid]) - ord2f(V.vmin[hs * D + tid]) : -INFINITY;
-  // (3) certificate
-  const float LSEp = hsd.M + logf(L);
+  hsd.M = Mc;
+  // (3) certificate; in the first pass also the first ranking position (the best selected
+  //     block by INT8 and by FP16 log-mass, ties to the lower index) and each block's
+  //     rung-2 weight mass_b eta_b (kept in `keys`, normalised if rung 2 is planned)
+  const float LSEp = Mc + logf(L);
   const float tail_mass = lt / L;
-  const float* lse8 = V.lse8 + hb * V.nbmax;
-  const float* lse16 = V.lse16 + hb * V.nbmax;
-  const float* dl = V.delta + hb * V.nbmax;
-  const float* eta = V.eta + (size_t)hs * V.nbmax;
   float S = 0.f, A = 0.f, Ev = 0.f;
-  // four blocks per thread and step (rows are padded to 16 blocks, 16-byte aligned)
-  for (int i4 = tid; i4 < (nb + 3) / 4; i4 += BS_THREADS) {
-    const uchar4 kf4 = reinterpret_cast<const uchar4*>(kfl)[i4];
-    const uchar4 vf4 = vfl ? reinterpret_cast<const uchar4*>(vfl)[i4] : make_uchar4(0, 0, 0, 0);
-    const float4 l8 = reinterpret_cast<const float4*>(lse8)[i4];
-    const float4 l16 = reinterpret_cast<const float4*>(lse16)[i4];
-    const float4 d4 = reinterpret_cast<const float4*>(dl)[i4];
-    const float4 e4 = reinterpret_cast<const float4*>(eta)[i4];
-    const unsigned char kf[4] = {kf4.x, kf4.y, kf4.z, kf4.w}, vf[4] = {vf4.x, vf4.y, vf4.z, vf4.w};
-    const float a8[4] = {l8.x, l8.y, l8.z, l8.w}, a16[4] = {l16.x, l16.y, l16.z, l16.w};
-    const float dd[4] = {d4.x, d4.y, d4.z, d4.w}, ee[4] = {e4.x, e4.y, e4.z, e4.w};
+  float b8 = -INFINITY, b16 = -INFINITY;
+  int i8 = 0x7fffffff, i16 = 0x7fffffff;
+  for (int i = i0; i < i1; i += 4) {
+    const BlockQuad q = (i == i0) ? q0 : load_quad(i);
+    const unsigned char kf[4] = {q.kf.x, q.kf.y, q.kf.z, q.kf.w}, vf[4] = {q.vf.x, q.vf.y, q.vf.z, q.vf.w};
+    const unsigned char sv[4] = {q.sl.x, q.sl.y, q.sl.z, q.sl.w};
+    const float a8[4] = {q.l8.x, q.l8.y, q.l8.z, q.l8.w}, a16[4] = {q.l16.x, q.l16.y, q.l16.z, q.l16.w};
+    const float dd[4] = {q.dl.x, q.dl.y, q.dl.z, q.dl.w}, ee[4] = {q.eta.x, q.eta.y, q.eta.z, q.eta.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      if (4 * i4 + j >= nb) break;
+      if (i + j >= i1) break;
       const bool kp = kf[j] != 0;
       const float pm = expf((kp ? a16[j] : a8[j]) - LSEp);
       if (kp) {
@@ -521,10 +598,44 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
         S += pm * expm1f(dd[j]);
         A += pm * expf(-dd[j]);
       }
-      if (!vf[j]) Ev += pm * ee[j];
+      const float pe = pm * ee[j];
+      if (!vf[j]) Ev += pe;
+      if (round == 0) keys[i + j] = __float_as_uint(pe);
+      if (sv[j]) {   // this thread's blocks are visited in ascending index order
+        if (a8[j] > b8 || (a8[j] == b8 && i + j < i8)) { b8 = a8[j]; i8 = i + j; }
+        if (a16[j] > b16 || (a16[j] == b16 && i + j < i16)) { b16 = a16[j]; i16 = i + j; }
+      }
     }
   }
-  block_max_sum3(R, S, A, Ev, ws.red);
+  // one cross-warp round: R (max), S, A, Ev (sums) and the two arg-maxima (largest value,
+  // then lowest index; value order by the order-preserving bits)
+  {
+    R = warp_max(R);
+    S = warp_sum(S);
+    A = warp_sum(A);
+    Ev = warp_sum(Ev);
+    uint32_t o8 = f2ord(b8), o16 = f2ord(b16);
+    o8 = __reduce_max_sync(0xffffffffu, o8);
+    o16 = __reduce_max_sync(0xffffffffu, o16);
+    i8 = (int)__reduce_min_sync(0xffffffffu, f2ord(b8) == o8 ? (unsigned)i8 : 0x7fffffffu);
+    i16 = (int)__reduce_min_sync(0xffffffffu, f2ord(b16) == o16 ? (unsigned)i16 : 0x7fffffffu);
+    if (lane == 0) {
+      cR[warp] = R; cS[warp] = S; cA[warp] = A; cE[warp] = Ev;
+      c8[warp] = o8; c16[warp] = o16; ci8[warp] = i8; ci16[warp] = i16;
+    }
+    __syncthreads();
+    const int l16 = lane & 15;
+    R = xw_max(cR[l16]);
+    S = xw_sum(cS[l16]);
+    A = xw_sum(cA[l16]);
+    Ev = xw_sum(cE[l16]);
+    o8 = __reduce_max_sync(0xffffffffu, c8[l16]);
+    o16 = __reduce_max_sync(0xffffffffu, c16[l16]);
+    i8 = (int)__reduce_min_sync(0xffffffffu, c8[l16] == o8 ? (unsigned)ci8[l16] : 0x7fffffffu);
+    i16 = (int)__reduce_min_sync(0xffffffffu, c16[l16] == o16 ? (unsigned)ci16[l16] : 0x7fffffffu);
+    b8 = ord2f(o8);
+    b16 = ord2f(o16);
+  }
   A += tail_mass;
   const float e_key = S / A * R;
   const float e_val = Ev;
@@ -541,16 +652,17 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
     }
     return;
   }
-  // (4) ranking-consistency check over S_h: top-R positions by INT8 and FP16 log-mass
-  const uint8_t* sel = V.sel + hb * V.nbmax;
+  // (4) ranking-consistency check over S_h: the top-R positions by INT8 and FP16 log-mass
+  //     (position 1 came with the certificate pass)
   bool ok = true;
   if (hsd.k_star > 1) {
-    float last8 = INFINITY, last16 = INFINITY;
-    int idx8 = -1, idx16 = -1;
+    ok = (i8 == i16);
+    float last8 = b8, last16 = b16;
+    int idx8 = i8, idx16 = i16;
     const int R_rank = min(V.rank_positions, hsd.k_star);
-    for (int pos = 0; pos < R_rank && ok; ++pos) {
-      float b8 = -INFINITY, b16 = -INFINITY;
-      int i8 = 0x7fffffff, i16 = 0x7fffffff;
+    for (int pos = 1; pos < R_rank && ok; ++pos) {
+      float c8v = -INFINITY, c16v = -INFINITY;
+      int j8 = 0x7fffffff, j16 = 0x7fffffff;
       for (int i4 = tid; i4 < (nb + 3) / 4; i4 += BS_THREADS) {
         const uchar4 s4 = reinterpret_cast<const uchar4*>(sel)[i4];
         if ((s4.x | s4.y | s4.z | s4.w) == 0) continue;
@@ -565,37 +677,34 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
           const float x8 = a8[j], x16 = a16[j];
           const bool after8 = (x8 < last8) || (x8 == last8 && i > idx8);
           const bool after16 = (x16 < last16) || (x16 == last16 && i > idx16);
-          if (after8 && (x8 > b8 || (x8 == b8 && i < i8))) { b8 = x8; i8 = i; }
-          if (after16 && (x16 > b16 || (x16 == b16 && i < i16))) { b16 = x16; i16 = i; }
+          if (after8 && (x8 > c8v || (x8 == c8v && i < j8))) { c8v = x8; j8 = i; }
+          if (after16 && (x16 > c16v || (x16 == c16v && i < j16))) { c16v = x16; j16 = i; }
         }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
-        const float ob8 = __shfl_xor_sync(0xffffffffu, b8, o);
-        const int oi8 = __shfl_xor_sync(0xffffffffu, i8, o);
-        if (ob8 > b8 || (ob8 == b8 && oi8 < i8)) { b8 = ob8; i8 = oi8; }
-        const float ob16 = __shfl_xor_sync(0xffffffffu, b16, o);
-        const int oi16 = __shfl_xor_sync(0xffffffffu, i16, o);
-        if (ob16 > b16 || (ob16 == b16 && oi16 < i16)) { b16 = ob16; i16 = oi16; }
+        const float ob8 = __shfl_xor_sync(0xffffffffu, c8v, o);
+        const int oi8 = __shfl_xor_sync(0xffffffffu, j8, o);
+        if (ob8 > c8v || (ob8 == c8v && oi8 < j8)) { c8v = ob8; j8 = oi8; }
+        const float ob16 = __shfl_xor_sync(0xffffffffu, c16v, o);
+        const int oi16 = __shfl_xor_sync(0xffffffffu, j16, o);
+        if (ob16 > c16v || (ob16 == c16v && oi16 < j16)) { c16v = ob16; j16 = oi16; }
       }
-      __syncthreads();
-      if ((tid & 31) == 0) {
-        ws.red.f[tid >> 5] = b8;
-        ws.red.i[tid >> 5] = i8;
-        ws.cidx[tid >> 5] = i16;
-        ws.ckey[tid >> 5] = __float_as_uint(b16);
+      __syncthreads();   // the previous position's slots have been read
+      if (lane == 0) {
+        cR[warp] = c8v; ci8[warp] = j8;
+        cS[warp] = c16v; ci16[warp] = j16;
       }
       __syncthreads();
       for (int w = 0; w < BS_WARPS; ++w) {
-        const float ob8 = ws.red.f[w], ob16 = __uint_as_float(ws.ckey[w]);
-        const int oi8 = ws.red.i[w], oi16 = ws.cidx[w];
-        if (ob8 > b8 || (ob8 == b8 && oi8 < i8)) { b8 = ob8; i8 = oi8; }
-        if (ob16 > b16 || (ob16 == b16 && oi16 < i16)) { b16 = ob16; i16 = oi16; }
+        const float ob8 = cR[w], ob16 = cS[w];
+        const int oi8 = ci8[w], oi16 = ci16[w];
+        if (ob8 > c8v || (ob8 == c8v && oi8 < j8)) { c8v = ob8; j8 = oi8; }
+        if (ob16 > c16v || (ob16 == c16v && oi16 < j16)) { c16v = ob16; j16 = oi16; }
       }
-      ok = (i8 == i16);
-      last8 = b8; idx8 = i8; last16 = b16; idx16 = i16;
+      ok = (j8 == j16);
+      last8 = c8v; idx8 = j8; last16 = c16v; idx16 = j16;
     }
-    __syncthreads();
   }
   if (V.debug & 0x1) ok = false;
   hsd.rank_ok = ok ? 1 : 0;
@@ -605,30 +714,29 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
   } else if (!(e_key + e_val <= V.eps && e_val <= V.v_tol)) {
     const float eps = V.eps;
     float S_proj = S;
+    bool keys_rung2 = true;   // keys still hold the certificate pass's mass_b eta_b
     uint8_t* k1 = V.kprom1 + (size_t)hs * V.nbmax;
     uint8_t* v1 = V.vprom1 + (size_t)hs * V.nbmax;
     if (e_key > eps * 0.5f) {
       planned = 1;
+      keys_rung2 = false;
       // rung 1: INT8 blocks by descending mass_b (e^Delta_b - 1) until the removed share
       // of S reaches 1 - eps A / (2 R S)
       const double need = 1.0 - (double)eps * (double)A / (2.0 * (double)R * (double)S);
-      for (int i4 = tid; i4 < (nb + 3) / 4; i4 += BS_THREADS) {   // four blocks per step
-        const uchar4 kf4 = reinterpret_cast<const uchar4*>(kfl)[i4];
-        const float4 l8 = reinterpret_cast<const float4*>(lse8)[i4];
-        const float4 d4 = reinterpret_cast<const float4*>(dl)[i4];
+      for (int i = i0; i < i1; i += 4) {
+        const uchar4 kf4 = reinterpret_cast<const uchar4*>(kfl)[i >> 2];
+        const float4 l8 = reinterpret_cast<const float4*>(lse8)[i >> 2];
+        const float4 d4 = reinterpret_cast<const float4*>(dl)[i >> 2];
         const unsigned char kf[4] = {kf4.x, kf4.y, kf4.z, kf4.w};
         const float a8[4] = {l8.x, l8.y, l8.z, l8.w}, dd[4] = {d4.x, d4.y, d4.z, d4.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          if (4 * i4 + j < nb)
-            keys[4 * i4 + j] = kf[j] ? 0u : __float_as_uint(expf(a8[j] - LSEp) * expm1f(dd[j]) / S);
+          if (i + j < i1)
+            keys[i + j] = kf[j] ? 0u : __float_as_uint(expf(a8[j] - LSEp) * expm1f(dd[j]) / S);
       }
-      __syncthreads();
-      unsigned long long taken = 0;
-      block_select_top(nb, keys, fixed62(need), [&](int i) { k1[i] = 1; }, ws, &taken);
-      S_proj = (float)((double)S * (1.0 - (double)taken / 4611686018427387904.0));
+      const SelResult sr = block_select_top(nb, fixed62(need), k1);
+      S_proj = (float)((double)S * (1.0 - (double)sr.taken / 4611686018427387904.0));
       if (S_proj < 0.f) S_proj = 0.f;
-      __syncthreads();
     }
     const float ekey_proj = S_proj / A * R;
     if (!(ekey_proj + e_val <= eps && e_val <= V.v_tol)) {
@@ -639,22 +747,26 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
         // are FP16 yet)
         const double target = fmin((double)eps - (double)ekey_proj, (double)V.v_tol);
         const double need = 1.0 - target / (double)e_val;
-        for (int i4 = tid; i4 < (nb + 3) / 4; i4 += BS_THREADS) {   // four blocks per step
-          const uchar4 kf4 = reinterpret_cast<const uchar4*>(kfl)[i4];
-          const float4 l8 = reinterpret_cast<const float4*>(lse8)[i4];
-          const float4 l16 = reinterpret_cast<const float4*>(lse16)[i4];
-          const float4 e4 = reinterpret_cast<const float4*>(eta)[i4];
-          const unsigned char kf[4] = {kf4.x, kf4.y, kf4.z, kf4.w};
-          const float a8[4] = {l8.x, l8.y, l8.z, l8.w}, a16[4] = {l16.x, l16.y, l16.z, l16.w};
-          const float ee[4] = {e4.x, e4.y, e4.z, e4.w};
+        for (int i = i0; i < i1; i += 4) {
+          if (keys_rung2) {
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            if (4 * i4 + j < nb)
-              keys[4 * i4 + j] = __float_as_uint(expf((kf[j] ? a16[j] : a8[j]) - LSEp) * ee[j] / e_val);
+            for (int j = 0; j < 4; ++j)
+              if (i + j < i1) keys[i + j] = __float_as_uint(__uint_as_float(keys[i + j]) / e_val);
+          } else {
+            const uchar4 kf4 = reinterpret_cast<const uchar4*>(kfl)[i >> 2];
+            const float4 l8 = reinterpret_cast<const float4*>(lse8)[i >> 2];
+            const float4 l16 = reinterpret_cast<const float4*>(lse16)[i >> 2];
+            const float4 e4 = reinterpret_cast<const float4*>(eta)[i >> 2];
+            const unsigned char kf[4] = {kf4.x, kf4.y, kf4.z, kf4.w};
+            const float a8[4] = {l8.x, l8.y, l8.z, l8.w}, a16[4] = {l16.x, l16.y, l16.z, l16.w};
+            const float ee[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (i + j < i1)
+                keys[i + j] = __float_as_uint(expf((kf[j] ? a16[j] : a8[j]) - LSEp) * ee[j] / e_val);
+          }
         }
-        __syncthreads();
-        unsigned long long taken = 0;
-        block_select_top(nb, keys, fixed62(need), [&](int i) { v1[i] = 1; }, ws, &taken);
+        block_select_top(nb, fixed62(need), v1);
       }
     }
     if (tid == 0 && planned > 0) {

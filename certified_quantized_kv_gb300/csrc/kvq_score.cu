@@ -251,13 +251,12 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
 __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
   pdl_trigger();
   pdl_wait();   // scores of the scoring pass
-  extern __shared__ __align__(16) unsigned char sel_dsm[];
-  BlockSelSmem& ws = *reinterpret_cast<BlockSelSmem*>(sel_dsm);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(sel_dsm + sizeof(BlockSelSmem));   // [nb padded]
-  float* xs = reinterpret_cast<float*>(keys);                                         // same storage
-  __shared__ float tail_s[BLK];
-  __shared__ int is_last;
-  const int tid = threadIdx.x;
+  BlockSelSmem& ws = sel_smem();
+  uint32_t* keys = sel_keys();                           // [nb padded]
+  float* xs = reinterpret_cast<float*>(keys);            // same storage: the log-masses first
+  __shared__ float wm[BS_WARPS], wsum[BS_WARPS], wtm[BS_WARPS], wtl[BS_WARPS];
+  __shared__ int is_last, ucnt;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int bh = blockIdx.x;
   const int b = bh / V.Hq, h = bh % V.Hq, g = h / V.n_rep;
   const int hs = b * V.Hkv + g;
@@ -266,35 +265,51 @@ __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
   if (!bounds_ok(V.counters, V.debug, nb, (long long)V.nbmax + 1, SITE_SELECT) ||
       !bounds_ok(V.counters, V.debug, hs, V.BG, SITE_SELECT))
     return;
-  // exact scores of the partial FP16 block (counts as covered)
-  float tmax = -INFINITY;
-  if (tid < V.n_tail) {
-    float sc = dot_f16_row(V.q + hb * D, V.tail_k + ((size_t)hs * BLK + tid) * D);
-    sc *= INV_SQRT_D;
-    tail_s[tid] = sc;
-    tmax = sc;
-  }
-  // block log-masses: staged in shared memory (16-byte loads; rows padded to 16 blocks)
+  // this thread's blocks: [i0, i1), log-masses staged in shared memory (16-byte loads;
+  // rows are padded to 16 blocks)
+  const int kpt = sel_kpt(nb);
+  const int i0 = min(nb, tid * kpt), i1 = min(nb, i0 + kpt);
   const float* lse8 = V.lse8 + hb * V.nbmax;
   float m = -INFINITY;
-  for (int i4 = tid; i4 < nbp / 4; i4 += BS_THREADS) {
-    const float4 x = reinterpret_cast<const float4*>(lse8)[i4];
+  for (int i = i0; i < i1; i += 4) {
+    const float4 x = reinterpret_cast<const float4*>(lse8)[i >> 2];
+    reinterpret_cast<float4*>(xs)[i >> 2] = x;
     const float xv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      if (4 * i4 + j < nb) m = fmaxf(m, xv[j]);
-    reinterpret_cast<float4*>(xs)[i4] = x;
+      if (i + j < i1) m = fmaxf(m, xv[j]);
   }
-  block_max2(m, tmax, ws.red);   // also makes tail_s and xs visible
+  // exact scores of the partial FP16 block (covered by definition): one score per thread
+  float sc = -INFINITY;
+  if (tid < V.n_tail)
+    sc = dot_f16_row(V.q + hb * D, V.tail_k + ((size_t)hs * BLK + tid) * D) * INV_SQRT_D;
+  float tm = -INFINITY;
+  // maxima and sums of exp(x - maximum), of the blocks and of the partial block: each warp
+  // sums against its own maximum (order-preserving bits, one reduction), and the warps'
+  // sums are moved to the block's maximum in one cross-warp round
+  m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(m)));
   float sp = 0.f;
-  for (int i = tid; i < nb; i += BS_THREADS) sp += expf(xs[i] - m);
-  float tl = tid < V.n_tail ? expf(tail_s[tid] - tmax) : 0.f;
-  block_sum2(sp, tl, ws.red);
-  const float tail_lse = V.n_tail > 0 ? tmax + logf(tl) : -INFINITY;
+  for (int i = i0; i < i1; ++i) sp += expf(xs[i] - m);
+  sp = warp_sum(sp);
+  float tl = 0.f;
+  if (warp < 2) {   // BLK <= 64 partial-block tokens
+    tm = ord2f(__reduce_max_sync(0xffffffffu, f2ord(sc)));
+    tl = warp_sum(tid < V.n_tail ? expf(sc - tm) : 0.f);
+  }
+  if (lane == 0) { wm[warp] = m; wsum[warp] = sp; wtm[warp] = tm; wtl[warp] = tl; }
+  __syncthreads();
+  {
+    const float mv = wm[lane & 15], tv = wtm[lane & 15];
+    m = ord2f(__reduce_max_sync(0xffffffffu, f2ord(mv)));
+    tm = ord2f(__reduce_max_sync(0xffffffffu, f2ord(tv)));
+    sp = xw_sum(mv == m ? wsum[lane & 15] : wsum[lane & 15] * expf(mv - m));
+    tl = xw_sum(tv == tm ? wtl[lane & 15] : wtl[lane & 15] * expf(tv - tm));
+  }
+  const float tail_lse = V.n_tail > 0 ? tm + logf(tl) : -INFINITY;
   // softmax reference of the passes that follow: >= every INT8 score (a block's log-mass
   // bounds its scores) and every partial-block score; a pass that meets a larger FP16
   // score raises its own reference
-  const float mref = fmaxf(m, tmax);
+  const float mref = fmaxf(m, tm);
   // log-sum-exp over the blocks (sum sp relative to m) and the partial block
   const float mm = fmaxf(m, tail_lse);
   float s = (nb > 0 ? sp * expf(m - mm) : 0.f) + (V.n_tail > 0 ? expf(tail_lse - mm) : 0.f);
@@ -304,17 +319,19 @@ __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
   unsigned long long target = 0ull;
   if (need > 0.0) target = (unsigned long long)ceil(need * 4611686018427387904.0);
   uint8_t* sel = V.sel + hb * V.nbmax;
+  // cleared before the selection's first barrier, marked after it
   for (int i16 = tid; i16 < nbp / 16; i16 += BS_THREADS) reinterpret_cast<uint4*>(sel)[i16] = make_uint4(0, 0, 0, 0);
-  for (int i = tid; i < nb; i += BS_THREADS) keys[i] = __float_as_uint(expf(xs[i] - LSE));   // mass
-  __syncthreads();
-  unsigned long long taken = 0;
-  const int kstar = block_select_top(nb, keys, target, [&](int i) { sel[i] = 1; }, ws, &taken);
+  for (int i = i0; i < i1; ++i) keys[i] = __float_as_uint(expf(xs[i] - LSE));   // mass
+  const SelResult sr = block_select_top(nb, target, sel);
+  // the last head of the group to finish forms the union (blocks whose FP16 keys are
+  // paged in); every mark of this head precedes the selection's closing barrier, and the
+  // padding bytes of every sel row are zero
   if (tid == 0) {
     HeadState hsd;
     hsd.M = mref;
     hsd.lse_int8 = LSE;
     hsd.tail_lse = tail_lse;
-    hsd.k_star = kstar;
+    hsd.k_star = sr.count;
     hsd.rank_ok = 1;
     hsd.planned = 0;
     hsd.level1 = 0;
@@ -324,11 +341,7 @@ __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
     hsd.n_vprom = 0;
     hsd.pad = 0;
     V.hst[hb] = hsd;
-  }
-  // the last head of the group to finish forms the union (blocks whose FP16 keys are
-  // paged in); the padding bytes of every sel row are zero
-  __syncthreads();
-  if (tid == 0) {
+    ucnt = 0;
     __threadfence();
     const unsigned int old = atomicAdd(&V.counters[CNT_GROUP_BASE + hs], 1u);
     is_last = (old == (unsigned int)(V.n_rep - 1));
@@ -348,16 +361,18 @@ __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
     reinterpret_cast<uint4*>(V.vprom1 + (size_t)hs * V.nbmax)[i16] = make_uint4(0, 0, 0, 0);
     cnt += __popc(u.x) + __popc(u.y) + __popc(u.z) + __popc(u.w);
   }
-  cnt = block_sum_int(cnt, ws.red);
+  cnt = (int)__reduce_add_sync(0xffffffffu, (unsigned)cnt);
+  if (lane == 0 && cnt) atomicAdd(&ucnt, cnt);
+  __syncthreads();
   if (tid == 0) {
     GroupState gs;
     gs.need_round1 = 0;
     gs.need_dense = 0;
-    gs.n_kprom0 = cnt;
-    gs.n_kprom1 = cnt;
+    gs.n_kprom0 = ucnt;
+    gs.n_kprom1 = ucnt;
     gs.n_vprom1 = 0;
     gs.pad = 0;
-    gs.bytes = (long long)cnt * F16_BLOCK_BYTES;
+    gs.bytes = (long long)ucnt * F16_BLOCK_BYTES;
     V.gst[hs] = gs;
     V.counters[CNT_GROUP_BASE + hs] = 0u;
   }
