@@ -66,11 +66,12 @@ __device__ __forceinline__ size_t head_row(const LayerView& V, int b, int g, int
   return (size_t)b * V.Hq + (size_t)g * V.n_rep + r;
 }
 
-__device__ __forceinline__ unsigned long long fixed62(double x) {
-  // x in [0, 1] -> x * 2^62 (rounded toward zero)
-  if (!(x > 0.0)) return 0ull;
-  if (x >= 1.0) return 4611686018427387904ull;
-  return (unsigned long long)(x * 4611686018427387904.0);
+__device__ __forceinline__ unsigned long long fixed62(float x) {
+  // x in [0, 1] -> x * 2^62 (rounded toward zero); the shares are formed in fp32, since
+  // FP64 is a narrow unit on this part and the inputs are fp32 sums
+  if (!(x > 0.f)) return 0ull;
+  if (x >= 1.f) return 1ull << 62;
+  return __float2ull_rz(x * 0x1p62f);
 }
 
 // Copy one FP16 block (64 x 128, 16 KiB) from tier 2 (or its resident copy) into shared
@@ -722,7 +723,7 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
       keys_rung2 = false;
       // rung 1: INT8 blocks by descending mass_b (e^Delta_b - 1) until the removed share
       // of S reaches 1 - eps A / (2 R S)
-      const double need = 1.0 - (double)eps * (double)A / (2.0 * (double)R * (double)S);
+      const float need = 1.f - eps * A / (2.f * R * S);
       for (int i = i0; i < i1; i += 4) {
         const uchar4 kf4 = reinterpret_cast<const uchar4*>(kfl)[i >> 2];
         const float4 l8 = reinterpret_cast<const float4*>(lse8)[i >> 2];
@@ -735,7 +736,7 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
             keys[i + j] = kf[j] ? 0u : __float_as_uint(expf(a8[j] - LSEp) * expm1f(dd[j]) / S);
       }
       const SelResult sr = block_select_top(nb, fixed62(need), k1);
-      S_proj = (float)((double)S * (1.0 - (double)sr.taken / 4611686018427387904.0));
+      S_proj = S * (1.f - __ull2float_rn(sr.taken) * 0x1p-62f);
       if (S_proj < 0.f) S_proj = 0.f;
     }
     const float ekey_proj = S_proj / A * R;
@@ -745,8 +746,8 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
         // rung 2: FP16 values by descending mass_b eta_b until the projected
         // E_key + E_val <= eps and E_val <= v_tol (every block is a candidate: no values
         // are FP16 yet)
-        const double target = fmin((double)eps - (double)ekey_proj, (double)V.v_tol);
-        const double need = 1.0 - target / (double)e_val;
+        const float target = fminf(eps - ekey_proj, V.v_tol);
+        const float need = 1.f - target / e_val;
         for (int i = i0; i < i1; i += 4) {
           if (keys_rung2) {
 #pragma unroll

@@ -314,10 +314,11 @@ __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
   const float mm = fmaxf(m, tail_lse);
   float s = (nb > 0 ? sp * expf(m - mm) : 0.f) + (V.n_tail > 0 ? expf(tail_lse - mm) : 0.f);
   const float LSE = mm + logf(s);
-  const double tail_mass = (V.n_tail > 0) ? (double)expf(tail_lse - LSE) : 0.0;
-  const double need = (double)V.tau - tail_mass;
+  // target weight ceil((tau - tail mass) 2^62), in fp32 (FP64 is a narrow unit here)
+  const float tail_mass = (V.n_tail > 0) ? expf(tail_lse - LSE) : 0.f;
+  const float need = V.tau - tail_mass;
   unsigned long long target = 0ull;
-  if (need > 0.0) target = (unsigned long long)ceil(need * 4611686018427387904.0);
+  if (need > 0.f) target = need >= 1.f ? (1ull << 62) : __float2ull_ru(need * 0x1p62f);
   uint8_t* sel = V.sel + hb * V.nbmax;
   // cleared before the selection's first barrier, marked after it
   for (int i16 = tid; i16 < nbp / 16; i16 += BS_THREADS) reinterpret_cast<uint4*>(sel)[i16] = make_uint4(0, 0, 0, 0);
