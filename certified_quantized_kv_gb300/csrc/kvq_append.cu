@@ -127,7 +127,19 @@ __global__ void __launch_bounds__(128, 5) append_kernel(AppendArgs a) {
     if (rb > 0) __syncthreads();   // the previous block is done with the staging buffers
 
     // ---- gather the block's FP16 tokens ----
-    if (VEC) {
+    if (VEC && t0 >= a.pos && rows == BLK) {
+      // a whole block of the caller's tokens: one base address per block
+      const __half* kp = a.k + ((size_t)hs * a.n + (size_t)(t0 - a.pos)) * D;
+      const __half* vp = a.v + ((size_t)hs * a.n + (size_t)(t0 - a.pos)) * D;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int i = tid + 128 * j, row = i >> 4, col = (i & 15) * 8;
+        cp_async16(&sk[row][col], kp + (size_t)i * 8);
+        cp_async16(&sv[row][svi(row, col)], vp + (size_t)i * 8);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+    } else if (VEC) {
       // straight into shared memory (cp.async): no registers held while the loads fly
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
