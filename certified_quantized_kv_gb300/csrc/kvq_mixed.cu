@@ -391,7 +391,10 @@ struct BlockQuad {
 // One CTA of BS_THREADS threads per (sequence, query head): combine the work-item partials
 // of a pass for the head, add the partial block, write the output and the certificate
 // and, after the first pass, run the ranking check and plan rungs 1-2.
-__global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int round) {
+// One instantiation per pass (`round`): each carries only its own code, which matters for a
+// kernel that runs once per head on an otherwise idle SM (cold instruction fetch).
+template <int round>
+__global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V) {
   pdl_trigger();
   pdl_wait();   // partials of the mixed pass
   BlockSelSmem& ws = sel_smem();
@@ -661,6 +664,7 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
     float last8 = b8, last16 = b16;
     int idx8 = i8, idx16 = i16;
     const int R_rank = min(V.rank_positions, hsd.k_star);
+#pragma unroll 1
     for (int pos = 1; pos < R_rank && ok; ++pos) {
       float c8v = -INFINITY, c16v = -INFINITY;
       int j8 = 0x7fffffff, j16 = 0x7fffffff;
@@ -724,6 +728,7 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V, int ro
       // rung 1: INT8 blocks by descending mass_b (e^Delta_b - 1) until the removed share
       // of S reaches 1 - eps A / (2 R S)
       const float need = 1.f - eps * A / (2.f * R * S);
+#pragma unroll 1
       for (int i = i0; i < i1; i += 4) {
         const uchar4 kf4 = reinterpret_cast<const uchar4*>(kfl)[i >> 2];
         const float4 l8 = reinterpret_cast<const float4*>(lse8)[i >> 2];
@@ -1192,9 +1197,10 @@ cudaError_t launch_mixed(const LayerView& V, int round, int grid, cudaStream_t s
 
 cudaError_t launch_combine(const LayerView& V, int round, cudaStream_t st) {
   const size_t dyn = sizeof(BlockSelSmem) + (size_t)((V.nb + 15) & ~15) * 4;
-  cudaError_t e = cudaFuncSetAttribute(combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+  auto* k = round == 0 ? combine_kernel<0> : combine_kernel<1>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
   if (e != cudaSuccess) return e;
-  return launch_dependent(combine_kernel, dim3(V.B * V.Hq), dim3(BS_THREADS), dyn, st, V, round);
+  return launch_dependent(k, dim3(V.B * V.Hq), dim3(BS_THREADS), dyn, st, V);
 }
 
 }  // namespace kvq
