@@ -9,15 +9,16 @@
 // the choice does not depend on summation order.
 //
 // Method: one block reduction gives the total weight, the number of candidates and the
-// smallest and largest candidate key (the first level's histograms are cleared meanwhile).  The threshold key is then narrowed by histogram
-// levels over the current key range [lo, hi], cut linearly into 1024 buckets (keys are
-// order-preserving fp32 bits, so this is a logarithmic cut of the values): each group of
-// warps accumulates its keys' weights into a private histogram, the groups' histograms
-// are summed, a block scan finds the bucket where the running weight from the top
-// reaches the target, and that bucket's key range becomes the next [lo, hi]; its keys are
-// gathered in the same pass that counts them.  Once it holds at most SEL_CAND keys they
-// are ranked exactly (one key value left: ties go to the lower indices).  Near-uniform
-// values usually need a single level.
+// smallest and largest candidate key (the first level's histograms are cleared
+// meanwhile).  The threshold key is then narrowed by histogram levels over the current
+// key range [lo, hi], cut linearly into 1024 buckets (keys are order-preserving fp32
+// bits, so this is a logarithmic cut of the values): each group of warps accumulates
+// its keys' weights into a private histogram, the warps' running totals of the summed
+// histograms locate the warp that holds the bucket where the weight from the top
+// reaches the target, that warp finds the bucket, and the bucket's key range becomes the
+// next [lo, hi]; its keys are gathered in the same pass that counts them.  Once it holds
+// at most SEL_CAND keys they are ranked exactly (one key value left: ties go to the lower
+// indices).  Near-uniform values usually need a single level.
 #pragma once
 
 #include "kvq_common.cuh"
@@ -32,96 +33,8 @@ static_assert(SEL_CAND <= BS_THREADS, "one thread per exactly ranked candidate")
 static_assert(BS_WARPS % BS_NHIST == 0 && 1024 % BS_THREADS == 0, "block shape");
 
 struct BlockRed {
-  float f[BS_WARPS];
-  float f1[BS_WARPS], f2[BS_WARPS], f3[BS_WARPS];
-  unsigned long long u[BS_WARPS];
-  int i[BS_WARPS];
+  unsigned long long u[BS_WARPS];   // per-warp totals of block_excl_scan_u64
 };
-
-// Several block reductions in one round of barriers: maxima of a and b (block_max2), or
-// the maximum of m and the sums of x, y, z (block_max_sum3).
-__device__ __forceinline__ void block_max2(float& a, float& b, BlockRed& r) {
-  a = warp_max(a);
-  b = warp_max(b);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) { r.f[threadIdx.x >> 5] = a; r.f1[threadIdx.x >> 5] = b; }
-  __syncthreads();
-  a = -INFINITY;
-  b = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < BS_WARPS; ++w) { a = fmaxf(a, r.f[w]); b = fmaxf(b, r.f1[w]); }
-}
-__device__ __forceinline__ void block_sum2(float& a, float& b, BlockRed& r) {
-  a = warp_sum(a);
-  b = warp_sum(b);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) { r.f[threadIdx.x >> 5] = a; r.f1[threadIdx.x >> 5] = b; }
-  __syncthreads();
-  a = 0.f;
-  b = 0.f;
-#pragma unroll
-  for (int w = 0; w < BS_WARPS; ++w) { a += r.f[w]; b += r.f1[w]; }
-}
-__device__ __forceinline__ void block_max_sum3(float& m, float& x, float& y, float& z, BlockRed& r) {
-  m = warp_max(m);
-  x = warp_sum(x);
-  y = warp_sum(y);
-  z = warp_sum(z);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) {
-    const int w = threadIdx.x >> 5;
-    r.f[w] = m; r.f1[w] = x; r.f2[w] = y; r.f3[w] = z;
-  }
-  __syncthreads();
-  m = -INFINITY;
-  x = y = z = 0.f;
-#pragma unroll
-  for (int w = 0; w < BS_WARPS; ++w) { m = fmaxf(m, r.f[w]); x += r.f1[w]; y += r.f2[w]; z += r.f3[w]; }
-}
-
-__device__ __forceinline__ float block_sum(float v, BlockRed& r) {
-  v = warp_sum(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) r.f[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float t = 0.f;
-#pragma unroll
-  for (int w = 0; w < BS_WARPS; ++w) t += r.f[w];
-  return t;
-}
-
-__device__ __forceinline__ float block_max(float v, BlockRed& r) {
-  v = warp_max(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) r.f[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float t = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < BS_WARPS; ++w) t = fmaxf(t, r.f[w]);
-  return t;
-}
-
-__device__ __forceinline__ unsigned long long block_sum_u64(unsigned long long v, BlockRed& r) {
-  v = warp_sum_u64(v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) r.u[threadIdx.x >> 5] = v;
-  __syncthreads();
-  unsigned long long t = 0;
-#pragma unroll
-  for (int w = 0; w < BS_WARPS; ++w) t += r.u[w];
-  return t;
-}
-
-__device__ __forceinline__ int block_sum_int(int v, BlockRed& r) {
-  v = (int)__reduce_add_sync(0xffffffffu, (unsigned)v);
-  __syncthreads();
-  if ((threadIdx.x & 31) == 0) r.i[threadIdx.x >> 5] = v;
-  __syncthreads();
-  int t = 0;
-#pragma unroll
-  for (int w = 0; w < BS_WARPS; ++w) t += r.i[w];
-  return t;
-}
 
 // Exclusive prefix sum over the block in thread order; *total = the block total.
 __device__ __forceinline__ unsigned long long block_excl_scan_u64(unsigned long long v, BlockRed& r,

@@ -397,8 +397,7 @@ template <int round>
 __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V) {
   pdl_trigger();
   pdl_wait();   // partials of the mixed pass
-  BlockSelSmem& ws = sel_smem();
-  uint32_t* keys = sel_keys();   // [nb padded]
+  uint32_t* keys = sel_keys();   // [nb padded], after the selection's workspace
   __shared__ __align__(16) float acc_s[BS_WARPS][D];
   __shared__ float l_s[BS_WARPS], m_s[BS_WARPS], tl_s[2];
   __shared__ float tail_p[BLK];

@@ -251,8 +251,7 @@ __global__ void __launch_bounds__(128, SCORE_CTAS_PER_SM) score_kernel(LayerView
 __global__ void __launch_bounds__(BS_THREADS) select_kernel(LayerView V) {
   pdl_trigger();
   pdl_wait();   // scores of the scoring pass
-  BlockSelSmem& ws = sel_smem();
-  uint32_t* keys = sel_keys();                           // [nb padded]
+  uint32_t* keys = sel_keys();                           // [nb padded], after the selection's workspace
   float* xs = reinterpret_cast<float*>(keys);            // same storage: the log-masses first
   __shared__ float wm[BS_WARPS], wsum[BS_WARPS], wtm[BS_WARPS], wtl[BS_WARPS];
   __shared__ int is_last, ucnt;
