@@ -27,7 +27,7 @@ namespace kvq {
 
 constexpr int BS_THREADS = 512;                   // per (sequence, head): latency-bound work
 constexpr int BS_WARPS = BS_THREADS / 32;
-constexpr int BS_NHIST = 8;                        // private histograms, BS_WARPS / BS_NHIST warps each
+constexpr int BS_NHIST = 4;                        // private histograms, BS_WARPS / BS_NHIST warps each
 constexpr int BS_BPT = 1024 / BS_THREADS;          // histogram buckets per thread in the scan
 static_assert(SEL_CAND <= BS_THREADS, "one thread per exactly ranked candidate");
 static_assert(BS_WARPS % BS_NHIST == 0 && 1024 % BS_THREADS == 0, "block shape");
@@ -337,24 +337,21 @@ static __device__ __noinline__ SelResult block_select_top(int n, unsigned long l
         const uint32_t ka = live ? ws.ckey[lane] : 0u;
         const int ia = live ? ws.cidx[lane] : 0x7fffffff;
         const unsigned long long wa = live ? key_weight(ka) : 0ull;
-        int rank = 0;
-        for (int j = 0; j < nc; ++j) {   // candidates before this one: key descending, index ascending
+        // weight of the candidates ranked before this one (key descending, index
+        // ascending); weights are non-negative, so a candidate is taken exactly when that
+        // weight is below the remainder, and the one whose running weight reaches it is
+        // the last taken
+        unsigned long long excl = 0ull, tot_c = 0ull;
+        for (int j = 0; j < nc; ++j) {
           const uint32_t kb = __shfl_sync(0xffffffffu, ka, j);
           const int ib = __shfl_sync(0xffffffffu, ia, j);
-          rank += (kb > ka) || (kb == ka && ib < ia);
-        }
-        unsigned long long excl = 0ull, tot_c = 0ull;   // weight of the candidates ranked before
-        for (int j = 0; j < nc; ++j) {
-          const int rb = __shfl_sync(0xffffffffu, rank, j);
           const unsigned long long wb = __shfl_sync(0xffffffffu, wa, j);
-          if (rb < rank) excl += wb;
+          if ((kb > ka) || (kb == ka && ib < ia)) excl += wb;
           tot_c += wb;
         }
-        // the candidate whose running weight first reaches the remainder is the last taken
         const unsigned crossing = __ballot_sync(0xffffffffu, live && excl < rem && excl + wa >= rem);
-        const int last = crossing ? __shfl_sync(0xffffffffu, rank, __ffs(crossing) - 1) : nc - 1;
         const unsigned long long tw = crossing ? __shfl_sync(0xffffffffu, excl + wa, __ffs(crossing) - 1) : tot_c;
-        if (live && rank <= last) { marks[ia] = 1; ++cnt; }
+        if (live && excl < rem) { marks[ia] = 1; ++cnt; }
         if (lane == 0) ws.take_w = tw;   // read after the closing barrier
       }
       small = true;
