@@ -381,9 +381,11 @@ kvq_status kvq_cache_create(const kvq_config* cfg, kvq_cache** out) {
 
   // ---- scratch ----
   const size_t HQ = (size_t)c->B * c->Hq;
-  // partial slots per group: enough for every split decode_split() can choose
+  // partial slots per group: enough for every split decode_split() can choose and for
+  // the INT4 value pass's runs (tail_runs), whichever asks for more
   const size_t target = (size_t)ITEMS_PER_CTA * mixed_grid(c->num_sms);
-  const size_t NCH = std::max(nbm / CHUNK + 1, (target + BG - 1) / BG + 1);
+  const size_t NCH = std::max({nbm / CHUNK + 1, (target + BG - 1) / BG + 1,
+                               (size_t)tail_runs(c->num_sms, (int)BG) + 1});
   c->nslot = (int)NCH;
   o = 0;
   const size_t s_shat = o;  o = align_up(o + HQ * nbm * BLK * 4, 256);
@@ -632,6 +634,8 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
   V.B = c->B; V.Hq = c->Hq; V.Hkv = c->Hkv; V.n_rep = c->n_rep; V.BG = c->BG;
   V.nb = N / BLK; V.n_tail = N % BLK; V.nbmax = c->nbmax; V.cap = c->cap;
   V.chunk = decode_split(c, V.nb); V.nslot = c->nslot; V.nparts = 0;
+  if (std::max(1, (V.nb + V.chunk - 1) / V.chunk) > V.nslot)
+    return fail(KVQ_ERR_INVALID, f + ": more work items per KV group than partial slots");
   V.kc = layer_kc(c, layer); V.ks = layer_ks(c, layer); V.vc = layer_vc(c, layer);
   V.vsv = layer_vsv(c, layer); V.eta = layer_eta(c, layer);
   V.vmin = layer_vmin(c, layer); V.vmax = layer_vmax(c, layer);
@@ -675,6 +679,7 @@ static kvq_status decode_impl(kvq_cache* c, int layer, const void* q, float tau,
     } else {
       // nothing is paged in: the INT4 value pass over every block, one partial per run
       const int runs = tail_runs(c->num_sms, V.BG);
+      if (runs > V.nslot) return fail(KVQ_ERR_INVALID, f + ": more INT4-pass runs than partial slots");
       KernelScope s(c, K_TAIL, st);
       KVQ_CUDA(s.done(launch_tail(V, runs, c->num_sms, st)), "int4_tail");
       V.nparts = runs;

@@ -36,7 +36,7 @@ constexpr int VC_BYTES = BLK * D / 2;      // 4096
 constexpr int VSV_WORDS = BLK * NG;        // 256 half2
 constexpr int F16_BLOCK_BYTES = BLK * D * 2;  // 16384 bytes of FP16 per block (K or V)
 constexpr int CHUNK = 16;        // most blocks per work item of the mixed and dense passes
-constexpr int ITEMS_PER_CTA = 4; // work items per resident CTA the split aims for
+constexpr int ITEMS_PER_CTA = 3; // work items per resident CTA the split aims for
 constexpr float KAPPA = 0.5f + 1.0f / 256.0f;
 constexpr float INV_SQRT_D = 0.088388347648318440550f;  // 1/sqrt(128), rounded to fp32
 
