@@ -13,7 +13,7 @@ Tolerances (stated once, used everywhere):
     exceeds 2e-3 above |x| = 4);
   * bounds: |gpu - oracle| <= BOUND_RTOL |oracle| + BOUND_ATOL;
   * coverage: at least MIN_STRICT_FRAC of the heads of every call are compared strictly
-    (level, ranking verdict and bounds), unless a test states a lower share and why.
+    (level, ranking-check outcome and bounds), unless a test states a lower share and why.
 """
 
 from __future__ import annotations
