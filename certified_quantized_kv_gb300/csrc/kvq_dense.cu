@@ -31,6 +31,8 @@ struct __align__(16) DenseSmem {
   float qf[MAXREP][D];
   float s[MAXREP][BLK];
   float red[MAXREP][4];
+  float cacc[4][D];         // final merge: each warp's sums for one head (channels)
+  float cml[4][2];          // ... and its reference and weight sum
   int item;
   int mask;
   int is_last;
@@ -70,36 +72,104 @@ __device__ void combine_dense(const LayerView& V, int hs, int mask, int all_dens
     }
   }
   __syncthreads();
-  // warp r combines head slot r's chunk partials (lane = four channels): the global max
-  // over the chunk maxima and the partial block, then the rescaled sums in chunk order
-  const int r = warp;
-  if (r < V.n_rep && (mask >> r & 1)) {
-    const int nchv = V.nb > 0 ? nch : 0;
+  const int nchv = V.nb > 0 ? nch : 0;
+  if (__popc(mask) == 1) {
+    // one dense head (rung 3): the four warps split its chunk partials (warp w takes
+    // chunks w, w + 4, ... in batches of eight; lane = four channels), each summing
+    // against its own running reference so that its loads go out together; thread =
+    // channel then adds the four warps' sums in warp order and the partial block's tokens
+    const int r = __ffs(mask) - 1;
     const float* P = V.dpart + ((size_t)hs * NCH * MAXREP + r) * (D + 4);   // chunk c at + c MAXREP (D + 4)
-    float M = -INFINITY;
-    for (int c = lane; c < nchv; c += 32) M = fmaxf(M, P[(size_t)c * MAXREP * (D + 4) + D]);
-    for (int t = lane; t < V.n_tail; t += 32) M = fmaxf(M, sm.s[r][t]);
-    M = warp_max(M);
-    float L = 0.f;
+    float Mw = -INFINITY, L = 0.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 16
-    for (int c = 0; c < nchv; ++c) {   // sixteen partials' loads in flight per lane
-      const float* pp = P + (size_t)c * MAXREP * (D + 4);
-      const float w = expf(pp[D] - M);
-      const float4 x = *reinterpret_cast<const float4*>(pp + 4 * lane);
-      L += pp[D + 1] * w;
-      a.x += x.x * w; a.y += x.y * w; a.z += x.z * w; a.w += x.w * w;
+    for (int base = warp; base < nchv; base += 4 * 8) {
+      float Mi[8], Li[8];
+      float4 x[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = base + 4 * j;
+        if (c < nchv) {
+          const float* pp = P + (size_t)c * MAXREP * (D + 4);
+          Mi[j] = pp[D];
+          Li[j] = pp[D + 1];
+          x[j] = *reinterpret_cast<const float4*>(pp + 4 * lane);
+        } else {
+          Mi[j] = -INFINITY;
+          Li[j] = 0.f;
+          x[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float Mb = Mw;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) Mb = fmaxf(Mb, Mi[j]);
+      if (Mb > Mw) {
+        const float f = expf(Mw - Mb);
+        a.x *= f; a.y *= f; a.z *= f; a.w *= f;
+        L *= f;
+        Mw = Mb;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        // a chunk at reference -inf still adds its sums (zero, or NaN from NaN inputs)
+        const float w = (Mi[j] == Mw) ? 1.f : expf(Mi[j] - Mw);
+        a.x = fmaf(x[j].x, w, a.x); a.y = fmaf(x[j].y, w, a.y);
+        a.z = fmaf(x[j].z, w, a.z); a.w = fmaf(x[j].w, w, a.w);
+        L = fmaf(Li[j], w, L);
+      }
+    }
+    *reinterpret_cast<float4*>(&sm.cacc[warp][4 * lane]) = a;
+    if (lane == 0) { sm.cml[warp][0] = Mw; sm.cml[warp][1] = L; }
+    __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, sm.cml[w][0]);
+    for (int t = 0; t < V.n_tail; ++t) M = fmaxf(M, sm.s[r][t]);
+    float acc = 0.f, Lt = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float mw = sm.cml[w][0];
+      const float f = (mw == -INFINITY) ? 0.f : expf(mw - M);
+      acc = fmaf(sm.cacc[w][tid], f, acc);
+      Lt = fmaf(sm.cml[w][1], f, Lt);
     }
     for (int t = 0; t < V.n_tail; ++t) {
       const float p = expf(sm.s[r][t] - M);
-      const uint2 vv = *reinterpret_cast<const uint2*>(V.tail_v + ((size_t)hs * BLK + t) * D + 4 * lane);
-      const float2 v01 = __half22float2(u32_as_h2(vv.x)), v23 = __half22float2(u32_as_h2(vv.y));
-      L += p;
-      a.x += p * v01.x; a.y += p * v01.y; a.z += p * v23.x; a.w += p * v23.y;
+      Lt += p;
+      acc = fmaf(p, __half2float(V.tail_v[((size_t)hs * BLK + t) * D + tid]), acc);
     }
-    __half2* o = reinterpret_cast<__half2*>(V.out + head_row(V, b, g, r) * D + 4 * lane);
-    o[0] = __floats2half2_rn(a.x / L, a.y / L);
-    o[1] = __floats2half2_rn(a.z / L, a.w / L);
+    V.out[head_row(V, b, g, r) * D + tid] = __float2half_rn(acc / Lt);
+  } else {
+    // several dense heads (rung 4): warp r combines head slot r's chunk partials (lane =
+    // four channels): the global max over the chunk maxima and the partial block, then
+    // the rescaled sums in chunk order
+    const int r = warp;
+    if (r < V.n_rep && (mask >> r & 1)) {
+      const float* P = V.dpart + ((size_t)hs * NCH * MAXREP + r) * (D + 4);   // chunk c at + c MAXREP (D + 4)
+      float M = -INFINITY;
+      for (int c = lane; c < nchv; c += 32) M = fmaxf(M, P[(size_t)c * MAXREP * (D + 4) + D]);
+      for (int t = lane; t < V.n_tail; t += 32) M = fmaxf(M, sm.s[r][t]);
+      M = warp_max(M);
+      float L = 0.f;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 16
+      for (int c = 0; c < nchv; ++c) {   // sixteen partials' loads in flight per lane
+        const float* pp = P + (size_t)c * MAXREP * (D + 4);
+        const float w = expf(pp[D] - M);
+        const float4 x = *reinterpret_cast<const float4*>(pp + 4 * lane);
+        L += pp[D + 1] * w;
+        a.x += x.x * w; a.y += x.y * w; a.z += x.z * w; a.w += x.w * w;
+      }
+      for (int t = 0; t < V.n_tail; ++t) {
+        const float p = expf(sm.s[r][t] - M);
+        const uint2 vv = *reinterpret_cast<const uint2*>(V.tail_v + ((size_t)hs * BLK + t) * D + 4 * lane);
+        const float2 v01 = __half22float2(u32_as_h2(vv.x)), v23 = __half22float2(u32_as_h2(vv.y));
+        L += p;
+        a.x += p * v01.x; a.y += p * v01.y; a.z += p * v23.x; a.w += p * v23.y;
+      }
+      __half2* o = reinterpret_cast<__half2*>(V.out + head_row(V, b, g, r) * D + 4 * lane);
+      o[0] = __floats2half2_rn(a.x / L, a.y / L);
+      o[1] = __floats2half2_rn(a.z / L, a.w / L);
+    }
   }
   __syncthreads();
   if (tid == 0) {

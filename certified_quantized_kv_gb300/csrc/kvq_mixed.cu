@@ -488,8 +488,7 @@ __global__ void __launch_bounds__(BS_THREADS) combine_kernel(LayerView V) {
         Mw = Mb;
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (Mi[j] == -INFINITY) continue;
+      for (int j = 0; j < 8; ++j) {   // a partial at reference -inf still adds its (zero or NaN) sums
         const float w = (Mi[j] == Mw) ? 1.f : expf(Mi[j] - Mw);
         a.x = fmaf(x[j].x, w, a.x); a.y = fmaf(x[j].y, w, a.y);
         a.z = fmaf(x[j].z, w, a.z); a.w = fmaf(x[j].w, w, a.w);
